@@ -1,0 +1,102 @@
+"""Planted mistakes in the oracle (CPU only): each must be caught by one of the pins.
+
+These show the pins are strong enough: a dropped term, a wrong sign, a transposed operand
+or a wrong owner index anywhere in the oracle makes at least one pin test fail.
+"""
+import numpy as np
+import pytest
+
+import test_oracle_collectives as tcol
+import test_oracle_gtp_ce_accounting as tgce
+import test_oracle_tp as ttp
+from oracle import collectives, gtp, numerics, tp_mlp, vocab_ce
+
+
+def _expect_failure(fn, *args):
+    with pytest.raises(AssertionError):
+        fn(*args)
+
+
+def test_dropped_term_in_gelu_derivative_is_caught(monkeypatch):
+    def bad(x):
+        x = np.asarray(x, dtype=np.float64)
+        u = numerics.SQRT_2_OVER_PI * (x + numerics.GELU_C * x ** 3)
+        return 0.5 * (1.0 + np.tanh(u))          # second product-rule term dropped
+    monkeypatch.setattr(numerics, "gelu_tanh_grad", bad)
+    monkeypatch.setattr(tp_mlp, "gelu_tanh_grad", bad)
+    _expect_failure(ttp.test_activation_derivatives_vs_autograd_and_finite_differences)
+    _expect_failure(ttp.test_backward_matches_finite_differences, "gelu_tanh")
+
+
+def test_wrong_swiglu_derivative_sign_is_caught(monkeypatch):
+    def bad(x):
+        s = numerics.sigmoid(x)
+        return s * (1.0 - np.asarray(x) * (1.0 - s))
+    monkeypatch.setattr(tp_mlp, "silu_grad", bad)
+    _expect_failure(ttp.test_backward_matches_finite_differences, "swiglu")
+
+
+def test_reversed_shard_ownership_is_caught(monkeypatch):
+    orig = tp_mlp.split_columns
+
+    def bad(W, t):
+        return orig(W, t)[::-1]
+    monkeypatch.setattr(tp_mlp, "split_columns", bad)
+    _expect_failure(ttp.test_column_parallel_t3_printed_table)
+
+
+def test_transposed_wgrad_operand_is_caught(monkeypatch):
+    def bad(X, W_shards, dY_shards):
+        X = np.asarray(X, float)
+        dW = [np.asarray(d, float).T @ X for d in dY_shards]      # dY^T X instead of X^T dY
+        pieces = [np.asarray(d, float) @ np.asarray(W, float).T for d, W in zip(dY_shards, W_shards)]
+        return dW, pieces, sum(pieces)
+    monkeypatch.setattr(tp_mlp, "column_parallel_backward", bad)
+    _expect_failure(ttp.test_column_parallel_t3_printed_table)
+
+
+def test_off_by_one_slab_owner_is_caught(monkeypatch):
+    orig = collectives.slab_rows
+
+    def bad(T, t, r):
+        return orig(T, t, (r + 1) % t)
+    monkeypatch.setattr(collectives, "slab_rows", bad)
+    _expect_failure(tcol.test_two_card_figure)
+
+
+def test_ce_combine_without_rescale_is_caught(monkeypatch):
+    def bad(stats):
+        ms = np.stack([s[0] for s in stats]); ss = np.stack([s[1] for s in stats])
+        ys = np.stack([s[2] for s in stats])
+        M = ms.max(axis=0); S = ss.sum(axis=0); zy = ys.sum(axis=0)   # forgot exp(m_i - M)
+        lt = np.log(S) + M - zy
+        return {"M": M, "S": S, "z_target": zy, "lse": M + np.log(S), "loss_tok": lt, "loss": lt.mean()}
+    monkeypatch.setattr(vocab_ce, "combine", bad)
+    _expect_failure(tgce.test_sharded_ce_equals_textbook_and_torch, 8)
+
+
+def test_gtp_reduce_scatter_wrong_block_is_caught(monkeypatch):
+    orig = gtp.wgrad_reduce_scatter
+
+    def bad(X, dY, g):
+        st = orig(X, dY, g)
+        return st[1:] + st[:1]
+    monkeypatch.setattr(gtp, "wgrad_reduce_scatter", bad)
+    _expect_failure(tgce.test_wgrad_reduce_scatter_equals_row_blocks_of_full_wgrad, 4)
+
+
+def test_finalize_not_deferred_is_caught(monkeypatch):
+    def bad(main_grad, staging):
+        mg = gtp.immediate_finalize(main_grad, staging)
+        L = len(staging)
+        return {"main_grad": mg, "updated_after_step": {l: list(range(l, L)) for l in range(L)}}
+    monkeypatch.setattr(gtp, "deferred_finalize", bad)
+    _expect_failure(tgce.test_deferred_finalize_visibility_and_result)
+
+
+def test_bf16_rounding_by_truncation_is_caught(monkeypatch):
+    def bad(x):
+        f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+        return ((f.view(np.uint32) >> 16) << 16).astype(np.uint32).view(np.float32)
+    monkeypatch.setattr(numerics, "round_to_bf16", bad)
+    _expect_failure(ttp.test_round_to_bf16_matches_torch_and_ties_to_even)
