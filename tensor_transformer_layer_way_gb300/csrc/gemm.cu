@@ -1,0 +1,615 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05) for sm_103a.
+//
+// One launch computes a list of problems (e.g. the t shards of a column-parallel layer,
+// or the t shards' dgrad and wgrad) so that the narrow per-shard GEMMs fill the GPU
+// together.  Each CTA owns one SM and walks the linearised tile list with a static
+// stride.  Roles (192 threads):
+//   warp 0      TMA producer: one thread issues cp.async.bulk.tensor loads of the A and B
+//               tiles of each 64-wide K block into a 4-stage shared-memory ring;
+//   warp 1      MMA issuer: allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//               and one thread issues tcgen05.mma (M=128, N=256, K=16) per K step;
+//   warps 2..5  epilogue: tcgen05.ld the accumulator rows, apply the fused op (bias,
+//               GeLU, SwiGLU, their derivatives) and store bf16/fp32 to global memory.
+// The accumulator is double-buffered, so the epilogue of tile n overlaps the MMAs of
+// tile n+1.  Every mbarrier wait is bounded in wall time; a timeout records
+// TTL_ERR_TIMEOUT, all roles leave their loops, in-flight copies and MMAs are waited
+// for (again bounded), TMEM is released and the kernel returns.
+//
+// Shared-memory operand layouts (128-byte swizzle, 1024-byte aligned stages):
+//   K-major operand  : box {64 K, 128 rows}; row r at r*128 B; 8-row atoms 1024 B apart
+//                      (SBO = 1024).  K step of 16 = +32 B on the descriptor start.
+//   MN-major operand : boxes {64 MN, 64 K} side by side 8 KiB apart (LBO = 8192);
+//                      K row k at k*128 B (SBO = 1024).  K step of 16 = +2048 B.
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ttl_device.cuh"
+#include "ttl_internal.h"
+
+namespace ttl {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;           // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;           // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;                    // two accumulators
+constexpr int GROUP_M = 16;
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+static_assert(sizeof(GemmParams) <= 32764, "kernel parameter block beyond the 32 KiB limit");
+static_assert(SMEM_BYTES <= 232448, "shared memory beyond the per-CTA limit");
+
+struct TileCoord {
+  int p, tm, tn;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile) {
+  int p = 0;
+#pragma unroll 1
+  while (p + 1 < P.nprob && tile >= P.probs[p + 1].tile_start) ++p;
+  const Problem& pr = P.probs[p];
+  const int local = tile - pr.tile_start;
+  const int per_group = GROUP_M * pr.tiles_n;
+  const int group = local / per_group;
+  const int first_m = group * GROUP_M;
+  const int gm = min(GROUP_M, pr.tiles_m - first_m);
+  const int r = local - group * per_group;
+  TileCoord c;
+  c.p = p;
+  c.tm = first_m + r % gm;
+  c.tn = r / gm;
+  return c;
+}
+
+// ------------------------------------------------------------------ epilogue math
+
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+
+__device__ __forceinline__ float gelu_tanh_grad_f(float x) {
+  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+  const float th = tanhf(u);
+  const float du = 0.7978845608028654f * (1.0f + 3.0f * 0.044715f * x * x);
+  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// Stores 32 consecutive bf16 values of one row (columns col0..col0+31), masking at N.
+__device__ __forceinline__ void store_row32_bf16(void* base, int64_t ld, int row, int col0, int N,
+                                                 const float* v) {
+  __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + static_cast<int64_t>(row) * ld + col0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (col0 + q * 8 < N) {
+      uint4 w;
+      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      *reinterpret_cast<uint4*>(p + q * 8) = w;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_row32_f32(void* base, int64_t ld, int row, int col0, int N,
+                                                const float* v) {
+  float* p = reinterpret_cast<float*>(base) + static_cast<int64_t>(row) * ld + col0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (col0 + q * 4 < N) {
+      *reinterpret_cast<float4*>(p + q * 4) = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void load_row32_bf16(const void* base, int64_t ld, int row, int col0, int N, float* v) {
+  const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(base) + static_cast<int64_t>(row) * ld + col0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (col0 + q * 8 < N) w = *reinterpret_cast<const uint4*>(p + q * 8);
+    v[q * 8 + 0] = bf16_lo(w.x);
+    v[q * 8 + 1] = bf16_hi(w.x);
+    v[q * 8 + 2] = bf16_lo(w.y);
+    v[q * 8 + 3] = bf16_hi(w.y);
+    v[q * 8 + 4] = bf16_lo(w.z);
+    v[q * 8 + 5] = bf16_hi(w.z);
+    v[q * 8 + 6] = bf16_lo(w.w);
+    v[q * 8 + 7] = bf16_hi(w.w);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Stages must sit on 1024-byte boundaries for the 128-byte swizzle atoms.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* done_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    for (int i = lane; i < P.nmaps; i += 32) tma_prefetch_map(&P.maps[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int* status = P.status;
+  const uint64_t tmo = P.timeout_ns;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+        const TileCoord c = decode_tile(P, tile);
+        const Problem& pr = P.probs[c.p];
+        const int am = pr.a_m0 + c.tm * BM;
+        for (int s = 0; ok && s < pr.nseg; ++s) {
+          const Seg& sg = pr.seg[s];
+          const CUtensorMap* ma = &P.maps[sg.map_a];
+          const CUtensorMap* mb0 = &P.maps[sg.map_b];
+          const CUtensorMap* mb1 = pr.paired ? &P.maps[sg.map_b2] : mb0;
+          const int bn0 = pr.paired ? pr.b_n0 + c.tn * (BN / 2) : pr.b_n0 + c.tn * BN;
+          const int bn1 = pr.paired ? bn0 : bn0 + BN / 2;
+          for (int kb = 0; kb < sg.kblocks; ++kb) {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, status, tmo)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sa = smem + stage * STAGE_BYTES;
+            uint8_t* sb = sa + A_STAGE_BYTES;
+            mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+            const int ka = sg.a_k0 + kb * BK;
+            const int kbb = sg.b_k0 + kb * BK;
+            if (!pr.a_mn) {
+              tma_load_2d(sa, ma, &full_bar[stage], ka, am);
+            } else {
+              tma_load_2d(sa, ma, &full_bar[stage], am, ka);
+              tma_load_2d(sa + 8192, ma, &full_bar[stage], am + 64, ka);
+            }
+            if (!pr.b_mn) {
+              tma_load_2d(sb, mb0, &full_bar[stage], kbb, bn0);
+              tma_load_2d(sb + 16384, mb1, &full_bar[stage], kbb, bn1);
+            } else {
+              tma_load_2d(sb, mb0, &full_bar[stage], bn0, kbb);
+              tma_load_2d(sb + 8192, mb0, &full_bar[stage], bn0 + 64, kbb);
+              tma_load_2d(sb + 16384, mb1, &full_bar[stage], bn1, kbb);
+              tma_load_2d(sb + 24576, mb1, &full_bar[stage], bn1 + 64, kbb);
+            }
+            ++issued;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Make sure no copy is still landing in shared memory when the CTA leaves: wait for
+      // the completion of the last min(issued, STAGES) loads (bounded).
+      const int pending = issued < STAGES ? issued : STAGES;
+      int s = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < pending; ++i) {
+        if (--s < 0) {
+          s = STAGES - 1;
+          ph ^= 1u;
+        }
+        int dummy_abort = 0;
+        mbar_wait(&full_bar[s], ph, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t sbase = smem_u32(smem);
+      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+        const TileCoord c = decode_tile(P, tile);
+        const Problem& pr = P.probs[c.p];
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, status, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t idesc = idesc_bf16_f32(BM, BN, pr.a_mn != 0, pr.b_mn != 0);
+        const uint32_t a_step = pr.a_mn ? 2048u : 32u;
+        const uint32_t b_step = pr.b_mn ? 2048u : 32u;
+        const uint32_t a_lbo = pr.a_mn ? 8192u : 16u;
+        const uint32_t b_lbo = pr.b_mn ? 8192u : 16u;
+        uint32_t accumulate = 0;
+        for (int s = 0; ok && s < pr.nseg; ++s) {
+          const int nkb = pr.seg[s].kblocks;
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait(&full_bar[stage], phase, abort_flag, status, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t adesc = smem_desc_sw128(sa + kk * a_step, a_lbo, 1024);
+              const uint64_t bdesc = smem_desc_sw128(sb + kk * b_step, b_lbo, 1024);
+              umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+              accumulate = 1;
+            }
+            umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs issued by this thread must finish before TMEM is released.
+      umma_commit(done_bar);
+      int dummy_abort = 0;
+      mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue warps
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
+      const TileCoord c = decode_tile(P, tile);
+      const Problem& pr = P.probs[c.p];
+      const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after_sync();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int row = c.tm * BM + row_in_tile;
+      const bool row_ok = row < pr.M;
+      const int epi = pr.epi;
+      if (pr.paired) {
+        const int n_base = c.tn * (BN / 2);
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 2 / 32; ++ch) {
+          uint32_t g[32], u[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tbase + ch * 32, g);
+          tmem_ld_32x32b_x32(tbase + BN / 2 + ch * 32, u);
+          tmem_ld_wait();
+          const int col0 = n_base + ch * 32;
+          if (row_ok && col0 < pr.N) {
+            float gv[32], uv[32], hv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              gv[j] = __uint_as_float(g[j]);
+              uv[j] = __uint_as_float(u[j]);
+              hv[j] = gv[j] * sigmoid_f(gv[j]) * uv[j];
+            }
+            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, gv);
+            store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, uv);
+            store_row32_bf16(pr.out2, pr.ld_out, row, col0, pr.N, hv);
+          }
+        }
+      } else {
+        const int n_base = c.tn * BN;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tbase + ch * 32, r);
+          tmem_ld_wait();
+          const int col0 = n_base + ch * 32;
+          if (row_ok && col0 < pr.N) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          if (epi == EPI_F32) {
+            store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
+          } else if (epi == EPI_BF16 || epi == EPI_GELU_FWD) {
+            if (pr.bias0) {
+              float b[32];
+              load_row32_bf16(pr.bias0, 0, 0, col0, pr.N, b);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += b[j];
+            }
+            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+            if (epi == EPI_GELU_FWD) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j]);
+              store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
+            }
+          } else if (epi == EPI_GELU_BWD) {
+            float x[32];
+            load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(x[j]);
+            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+          } else if (epi == EPI_SWIGLU_BWD) {
+            float gg[32], vv[32], dg[32];
+            load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, gg);
+            load_row32_bf16(pr.aux1, pr.ld_aux, row, col0, pr.N, vv);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float s = sigmoid_f(gg[j]);
+              dg[j] = v[j] * vv[j] * s * (1.0f + gg[j] * (1.0f - s));
+              v[j] = v[j] * gg[j] * s;
+            }
+            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, dg);
+            store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
+          }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
+
+// The driver's tensor-map encoder, looked up through the runtime so that the library does
+// not link libcuda (it then loads on machines without a driver, e.g. for symbol checks).
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int smem_attr_set(int device) {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) return set_error(TTL_ERR_CUDA, "device index out of range");
+  if (!done[device]) {
+    int rc = cuda_check(cudaFuncSetAttribute(gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES),
+                        "cudaFuncSetAttribute(gemm smem)");
+    if (rc) return rc;
+    done[device] = true;
+  }
+  return TTL_OK;
+}
+
+}  // namespace
+
+GemmBatch::GemmBatch() : p_(new GemmParams), nmaps_(0), err_(TTL_OK), flops_(0.0), bytes_(0.0) {
+  std::memset(static_cast<void*>(p_), 0, sizeof(GemmParams));
+}
+
+GemmBatch::~GemmBatch() { delete p_; }
+
+int GemmBatch::add_map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool mn_major) {
+  if (err_) return -1;
+  if (nmaps_ >= kMaxMaps) {
+    err_ = set_error(TTL_ERR_ARG, "GEMM batch: too many operands (max %d)", kMaxMaps);
+    return -1;
+  }
+  if (!aligned16(ptr) || (ld * 2) % 16 != 0 || cols % 8 != 0) {
+    err_ = set_error(TTL_ERR_ALIGN, "GEMM operand %p: pointer, row stride (%lld) and width (%lld) must be 16-byte aligned",
+                     ptr, (long long)ld, (long long)cols);
+    return -1;
+  }
+  if (rows <= 0 || cols <= 0) {
+    err_ = set_error(TTL_ERR_SHAPE, "GEMM operand with empty extent");
+    return -1;
+  }
+  for (int i = 0; i < nmaps_; ++i) {
+    const MapKey& k = keys_[i];
+    if (k.ptr == ptr && k.rows == rows && k.cols == cols && k.ld == ld && k.mn == mn_major) return i;
+  }
+  keys_[nmaps_] = MapKey{ptr, rows, cols, ld, mn_major};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, mn_major ? 64u : 128u};
+  cuuint32_t estr[2] = {1, 1};
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) {
+    err_ = set_error(TTL_ERR_CUDA, "cuTensorMapEncodeTiled not available from the CUDA driver");
+    return -1;
+  }
+  CUresult r = enc(&p_->maps[nmaps_], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    err_ = cu_check(r, "cuTensorMapEncodeTiled");
+    return -1;
+  }
+  return nmaps_++;
+}
+
+Problem* GemmBatch::add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired) {
+  if (err_) return nullptr;
+  if (p_->nprob >= kMaxProblems) {
+    err_ = set_error(TTL_ERR_ARG, "GEMM batch: too many problems (max %d)", kMaxProblems);
+    return nullptr;
+  }
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) {
+    err_ = set_error(TTL_ERR_SHAPE, "GEMM extent beyond 2^31");
+    return nullptr;
+  }
+  Problem* p = &p_->probs[p_->nprob++];
+  std::memset(static_cast<void*>(p), 0, sizeof(Problem));
+  p->M = static_cast<int32_t>(M);
+  p->N = static_cast<int32_t>(N);
+  p->a_mn = a_mn;
+  p->b_mn = b_mn;
+  p->epi = static_cast<uint8_t>(epi);
+  p->paired = paired;
+  return p;
+}
+
+int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K) {
+  if (err_) return err_;
+  if (!p || map_a < 0 || map_b < 0 || (p->paired && map_b2 < 0)) return err_ = set_error(TTL_ERR_ARG, "bad GEMM segment");
+  if (p->nseg >= kMaxSegs) return err_ = set_error(TTL_ERR_ARG, "GEMM problem: too many K segments");
+  if (K <= 0) return err_ = set_error(TTL_ERR_SHAPE, "GEMM segment with empty K");
+  Seg& s = p->seg[p->nseg++];
+  s.map_a = static_cast<int16_t>(map_a);
+  s.map_b = static_cast<int16_t>(map_b);
+  s.map_b2 = static_cast<int16_t>(map_b2 < 0 ? map_b : map_b2);
+  s.a_k0 = static_cast<int32_t>(a_k0);
+  s.b_k0 = static_cast<int32_t>(b_k0);
+  s.kblocks = static_cast<int32_t>((K + BK - 1) / BK);
+  const double ncols = p->paired ? 2.0 * p->N : static_cast<double>(p->N);
+  flops_ += 2.0 * p->M * ncols * static_cast<double>(K);
+  bytes_ += 2.0 * (static_cast<double>(p->M) * K + ncols * K);
+  if (p->nseg == 1) {
+    const int nout = p->epi == EPI_SWIGLU_FWD ? 3 : (p->epi == EPI_GELU_FWD || p->epi == EPI_SWIGLU_BWD) ? 2 : 1;
+    const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : p->epi == EPI_GELU_BWD ? 1 : 0;
+    const double esz = p->epi == EPI_F32 ? 4.0 : 2.0;
+    bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux);
+  }
+  return TTL_OK;
+}
+
+int GemmBatch::flush(cudaStream_t stream) {
+  if (err_) return err_;
+  const int rc = p_->nprob ? launch(stream) : TTL_OK;
+  std::memset(static_cast<void*>(p_), 0, sizeof(GemmParams));
+  nmaps_ = 0;
+  flops_ = 0.0;
+  bytes_ = 0.0;
+  return rc;
+}
+
+int GemmBatch::launch(cudaStream_t stream) {
+  if (err_) return err_;
+  int total = 0;
+  for (int i = 0; i < p_->nprob; ++i) {
+    Problem& p = p_->probs[i];
+    if (p.nseg == 0) return set_error(TTL_ERR_ARG, "GEMM problem %d has no K segment", i);
+    // Every TMA x coordinate (innermost, in elements) must be a multiple of 8 bf16 = 16 bytes.
+    bool aligned = (p.a_m0 % 8 == 0) && (p.b_n0 % 8 == 0);
+    for (int k = 0; k < p.nseg; ++k) aligned = aligned && p.seg[k].a_k0 % 8 == 0 && p.seg[k].b_k0 % 8 == 0;
+    if (!aligned) return set_error(TTL_ERR_ALIGN, "GEMM problem %d: operand offsets must be multiples of 8", i);
+    const int tn = p.paired ? BN / 2 : BN;
+    p.tiles_m = (p.M + BM - 1) / BM;
+    p.tiles_n = (p.N + tn - 1) / tn;
+    p.tile_start = total;
+    total += p.tiles_m * p.tiles_n;
+  }
+  p_->total_tiles = total;
+  p_->nmaps = nmaps_;
+  if (total == 0) return TTL_OK;
+  int rc = require_sm103();
+  if (rc) return rc;
+  int dev = 0;
+  if ((rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
+  if ((rc = smem_attr_set(dev))) return rc;
+  p_->status = device_status_ptr();
+  if (!p_->status) return TTL_ERR_CUDA;
+  p_->timeout_ns = 2000000000ull;  // 2 s per wait: far beyond any legitimate stall
+  const int grid = total < num_sms() ? total : num_sms();
+  TraceScope trace(stream, TTL_K_GEMM, flops_, bytes_);
+  gemm_tcgen05_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(*p_);
+  return cuda_check(cudaGetLastError(), "gemm_tcgen05_kernel launch");
+}
+
+}  // namespace ttl
+
+// ------------------------------------------------------------------ C entry point
+
+extern "C" int ttl_gemm(int64_t M, int64_t N, int64_t K, const ttl_bf16* A, int64_t lda, int a_kmajor,
+                        const ttl_bf16* B, int64_t ldb, int b_kmajor, void* D, int64_t ldd, int d_fp32,
+                        void* stream) {
+  using namespace ttl;
+  if (M < 0 || N < 0 || K < 0) return set_error(TTL_ERR_ARG, "ttl_gemm: negative extent");
+  if (M == 0 || N == 0) return TTL_OK;
+  if (!D) return set_error(TTL_ERR_ARG, "ttl_gemm: null D");
+  if (N % 8 || K % 8) return set_error(TTL_ERR_SHAPE, "ttl_gemm: N and K must be multiples of 8");
+  if (!aligned16(D) || (ldd * (d_fp32 ? 4 : 2)) % 16) return set_error(TTL_ERR_ALIGN, "ttl_gemm: D not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K > 0 && (!A || !B)) return set_error(TTL_ERR_ARG, "ttl_gemm: null operand");
+  if (K == 0) {
+    // Empty contraction: D = 0.
+    if (ldd == N) return fill_zero(D, static_cast<size_t>(M * N) * (d_fp32 ? 4 : 2), s);
+    for (int64_t r = 0; r < M; ++r) {
+      int rc = fill_zero(static_cast<char*>(D) + r * ldd * (d_fp32 ? 4 : 2), N * (d_fp32 ? 4 : 2), s);
+      if (rc) return rc;
+    }
+    return TTL_OK;
+  }
+  GemmBatch b;
+  const int ma = a_kmajor ? b.add_map(A, M, K, lda, false) : b.add_map(A, K, M, lda, true);
+  const int mb = b_kmajor ? b.add_map(B, N, K, ldb, false) : b.add_map(B, K, N, ldb, true);
+  Problem* p = b.add_problem(M, N, !a_kmajor, !b_kmajor, d_fp32 ? EPI_F32 : EPI_BF16, false);
+  if (b.error()) return b.error();
+  p->out0 = D;
+  p->ld_out = ldd;
+  b.add_seg(p, ma, 0, mb, -1, 0, K);
+  return b.launch(s);
+}

@@ -1,0 +1,150 @@
+// Internal declarations shared by the library's translation units (host side) and the
+// GEMM problem description that crosses into the kernel as a parameter block.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ttl.h"
+
+namespace ttl {
+
+constexpr int kMaxShards = TTL_MAX_SHARDS;
+
+// ------------------------------------------------------------------ errors
+
+// Records a formatted message for ttl_last_error() and returns `code`.
+int set_error(int code, const char* fmt, ...);
+// TTL_OK if e == cudaSuccess, else records the CUDA error string.
+int cuda_check(cudaError_t e, const char* what);
+// TTL_OK if r == CUDA_SUCCESS, else records the driver error.
+int cu_check(CUresult r, const char* what);
+
+// Device address of the current device's status word (looked up once per device).
+int* device_status_ptr();
+// Multiprocessor count of the current device (cached per device).
+int num_sms();
+// TTL_OK if the current device is sm_103 (compute capability 10.3).
+int require_sm103();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch tracing (no-ops unless ttl_trace_enable(1, ...) was called).  trace_begin records
+// the start event on `s` and returns a slot (or -1); trace_end records the stop event.
+int trace_begin(cudaStream_t s);
+void trace_end(int slot, cudaStream_t s, int kind, double flops, double bytes);
+
+// RAII helper: brackets one launch.
+struct TraceScope {
+  int slot;
+  cudaStream_t s;
+  int kind;
+  double flops, bytes;
+  TraceScope(cudaStream_t st, int k, double f, double b) : slot(trace_begin(st)), s(st), kind(k), flops(f), bytes(b) {}
+  ~TraceScope() { trace_end(slot, s, kind, flops, bytes); }
+};
+
+// ------------------------------------------------------------------ GEMM problem block
+
+constexpr int kMaxMaps = 40;
+constexpr int kMaxProblems = 32;
+constexpr int kMaxSegs = kMaxShards;
+
+enum Epilogue : int {
+  EPI_BF16 = 0,        // out0 = bf16(acc + bias0[n])
+  EPI_F32 = 1,         // out0 = acc (fp32)
+  EPI_GELU_FWD = 2,    // out0 = U = bf16(acc + bias0[n]); out1 = bf16(GeLU(acc + bias0[n]))
+  EPI_SWIGLU_FWD = 3,  // paired tile: out0 = G, out1 = V, out2 = SiLU(G) * V
+  EPI_GELU_BWD = 4,    // out0 = bf16(acc * GeLU'(aux0))                          (dU)
+  EPI_SWIGLU_BWD = 5,  // out0 = bf16(acc * aux1 * SiLU'(aux0)), out1 = bf16(acc * SiLU(aux0))
+};
+
+// One K-range of a problem: k-blocks of 64 read from map_a at K offset a_k0 and from
+// map_b (and, for a paired tile, map_b2) at K offset b_k0.
+struct Seg {
+  int16_t map_a, map_b, map_b2, pad;
+  int32_t a_k0, b_k0, kblocks, pad2;
+};
+
+// One output matrix [M, N]; tiles of 128 rows x 256 accumulator columns.  A paired tile
+// (SwiGLU forward) covers 128 output columns: accumulator columns [0,128) come from
+// map_b and [128,256) from map_b2 at the same N coordinates.
+struct Problem {
+  int32_t M, N;
+  int32_t tiles_m, tiles_n;
+  int32_t tile_start;     // first linear tile index of this problem
+  int32_t a_m0, b_n0;     // offsets added to the M coordinate of A and N coordinate of B
+  uint8_t a_mn, b_mn;     // 1 = operand stored MN-major (A as [K,M], B as [K,N])
+  uint8_t epi, nseg;
+  uint8_t paired, pad[3];
+  Seg seg[kMaxSegs];
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* aux0;
+  const void* aux1;
+  const void* bias0;
+  int64_t ld_out;         // row stride (elements) of out0/out1/out2
+  int64_t ld_aux;         // row stride (elements) of aux0/aux1
+};
+
+struct GemmParams {
+  CUtensorMap maps[kMaxMaps];
+  Problem probs[kMaxProblems];
+  int32_t nprob;
+  int32_t total_tiles;
+  int32_t nmaps;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+// Host-side builder: collects tensor maps and problems, then launches the persistent
+// tcgen05 GEMM kernel once for all of them.
+class GemmBatch {
+ public:
+  GemmBatch();
+  ~GemmBatch();
+  // Registers a bf16 operand stored row-major [rows, cols] with row stride `ld` elements.
+  // mn_major selects the 64x64 box of an MN-major operand; otherwise the 64x128 box of a
+  // K-major one.  Returns the map index or -1 (error recorded).
+  int add_map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool mn_major);
+  // Adds a problem and returns it (nullptr if the batch is full).  Segments are appended
+  // with add_seg(); tile counts are filled in by launch().
+  Problem* add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired);
+  int add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K);
+  int launch(cudaStream_t stream);
+  int error() const { return err_; }
+  // True if `maps` more operands and `probs` more problems still fit in this launch.
+  bool has_room(int maps, int probs) const {
+    return nmaps_ + maps <= kMaxMaps && p_->nprob + probs <= kMaxProblems;
+  }
+  // Launches what has been collected (if anything) and starts an empty batch.
+  int flush(cudaStream_t stream);
+
+ private:
+  struct MapKey {
+    const void* ptr;
+    int64_t rows, cols, ld;
+    bool mn;
+  };
+  GemmParams* p_;
+  MapKey keys_[kMaxMaps];
+  int nmaps_;
+  int err_;
+  double flops_;   // algorithmic FLOPs of the collected problems (2 M N K each)
+  double bytes_;   // operand bytes read once + output bytes written once
+};
+
+// Zero-fill helper (used where a contraction is empty).
+int fill_zero(void* ptr, size_t bytes, cudaStream_t stream);
+
+// Column sums of a [rows, cols] bf16 matrix (row stride ld) into bf16 [cols].
+int column_sum_bf16(const void* x, int64_t rows, int64_t cols, int64_t ld, void* out, cudaStream_t s);
+
+// In-place all-reduce over t shard buffers (validated like ttl_shard_all_reduce).
+int shard_all_reduce_internal(int t, int64_t rows, int64_t cols, ttl_bf16* const* bufs, const ttl_bf16* bias,
+                              cudaStream_t s);
+
+}  // namespace ttl

@@ -1,0 +1,82 @@
+"""Vocab-parallel LM head + cross-entropy vs the oracle (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as si
+import tensor_transformer_layer_way_gb300 as ttl
+from oracle import vocab_ce
+from parity import assert_fp32_close, assert_gemm_close, dev, f32, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(H, W, target, t, flags=0):
+    Ws = dev([w.contiguous() for w in W.chunk(t, 0)])
+    out = ttl.vocab_parallel_ce(dev(H), Ws, dev(target), flags=flags)
+    return out
+
+
+@pytest.mark.parametrize("t,T,h,V", [(1, 64, 64, 512), (4, 100, 64, 4 * 296), (8, 130, 136, 8 * 48)])
+def test_small_full_parity(t, T, h, V):
+    inp = si.ce_inputs(T, h, V, seed=t + T)
+    out = _run(inp["H"], inp["W"], inp["target"], t)
+    assert ttl.device_status() == 0
+    ref = vocab_ce.vocab_parallel_ce(f64(inp["H"]), f64(inp["W"]), inp["target"].numpy(), t)
+    Vs = V // t
+    stats = f32(out["stats"]).reshape(3 * t + 2, T)
+    for i in range(t):
+        assert_fp32_close(f32(out["logits"][i]), ref["Z"][i], f"logits[{i}]")
+        assert_fp32_close(stats[3 * i], ref["stats"][i][0], f"max[{i}]")
+        assert_fp32_close(stats[3 * i + 1], ref["stats"][i][1], f"sumexp[{i}]")
+        assert_fp32_close(stats[3 * i + 2], ref["stats"][i][2], f"target logit[{i}]")
+        assert_gemm_close(f64(out["dlogits"][i]), ref["dZ"][i], f"dlogits[{i}]")
+    assert_fp32_close(stats[3 * t], ref["lse"], "lse")
+    assert_fp32_close(stats[3 * t + 1], ref["loss_tok"], "loss per token")
+    assert abs(out["loss"].item() - ref["loss"]) <= 1e-5 * abs(ref["loss"])
+    assert_gemm_close(f64(out["dH"]), ref["dH"], "dH")
+    del Vs
+
+
+def test_fp32_dlogits_in_place_and_forward_only():
+    t, T, h, V = 2, 64, 64, 2 * 136
+    inp = si.ce_inputs(T, h, V, seed=1)
+    out = _run(inp["H"], inp["W"], inp["target"], t, flags=ttl.CE_FP32_DLOGITS)
+    ref = vocab_ce.vocab_parallel_ce(f64(inp["H"]), f64(inp["W"]), inp["target"].numpy(), t)
+    for i in range(t):
+        assert_fp32_close(f32(out["logits"][i]), ref["dZ"][i], f"fp32 dlogits[{i}]", rel=1e-5)
+    fo = _run(inp["H"], inp["W"], inp["target"], t, flags=ttl.CE_FORWARD_ONLY)
+    assert abs(fo["loss"].item() - ref["loss"]) <= 1e-5 * abs(ref["loss"])
+
+
+def test_all_zero_logits_give_log_v():
+    t, T, h, V = 8, 32, 64, 8 * 64
+    H = torch.zeros((T, h), dtype=torch.bfloat16)
+    W = si.randn_bf16(si.generator(0), (V, h))
+    target = torch.randint(0, V, (T,), generator=si.generator(1))
+    out = _run(H, W, target, t, flags=ttl.CE_FP32_DLOGITS)
+    assert abs(out["loss"].item() - np.log(V)) <= 1e-5 * np.log(V)
+    # fp32 dlogits: each row sums to zero up to fp32 rounding of V terms
+    dZ32 = torch.cat(out["logits"], 1).double()
+    assert dZ32.sum(1).abs().max().item() <= 1e-6 / T
+    # bf16 dlogits: the target entry (1/V - 1)/T carries one bf16 rounding (2^-9 relative)
+    dZ = torch.cat([d.double() for d in out["dlogits"]], 1)
+    assert dZ.sum(1).abs().max().item() <= 2.0 ** -8 / T
+
+
+def test_vocab_parallel_ce_full_size_sampled():
+    """H [8192, 4096], W [151936, 4096] in 8 vocab shards of 18992 rows (fp32 logits 4.98 GB)."""
+    cfg = si.VOCAB_CE_T8
+    inp = si.ce_inputs(cfg.T, cfg.h, cfg.V, cfg.seed)
+    out = _run(inp["H"], inp["W"], inp["target"], cfg.t)
+    assert ttl.device_status() == 0
+    rows = si.sample_indices(cfg.T, 48, cfg.seed).numpy()
+    ref = vocab_ce.vocab_parallel_ce(f64(inp["H"]), f64(inp["W"]), inp["target"].numpy(), cfg.t, rows=rows)
+    stats = f32(out["stats"]).reshape(3 * cfg.t + 2, cfg.T)
+    assert_fp32_close(stats[3 * cfg.t + 1][rows], ref["loss_tok"], "loss per token (sampled rows)")
+    loss_tok = stats[3 * cfg.t + 1].astype(np.float64)
+    assert abs(out["loss"].item() - loss_tok.mean()) <= 1e-5 * abs(loss_tok.mean())
+    r = torch.as_tensor(rows).cuda()
+    for i in (0, cfg.t - 1):
+        assert_gemm_close(f64(out["dlogits"][i][r]), ref["dZ"][i], f"dlogits[{i}] rows")
+    assert_gemm_close(f64(out["dH"][r]), ref["dH"], "dH rows")
