@@ -1,0 +1,499 @@
+#!/usr/bin/env python
+"""Benchmark of the tensor-parallel block hot path on GB300.
+
+Headline (``value``): TP-sharded MLP forward + backward TFLOP/s on the Qwen3-8B-shaped
+SwiGLU block with t = 8 logical shards on one GPU: X [8192, 4096], gate/up [4096, 12288]
+in 1536-column shards, down [12288, 4096] in 1536-row shards.  One step is
+ttl_tp_mlp_fwd + ttl_tp_mlp_bwd: fc1 (SwiGLU fused), fc2 partials, the g all-reduce,
+fc2 dgrad (SwiGLU' fused), every weight gradient, the dX partials and the f all-reduce.
+Algorithmic work: 9 GEMMs of 2*8192*4096*12288 FLOPs = 7.422 TFLOP per step.
+
+The same run measures the other rows of the path on their own workloads:
+  shard_reduce  reduce-scatter / all-gather / all-reduce of t in {2,4,8,16} bf16 partial
+                sums [4096, 8192] (64 MiB each), HBM GB/s with L2 flushed before each launch;
+  gtp_chain     8-layer GTP_remat chain (TP slice [8192, 2048] as 8 shards of 4 MiB,
+                X [4096, 8192]): warm forward with side-stream prefetch, backward with
+                prefetch, wgrad reduce-scatter and one-layer-deferred finalize;
+  vocab_ce      LM head [151936, 4096] in 8 vocab shards + cross-entropy on 8192 tokens.
+
+``--impl reference`` times the CPU oracle (the reference arm of this build) on a bounded
+sample of the same workload.  Inputs are synthetic (seeded), drawn on the device for our
+arm and on the host for the oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TP-sharded MLP fwd+bwd TFLOP/s (% BF16 peak); shard-reduce HBM GB/s"
+MLP = dict(t=8, T=8192, h=4096, f=12288, act="swiglu", seed=3)
+MLP_FLOPS = 9 * 2.0 * MLP["T"] * MLP["h"] * MLP["f"]
+WORKLOAD = "qwen3_8b_swiglu_mlp_t8_T8192_h4096_f12288_fwd_bwd"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-components", action="store_true", help="skip the shard_reduce/gtp/ce legs")
+    ap.add_argument("--cpu-tokens", type=int, default=256, help="token rows of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+class Dist:
+    def __init__(self, want: int):
+        import torch
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+        if want != self.world and self.rank == 0:
+            print(f"# note: --gpus {want} but WORLD_SIZE={self.world}; using WORLD_SIZE", file=sys.stderr)
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks and peaks
+
+class Clocks:
+    """nvidia-smi sampled every 100 ms while running; summarised into the JSON line."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait(timeout=5)
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def committed_traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "tensor_transformer_layer_way_gb300", "csrc", d["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return d["bytes_per_launch"] if h == d.get("source_sha256_16") else None
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, dist):
+    import torch
+    import tensor_transformer_layer_way_gb300 as ttl
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    pk = peaks()
+    t, T, h, f, act = MLP["t"], MLP["T"], MLP["h"], MLP["f"], MLP["act"]
+    fs = f // t
+    g = torch.Generator(device=dev).manual_seed(MLP["seed"] + 1000 * dist.rank)
+
+    def rnd(shape, std):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    X, dY = rnd((T, h), 1.0), rnd((T, h), 1.0)
+    Wg = [rnd((h, fs), 0.02) for _ in range(t)]
+    Wu = [rnd((h, fs), 0.02) for _ in range(t)]
+    Wd = [rnd((fs, h), 0.02) for _ in range(t)]
+    fo = ttl.mlp_fwd_buffers(t, act, T, h, f, dev)
+    bo = ttl.mlp_bwd_buffers(t, act, T, h, f, dev)
+
+    def step():
+        ttl.tp_mlp_fwd(X, Wg, Wd, act=act, A_up=Wu, out=fo)
+        ttl.tp_mlp_bwd(X, dY, Wg, Wd, fo, act=act, A_up=Wu, out=bo)
+
+    # Clocks are sampled from the start of the warm-up to the end of the timed region, so a
+    # short timed region still has samples under load.
+    clocks = Clocks(dist.local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ttl.device_status() != 0:
+        raise RuntimeError("device status set during warm-up: " + ttl.last_error())
+
+    dist.barrier()
+    torch.cuda.synchronize()
+    ttl.trace_enable(True, 1 << 16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    recs = ttl.trace_read(1 << 16)
+    ttl.trace_enable(False)
+    if ttl.device_status() != 0:
+        raise RuntimeError("device status set during the timed region: " + ttl.last_error())
+    ms_max = dist.max(ms)
+    value = dist.world * MLP_FLOPS * args.steps / (ms_max * 1e-3) / 1e12
+
+    gemm = [r for r in recs if r[0] == "gemm"]
+    red = [r for r in recs if r[0] == "reduce"]
+    g_ms = sum(r[1] for r in gemm)
+    g_fl = sum(r[2] for r in gemm)
+    achieved = g_fl / (g_ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": "gemm_tcgen05_kernel", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)",
+                "traffic": committed_traffic("gemm_tcgen05_kernel"),
+                "launches_per_step": len(gemm) / args.steps,
+                "flops_per_launch": g_fl / max(len(gemm), 1),
+                "avg_launch_ms": g_ms / max(len(gemm), 1),
+                "share_of_step": round(g_ms / ms, 4)}
+    r_ms = sum(r[1] for r in red)
+    r_by = sum(r[3] for r in red)
+    allreduce = {"kernel": "shard_reduce_kernel<8,AR>", "achieved_gbs": round(r_by / (r_ms * 1e-3) / 1e9, 1),
+                 "peak_gbs": pk["hbm_gbs"], "frac": round(r_by / (r_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                 "share_of_step": round(r_ms / ms, 4)}
+
+    # End to end through the public API with host buffers: inputs copied in from pinned host
+    # memory and the step's results (Z and dX, one copy each) copied back, every step.
+    Xh = X.cpu().pin_memory()
+    dYh = dY.cpu().pin_memory()
+    Zh = torch.empty((T, h), dtype=torch.bfloat16).pin_memory()
+    dXh = torch.empty((T, h), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        X.copy_(Xh, non_blocking=True)
+        dY.copy_(dYh, non_blocking=True)
+        step()
+        Zh.copy_(fo["Z"][0], non_blocking=True)
+        dXh.copy_(bo["dX"][0], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_ms = dist.max(e0.elapsed_time(e1))
+    e2e = {"value": round(dist.world * MLP_FLOPS * args.steps / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": 2 * T * h * 2, "d2h_bytes_per_step": 2 * T * h * 2,
+           "ms_per_step": round(e2e_ms / args.steps, 4)}
+    del fo, bo, Xh, dYh, Zh, dXh
+    torch.cuda.empty_cache()
+
+    comps = {}
+    if not args.no_components:
+        comps["shard_reduce"] = bench_shard_reduce(ttl, torch, dev, pk, args)
+        comps["gtp_chain"] = bench_gtp(ttl, torch, dev, pk, args)
+        comps["vocab_ce"] = bench_ce(ttl, torch, dev, pk, args)
+
+    out = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": dist.world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded randn drawn on the device, Qwen3-8B MLP shapes)",
+           "config": {"workload": WORKLOAD, "t": t, "tokens": T, "h": h, "ffn": f, "act": act,
+                      "parallelism": f"{dist.world} independent replica(s), t={t} logical shards each",
+                      "l2": "working set larger than L2 (288 MiB of weights + 1.5 GiB of activations); no flush"},
+           "pct_of_bf16_peak": round(value / dist.world / peak, 4),
+           "roofline": roofline, "allreduce_in_step": allreduce,
+           "e2e": e2e, "gpu_launches": len(recs), "clocks": clk}
+    out.update(comps)
+    return out
+
+
+def _flush(torch, buf):
+    buf.add_(1)  # writes the whole buffer (larger than L2)
+
+
+def bench_shard_reduce(ttl, torch, dev, pk, args):
+    T, h = 4096, 8192
+    g = torch.Generator(device=dev).manual_seed(2)
+    flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    res = {"workload": "partial_sum_reduce_T4096_h8192", "bytes_model": "RS (t+1)S, AG tS, AR 2tS; S = 64 MiB",
+           "l2": "flushed by a 512 MiB write before each timed launch", "peak_gbs": pk["hbm_gbs"]}
+    reps = max(5, min(args.steps, 20))
+    for t in (2, 4, 8, 16):
+        bufs = [torch.randn((T, h), generator=g, device=dev).to(torch.bfloat16) for _ in range(t)]
+        row = {}
+        for mode, fn, kind in (("rs", ttl.shard_reduce_scatter, "reduce"), ("ag", ttl.shard_all_gather, "gather"),
+                               ("ar", ttl.shard_all_reduce, "reduce")):
+            for _ in range(2):
+                fn(bufs)
+            ttl.trace_enable(True, 1024)
+            for _ in range(reps):
+                _flush(torch, flush)
+                fn(bufs)
+            torch.cuda.synchronize()
+            recs = [r for r in ttl.trace_read(1024) if r[0] == kind]
+            ttl.trace_enable(False)
+            ms = sum(r[1] for r in recs) / len(recs)
+            by = recs[0][3]
+            gbs = by / (ms * 1e-3) / 1e9
+            row[mode] = {"gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "us": round(ms * 1e3, 1)}
+        res[f"t{t}"] = row
+        del bufs
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_gtp(ttl, torch, dev, pk, args):
+    L, K, N, M, gdeg = 8, 8192, 2048, 4096, 8
+    g = torch.Generator(device=dev).manual_seed(4)
+    X = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+    shards = [[(torch.randn((K // gdeg, N), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+               for _ in range(gdeg)] for _ in range(L)]
+    dY = [torch.randn((M, N), generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+    Y = [torch.empty((M, N), device=dev, dtype=torch.bfloat16) for _ in range(L)]
+    dX = torch.empty((M, K), device=dev, dtype=torch.bfloat16)
+    slots = [torch.empty((K, N), device=dev, dtype=torch.bfloat16) for _ in range(2)]
+    staging = [[torch.empty((K // gdeg, N), device=dev) for _ in range(gdeg)] for _ in range(L)]
+    main_grad = [[torch.zeros((K // gdeg, N), device=dev) for _ in range(gdeg)] for _ in range(L)]
+    from tensor_transformer_layer_way_gb300 import chain
+    runner = chain.GtpChain(ttl, torch, shards, slots)
+
+    def fwd_bwd(folded=False):
+        runner.forward(X, Y, folded=folded)
+        runner.backward(X, dY, dX, staging, main_grad, folded=folded)
+
+    runner.forward(X, Y, cold=True)           # cold start: every first gather synchronous
+    for _ in range(2):
+        fwd_bwd()
+    torch.cuda.synchronize()
+    res = {"workload": "gtp_chain_L8_h8192_tp4_g8_T4096", "gemm_flops_per_pass": 3 * L * 2.0 * M * K * N}
+    for folded in (False, True):
+        ttl.trace_enable(True, 1 << 14)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        e0.record()
+        for _ in range(reps):
+            fwd_bwd(folded)
+        e1.record()
+        torch.cuda.synchronize()
+        wall = e0.elapsed_time(e1) / reps
+        recs = ttl.trace_read(1 << 14)
+        ttl.trace_enable(False)
+        gm = [r for r in recs if r[0] == "gemm"]
+        ga = [r for r in recs if r[0] == "gtp_gather"]
+        fi = [r for r in recs if r[0] == "finalize"]
+        gemm_ms = sum(r[1] for r in gm) / reps
+        key = "folded" if folded else "slot_prefetch"
+        res[key] = {"ms_per_fwd_bwd": round(wall, 3),
+                    "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
+                    "gemm_ms": round(gemm_ms, 3),
+                    "exposed_ms": round(wall - gemm_ms - sum(r[1] for r in fi) / reps, 3),
+                    "finalize_gbs": round(sum(r[3] for r in fi) / (sum(r[1] for r in fi) * 1e-3) / 1e9, 1) if fi else None}
+        if ga:
+            res[key]["gather_gbs"] = round(sum(r[3] for r in ga) / (sum(r[1] for r in ga) * 1e-3) / 1e9, 1)
+    res["peak_tflops"] = pk["bf16_tflops_sustained"]
+    res["peak_gbs"] = pk["hbm_gbs"]
+    del X, shards, dY, Y, dX, slots, staging, main_grad, runner
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_ce(ttl, torch, dev, pk, args):
+    t, T, h, V = 8, 8192, 4096, 151936
+    g = torch.Generator(device=dev).manual_seed(5)
+    H = torch.randn((T, h), generator=g, device=dev).to(torch.bfloat16)
+    W = [(torch.randn((V // t, h), generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(t)]
+    target = torch.randint(0, V, (T,), generator=g, device=dev)
+    out = ttl.ce_buffers(t, T, h, V, dev)
+    for _ in range(2):
+        ttl.vocab_parallel_ce(H, W, target, out=out)
+    torch.cuda.synchronize()
+    reps = 3
+    ttl.trace_enable(True, 4096)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ttl.vocab_parallel_ce(H, W, target, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    recs = ttl.trace_read(4096)
+    ttl.trace_enable(False)
+    wall = e0.elapsed_time(e1) / reps
+
+    def agg(kind, flops=False):
+        rr = [r for r in recs if r[0] == kind]
+        if not rr:
+            return None
+        ms = sum(r[1] for r in rr)
+        if flops:
+            v = sum(r[2] for r in rr) / (ms * 1e-3) / 1e12
+            return {"tflops": round(v, 1), "frac": round(v / pk["bf16_tflops_sustained"], 4),
+                    "ms": round(ms / reps, 3)}
+        v = sum(r[3] for r in rr) / (ms * 1e-3) / 1e9
+        return {"gbs": round(v, 1), "frac": round(v / pk["hbm_gbs"], 4), "ms": round(ms / reps, 3)}
+
+    res = {"workload": "vocab_parallel_ce_t8_T8192_h4096_V151936", "ms_per_fwd_bwd": round(wall, 3),
+           "loss": float(out["loss"].item()), "gemm": agg("gemm", True), "stats": agg("ce_stats"),
+           "dlogits": agg("ce_dlogits"), "combine_mean": agg("ce_small")}
+    del H, W, target, out
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)
+
+def oracle_sample(tokens: int):
+    import numpy as np
+    import synth_inputs as si
+    g = si.generator(MLP["seed"])
+    X = si.randn_bf16(g, (tokens, MLP["h"])).float().numpy().astype(np.float64)
+    W = {k: si.randn_bf16(g, s, 0.02).float().numpy().astype(np.float64)
+         for k, s in (("Wg", (MLP["h"], MLP["f"])), ("Wu", (MLP["h"], MLP["f"])), ("Wd", (MLP["f"], MLP["h"])))}
+    dY = si.randn_bf16(g, (tokens, MLP["h"])).float().numpy().astype(np.float64)
+    return X, W, dY
+
+
+def time_oracle(tokens: int, reps: int, warm: int = 0):
+    from oracle import tp_mlp
+    X, W, dY = oracle_sample(tokens)
+    times = []
+    for i in range(warm + reps):
+        t0 = time.perf_counter()
+        fwd = tp_mlp.tp_mlp_forward(X, W, MLP["t"], MLP["act"])
+        tp_mlp.tp_mlp_backward(X, W, MLP["t"], MLP["act"], dY, fwd)
+        if i >= warm:
+            times.append(time.perf_counter() - t0)
+    flops = MLP_FLOPS * tokens / MLP["T"]
+    return flops, times
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(tokens: int) -> dict:
+    flops, times = time_oracle(tokens, 1)
+    return {"value": round(flops / times[0] / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, sharded t=8 SwiGLU MLP fwd+bwd on {tokens} of 8192 tokens "
+                      f"(full weights), {times[0]:.2f} s"}
+
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return None
+    tokens = args.cpu_tokens
+    flops, times = time_oracle(tokens, args.steps, args.warmup)
+    total = sum(times)
+    v = flops * args.steps / total / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "TFLOP/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "t": 8, "tokens_per_step": tokens},
+            "cpu_baseline": {"value": round(v, 5), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{tokens} of 8192 tokens per step, full weights"},
+            "e2e": {"value": round(v, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            out = run_reference(args, dist)
+        else:
+            out = run_ours(args, dist)
+            if dist.rank == 0 and not args.no_cpu_baseline:
+                out["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+        if dist.rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -138,3 +138,51 @@ def test_full_size_chain_layer_sampled():
     full_rows = (Xs[:, kr].T @ dYs)           # rows kr of X^T dY, every token
     got = np.stack([f32(staging[k // (K // g)][k % (K // g)]) for k in kr.tolist()])
     assert_fp32_close(got, full_rows, "staging rows", rel=2e-5)
+
+
+def test_prefetch_chain_runner_matches_direct_and_oracle():
+    """The two-slot side-stream chain (warm, cold and folded) gives the same bits as direct
+    calls, and its deferred finalize leaves main_grad = initial + staging, as the oracle's
+    schedule does."""
+    from tensor_transformer_layer_way_gb300 import chain
+    L, g, M, K, N = 5, 4, 192, 512, 136
+    inp = si.gtp_inputs(L, K, N, M, seed=23)
+    shards = [_shards(W, g) for W in inp["W"]]
+    X = dev(inp["X"])
+    dYs = dev(inp["dY"])
+    slots = [torch.empty((K, N), device="cuda", dtype=torch.bfloat16) for _ in range(2)]
+    runner = chain.GtpChain(ttl, torch, shards, slots)
+    Yc = [torch.empty((M, N), device="cuda", dtype=torch.bfloat16) for _ in range(L)]
+    Yw = [torch.empty_like(y) for y in Yc]
+    Yf = [torch.empty_like(y) for y in Yc]
+    runner.forward(X, Yc, cold=True)
+    runner.forward(X, Yw)
+    runner.forward(X, Yf, folded=True)
+    dX = [torch.empty((M, K), device="cuda", dtype=torch.bfloat16) for _ in range(L)]
+    staging = [[torch.empty((K // g, N), device="cuda") for _ in range(g)] for _ in range(L)]
+    mg = [[torch.zeros((K // g, N), device="cuda") for _ in range(g)] for _ in range(L)]
+    runner.backward(X, dYs, dX, staging, mg)
+    torch.cuda.synchronize()
+    assert ttl.device_status() == 0
+    for l in range(L):
+        assert torch.equal(Yc[l], Yw[l]) and torch.equal(Yc[l], Yf[l])
+        direct = torch.empty_like(dX[l])
+        ttl.gtp_gather_gemm(dYs[l], shards[l], direct, transpose_w=True)
+        assert torch.equal(direct, dX[l])
+        assert_gemm_close(f64(Yw[l]), gtp.forward_gemm(f64(inp["X"]), f64(inp["W"][l])), f"Y[{l}]")
+    st_ref = [gtp.wgrad_reduce_scatter(f64(inp["X"]), f64(inp["dY"][l]), g) for l in range(L)]
+    ref = gtp.deferred_finalize([[np.zeros((K // g, N)) for _ in range(g)] for _ in range(L)], st_ref)
+    for l in range(L):
+        for j in range(g):
+            assert_fp32_close(f32(mg[l][j]), ref["main_grad"][l][j], f"main_grad[{l}][{j}]", rel=2e-5)
+
+
+def test_trace_records_launches():
+    K, N, g = 256, 64, 4
+    sh = _shards(si.randn_bf16(si.generator(0), (K, N)), g)
+    slot = torch.empty((K, N), device="cuda", dtype=torch.bfloat16)
+    ttl.trace_enable(True, 64)
+    ttl.gtp_gather(sh, slot)
+    recs = ttl.trace_read(64)
+    ttl.trace_enable(False)
+    assert len(recs) == 1 and recs[0][0] == "gtp_gather" and recs[0][1] > 0 and recs[0][3] == 2 * K * N * 2
