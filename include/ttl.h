@@ -171,6 +171,32 @@ int ttl_tp_mlp_bwd(int t, int act, int64_t T, int64_t h, int64_t f, const ttl_bf
                    ttl_bf16* const* dA, ttl_bf16* const* dA_up, ttl_bf16* const* dB, ttl_bf16* const* db1,
                    ttl_bf16* db2, ttl_bf16* const* dX, void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the library's own scratch area used by ttl_tp_mlp_bwd_static_ws: 16 MiB. */
+#define TTL_STATIC_WS_BYTES (16u << 20)
+
+/* ttl_tp_mlp_bwd without a workspace argument, for callers that cannot allocate device
+ * memory: for example a program whose device memory is all owned by another allocator that
+ * forbids further cudaMalloc, or a latency-critical loop that must not pay for cudaMalloc and
+ * its implicit device-wide synchronisation.  The pages have no counterpart to this entry
+ * point; it exists only for such callers.
+ *   Arguments and results are those of ttl_tp_mlp_bwd (minus ws / ws_bytes).  The scratch is
+ *   a fixed TTL_STATIC_WS_BYTES array inside the library, present on every GPU that loads the
+ *   library until the process exits.  A shape whose ttl_tp_mlp_bwd_workspace_size() exceeds
+ *   it is rejected with TTL_ERR_UNSUPPORTED before anything runs.
+ *   No device memory is allocated or freed.  The first call on each device looks up the
+ *   scratch's device address with that device current; make that first call before any
+ *   stream capture.
+ *   All calls share the one scratch array, and it keeps whatever the last call left in it
+ *   (nothing in it needs to start at zero: every element is written before it is read).
+ *   Calls that overlap on the GPU (e.g. on two streams at once) race on it and give wrong
+ *   results: order them on one stream or with events. */
+int ttl_tp_mlp_bwd_static_ws(int t, int act, int64_t T, int64_t h, int64_t f, const ttl_bf16* X,
+                             const ttl_bf16* dY, const ttl_bf16* const* A, const ttl_bf16* const* A_up,
+                             const ttl_bf16* const* B, const ttl_bf16* const* U_save,
+                             const ttl_bf16* const* V_save, const ttl_bf16* const* Hact, ttl_bf16* const* dA,
+                             ttl_bf16* const* dA_up, ttl_bf16* const* dB, ttl_bf16* const* db1, ttl_bf16* db2,
+                             ttl_bf16* const* dX, void* stream);
+
 /* ------------------------------------------------------------------ GTP_remat weight path */
 
 /* [GTP] concepts "GTP_remat", "Prefetch chain", "Deferred finalize", Fig. 1 and the list

@@ -50,6 +50,8 @@ _SIGS = {
     "ttl_tp_mlp_bwd_workspace_size": (ctypes.c_size_t, [_int, _int, _i64, _i64, _i64]),
     "ttl_tp_mlp_bwd": (_int, [_int, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "ttl_tp_mlp_bwd_static_ws": (_int, [_int, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _vp, _vp, _vp, _vp, _vp, _vp]),
     "ttl_gtp_gather": (_int, [_int, _i64, _i64, _vp, _vp, _vp, _vp]),
     "ttl_gtp_gather_gemm": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp]),
     "ttl_gtp_wgrad_rs_finalize": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp, _vp]),
@@ -288,6 +290,25 @@ def tp_mlp_bwd(X, dY, A, B, fwd, *, act="gelu_tanh", A_up=None, out=None, bias=F
                                 _arr(fwd["V"]), _arr(fwd["H"]), _arr(out["dA"]), _arr(out["dA_up"]), _arr(out["dB"]),
                                 _arr(out["db1"]), _p(out["db2"]), _arr(out["dX"]), _p(ws), ws.numel(),
                                 _stream(stream)))
+    return out
+
+
+STATIC_WS_BYTES = 16 << 20
+
+
+def tp_mlp_bwd_static_ws(X, dY, A, B, fwd, *, act="gelu_tanh", A_up=None, out, stream=None):
+    """tp_mlp_bwd using the library's built-in 16 MiB scratch instead of a caller workspace,
+    for callers that cannot allocate device memory.  ``out`` (dA, dA_up, dB, db1, db2, dX) must be
+    provided.  Calls that overlap on the GPU share the scratch and race."""
+    t = len(A)
+    T, h = X.shape
+    f = A[0].shape[1] * t
+    _need(X, "X")
+    _need(dY, "dY", shape=(T, h))
+    _check(lib().ttl_tp_mlp_bwd_static_ws(t, ACT[act], T, h, f, _p(X), _p(dY), _arr(A), _arr(A_up), _arr(B),
+                                          _arr(fwd["U"]), _arr(fwd["V"]), _arr(fwd["H"]), _arr(out["dA"]),
+                                          _arr(out["dA_up"]), _arr(out["dB"]), _arr(out["db1"]), _p(out["db2"]),
+                                          _arr(out["dX"]), _stream(stream)))
     return out
 
 
