@@ -2,18 +2,27 @@
 //
 // One launch computes a list of problems (e.g. the t shards of a column-parallel layer,
 // or the t shards' dgrad and wgrad) so that the narrow per-shard GEMMs fill the GPU
-// together.  Each CTA owns one SM and walks the linearised tile list with a static
-// stride.  Roles (192 threads):
-//   warp 0      TMA producer: one thread issues cp.async.bulk.tensor loads of the A and B
-//               tiles of each 64-wide K block into a 4-stage shared-memory ring;
-//   warp 1      MMA issuer: allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and one thread issues tcgen05.mma (M=128, N=256, K=16) per K step;
+// together.  Work is cut into tiles of TILE_M rows x 256 accumulator columns, walked by
+// persistent workers with a static stride.  Roles (192 threads per CTA):
+//   warp 0      TMA producer: one thread issues cp.async.bulk.tensor loads of this CTA's
+//               A rows and B columns for each 64-wide K block into a shared-memory ring;
+//   warp 1      MMA issuer: allocates 512 TMEM columns (two 128 x 256 fp32 accumulators,
+//               double-buffered) and one thread issues tcgen05.mma per 16-wide K step;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator rows, apply the fused op (bias,
 //               GeLU, SwiGLU, their derivatives) and store bf16/fp32 to global memory.
-// The accumulator is double-buffered, so the epilogue of tile n overlaps the MMAs of
-// tile n+1.  Every mbarrier wait is bounded in wall time; a timeout records
-// TTL_ERR_TIMEOUT, all roles leave their loops, in-flight copies and MMAs are waited
-// for (again bounded), TMEM is released and the kernel returns.
+//
+// Two variants share the code:
+//   single CTA  (PAIR = false): TILE_M = 128, MMA M=128 N=256, 4 stages of 48 KiB.
+//   CTA pair    (PAIR = true) : a cluster of two CTAs on two SMs computes a 256 x 256 tile
+//               with tcgen05.mma.cta_group::2 (M=256 N=256).  Each CTA holds its own 128 A
+//               rows and 128 of the 256 B columns, so the B tile is read from HBM/L2 and
+//               shared memory once per pair; each stage is 32 KiB and 6 stages fit.  Both
+//               CTAs' TMA loads complete on the leader CTA's full barrier, the leader alone
+//               issues MMAs, and its commits arrive on both CTAs' barriers (multicast).
+//
+// Every mbarrier wait is bounded in wall time; a timeout records TTL_ERR_TIMEOUT, all roles
+// leave their loops, in-flight copies and MMAs are waited for (again bounded), TMEM is
+// released and the kernel returns.
 //
 // Shared-memory operand layouts (128-byte swizzle, 1024-byte aligned stages):
 //   K-major operand  : box {64 K, 128 rows}; row r at r*128 B; 8-row atoms 1024 B apart
@@ -23,6 +32,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -31,19 +41,25 @@
 
 namespace ttl {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;           // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;           // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int TMEM_COLS = 2 * BN;                    // two accumulators
+constexpr int BN = 256;            // accumulator columns per tile
+constexpr int BK = 64;             // K per stage
+constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int GROUP_M = 16;
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+
+template <bool PAIR>
+struct Cfg {
+  static constexpr int TILE_M = PAIR ? 256 : 128;     // rows per tile (both CTAs of a pair)
+  static constexpr int B_COLS = PAIR ? 128 : 256;     // B columns held by one CTA
+  static constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
+  static constexpr int B_BYTES = B_COLS * BK * 2;     // 16 or 32 KiB
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int TX_BYTES = PAIR ? 2 * STAGE : STAGE;   // counted on the (leader's) full barrier
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
+  static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+};
 static_assert(sizeof(GemmParams) <= 32764, "kernel parameter block beyond the 32 KiB limit");
-static_assert(SMEM_BYTES <= 232448, "shared memory beyond the per-CTA limit");
 
 struct TileCoord {
   int p, tm, tn;
@@ -128,15 +144,97 @@ __device__ __forceinline__ void load_row32_bf16(const void* base, int64_t ld, in
   }
 }
 
+// Applies the problem's epilogue to one accumulator tile slice held in this CTA's TMEM
+// (128 rows; this thread owns one row) and stores it.
+__device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase, int row, int n_base_paired,
+                                              int n_base) {
+  const bool row_ok = row < pr.M;
+  const int epi = pr.epi;
+  if (pr.paired) {
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 2 / 32; ++ch) {
+      uint32_t g[32], u[32];
+      __syncwarp();
+      tmem_ld_32x32b_x32(tbase + ch * 32, g);
+      tmem_ld_32x32b_x32(tbase + BN / 2 + ch * 32, u);
+      tmem_ld_wait();
+      const int col0 = n_base_paired + ch * 32;
+      if (row_ok && col0 < pr.N) {
+        float gv[32], uv[32], hv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          gv[j] = __uint_as_float(g[j]);
+          uv[j] = __uint_as_float(u[j]);
+          hv[j] = gv[j] * sigmoid_f(gv[j]) * uv[j];
+        }
+        store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, gv);
+        store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, uv);
+        store_row32_bf16(pr.out2, pr.ld_out, row, col0, pr.N, hv);
+      }
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld_32x32b_x32(tbase + ch * 32, r);
+    tmem_ld_wait();
+    const int col0 = n_base + ch * 32;
+    if (row_ok && col0 < pr.N) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      if (epi == EPI_F32) {
+        store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
+      } else if (epi == EPI_BF16 || epi == EPI_GELU_FWD) {
+        if (pr.bias0) {
+          float b[32];
+          load_row32_bf16(pr.bias0, 0, 0, col0, pr.N, b);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += b[j];
+        }
+        store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+        if (epi == EPI_GELU_FWD) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j]);
+          store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
+        }
+      } else if (epi == EPI_GELU_BWD) {
+        float x[32];
+        load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, x);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(x[j]);
+        store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+      } else if (epi == EPI_SWIGLU_BWD) {
+        float gg[32], vv[32], dg[32];
+        load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, gg);
+        load_row32_bf16(pr.aux1, pr.ld_aux, row, col0, pr.N, vv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float s = sigmoid_f(gg[j]);
+          dg[j] = v[j] * vv[j] * s * (1.0f + gg[j] * (1.0f - s));
+          v[j] = v[j] * gg[j] * s;
+        }
+        store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, dg);
+        store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 
+template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams P) {
+  using C = Cfg<PAIR>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // Stages must sit on 1024-byte boundaries for the 128-byte swizzle atoms.
+  // Stages must sit on 1024-byte boundaries for the 128-byte swizzle atoms.  The offset is
+  // the same in both CTAs of a pair, which the pair MMA's shared descriptors rely on.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty_bar = full_bar + C::STAGES;
+  uint64_t* tfull_bar = empty_bar + C::STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* done_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -144,15 +242,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // 0 = leader of the pair
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4);
+      mbar_init(&tempty_bar[a], PAIR ? 8 : 4);   // every epilogue warp of the pair arrives
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -162,11 +264,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     for (int i = lane; i < P.nmaps; i += 32) tma_prefetch_map(&P.maps[i]);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if (PAIR) cluster_sync_all();   // the peer's barriers must be initialised before any remote signal
+  else __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -180,10 +288,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+      for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.probs[c.p];
-        const int am = pr.a_m0 + c.tm * BM;
+        const int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
         for (int s = 0; ok && s < pr.nseg; ++s) {
           const Seg& sg = pr.seg[s];
           const CUtensorMap* ma = &P.maps[sg.map_a];
@@ -196,59 +304,84 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
               ok = false;
               break;
             }
-            uint8_t* sa = smem + stage * STAGE_BYTES;
-            uint8_t* sb = sa + A_STAGE_BYTES;
-            mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+            uint8_t* sa = smem + stage * C::STAGE;
+            uint8_t* sb = sa + C::A_BYTES;
             const int ka = sg.a_k0 + kb * BK;
             const int kbb = sg.b_k0 + kb * BK;
-            if (!pr.a_mn) {
-              tma_load_2d(sa, ma, &full_bar[stage], ka, am);
+            if (PAIR) {
+              // Both CTAs' copies complete on the leader's full barrier, which the leader
+              // arms with the bytes of the whole pair.
+              if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+              const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+              if (!pr.a_mn) {
+                tma_load_2d_pair(sa, ma, fb, ka, am);
+              } else {
+                tma_load_2d_pair(sa, ma, fb, am, ka);
+                tma_load_2d_pair(sa + 8192, ma, fb, am + 64, ka);
+              }
+              const CUtensorMap* mb = rank ? mb1 : mb0;
+              const int bn = rank ? bn1 : bn0;
+              if (!pr.b_mn) {
+                tma_load_2d_pair(sb, mb, fb, kbb, bn);
+              } else {
+                tma_load_2d_pair(sb, mb, fb, bn, kbb);
+                tma_load_2d_pair(sb + 8192, mb, fb, bn + 64, kbb);
+              }
             } else {
-              tma_load_2d(sa, ma, &full_bar[stage], am, ka);
-              tma_load_2d(sa + 8192, ma, &full_bar[stage], am + 64, ka);
-            }
-            if (!pr.b_mn) {
-              tma_load_2d(sb, mb0, &full_bar[stage], kbb, bn0);
-              tma_load_2d(sb + 16384, mb1, &full_bar[stage], kbb, bn1);
-            } else {
-              tma_load_2d(sb, mb0, &full_bar[stage], bn0, kbb);
-              tma_load_2d(sb + 8192, mb0, &full_bar[stage], bn0 + 64, kbb);
-              tma_load_2d(sb + 16384, mb1, &full_bar[stage], bn1, kbb);
-              tma_load_2d(sb + 24576, mb1, &full_bar[stage], bn1 + 64, kbb);
+              mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+              if (!pr.a_mn) {
+                tma_load_2d(sa, ma, &full_bar[stage], ka, am);
+              } else {
+                tma_load_2d(sa, ma, &full_bar[stage], am, ka);
+                tma_load_2d(sa + 8192, ma, &full_bar[stage], am + 64, ka);
+              }
+              if (!pr.b_mn) {
+                tma_load_2d(sb, mb0, &full_bar[stage], kbb, bn0);
+                tma_load_2d(sb + 16384, mb1, &full_bar[stage], kbb, bn1);
+              } else {
+                tma_load_2d(sb, mb0, &full_bar[stage], bn0, kbb);
+                tma_load_2d(sb + 8192, mb0, &full_bar[stage], bn0 + 64, kbb);
+                tma_load_2d(sb + 16384, mb1, &full_bar[stage], bn1, kbb);
+                tma_load_2d(sb + 24576, mb1, &full_bar[stage], bn1 + 64, kbb);
+              }
             }
             ++issued;
-            if (++stage == STAGES) {
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
       }
-      // Make sure no copy is still landing in shared memory when the CTA leaves: wait for
-      // the completion of the last min(issued, STAGES) loads (bounded).
-      const int pending = issued < STAGES ? issued : STAGES;
-      int s = stage;
-      uint32_t ph = phase;
-      for (int i = 0; i < pending; ++i) {
-        if (--s < 0) {
-          s = STAGES - 1;
-          ph ^= 1u;
+      // No copy may still be landing in shared memory when the CTA leaves: wait for the
+      // completion of the last min(issued, STAGES) loads (bounded).  In a pair the leader's
+      // full barriers count the follower's copies too, and the follower leaves only after
+      // the leader (cluster barrier below).
+      if (leader) {
+        const int pending = issued < C::STAGES ? issued : C::STAGES;
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < pending; ++i) {
+          if (--s < 0) {
+            s = C::STAGES - 1;
+            ph ^= 1u;
+          }
+          int dummy_abort = 0;
+          mbar_wait(&full_bar[s], ph, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
         }
-        int dummy_abort = 0;
-        mbar_wait(&full_bar[s], ph, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       const uint32_t sbase = smem_u32(smem);
-      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+      for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.probs[c.p];
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, status, tmo)) {
@@ -257,7 +390,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        const uint32_t idesc = idesc_bf16_f32(BM, BN, pr.a_mn != 0, pr.b_mn != 0);
+        const uint32_t idesc = idesc_bf16_f32(C::TILE_M, BN, pr.a_mn != 0, pr.b_mn != 0);
         const uint32_t a_step = pr.a_mn ? 2048u : 32u;
         const uint32_t b_step = pr.b_mn ? 2048u : 32u;
         const uint32_t a_lbo = pr.a_mn ? 8192u : 16u;
@@ -271,31 +404,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
               break;
             }
             tc_fence_after_sync();
-            const uint32_t sa = sbase + stage * STAGE_BYTES;
-            const uint32_t sb = sa + A_STAGE_BYTES;
+            const uint32_t sa = sbase + stage * C::STAGE;
+            const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t adesc = smem_desc_sw128(sa + kk * a_step, a_lbo, 1024);
               const uint64_t bdesc = smem_desc_sw128(sb + kk * b_step, b_lbo, 1024);
-              umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+              if (PAIR) umma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+              else umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
               accumulate = 1;
             }
-            umma_commit(&empty_bar[stage]);
-            if (++stage == STAGES) {
+            // Frees this stage in both CTAs once the MMAs reading it are done.
+            if (PAIR) umma_commit_pair(&empty_bar[stage], 0x3);
+            else umma_commit(&empty_bar[stage]);
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
         if (!ok) break;
-        umma_commit(&tfull_bar[acc]);
+        if (PAIR) umma_commit_pair(&tfull_bar[acc], 0x3);
+        else umma_commit(&tfull_bar[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // All MMAs issued by this thread must finish before TMEM is released.
-      umma_commit(done_bar);
+      if (PAIR) umma_commit_pair(done_bar, 0x1);
+      else umma_commit(done_bar);
       int dummy_abort = 0;
       mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
     }
@@ -306,92 +444,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
+    const uint32_t tempty_leader0 = PAIR ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
+    for (int tile = unit; tile < P.total_tiles; tile += nunits) {
       const TileCoord c = decode_tile(P, tile);
       const Problem& pr = P.probs[c.p];
       const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const int row = c.tm * BM + row_in_tile;
-      const bool row_ok = row < pr.M;
-      const int epi = pr.epi;
-      if (pr.paired) {
-        const int n_base = c.tn * (BN / 2);
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 2 / 32; ++ch) {
-          uint32_t g[32], u[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(tbase + ch * 32, g);
-          tmem_ld_32x32b_x32(tbase + BN / 2 + ch * 32, u);
-          tmem_ld_wait();
-          const int col0 = n_base + ch * 32;
-          if (row_ok && col0 < pr.N) {
-            float gv[32], uv[32], hv[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              gv[j] = __uint_as_float(g[j]);
-              uv[j] = __uint_as_float(u[j]);
-              hv[j] = gv[j] * sigmoid_f(gv[j]) * uv[j];
-            }
-            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, gv);
-            store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, uv);
-            store_row32_bf16(pr.out2, pr.ld_out, row, col0, pr.N, hv);
-          }
-        }
-      } else {
-        const int n_base = c.tn * BN;
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint32_t r[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(tbase + ch * 32, r);
-          tmem_ld_wait();
-          const int col0 = n_base + ch * 32;
-          if (row_ok && col0 < pr.N) {
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          if (epi == EPI_F32) {
-            store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
-          } else if (epi == EPI_BF16 || epi == EPI_GELU_FWD) {
-            if (pr.bias0) {
-              float b[32];
-              load_row32_bf16(pr.bias0, 0, 0, col0, pr.N, b);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += b[j];
-            }
-            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
-            if (epi == EPI_GELU_FWD) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j]);
-              store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
-            }
-          } else if (epi == EPI_GELU_BWD) {
-            float x[32];
-            load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, x);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(x[j]);
-            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
-          } else if (epi == EPI_SWIGLU_BWD) {
-            float gg[32], vv[32], dg[32];
-            load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, gg);
-            load_row32_bf16(pr.aux1, pr.ld_aux, row, col0, pr.N, vv);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float s = sigmoid_f(gg[j]);
-              dg[j] = v[j] * vv[j] * s * (1.0f + gg[j] * (1.0f - s));
-              v[j] = v[j] * gg[j] * s;
-            }
-            store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, dg);
-            store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
-          }
-          }
-        }
-      }
+      const int row = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + row_in_tile;
+      epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(tempty_leader0 + acc * 8u);
+        else mbar_arrive(&tempty_bar[acc]);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -400,10 +468,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     tc_fence_before_sync();
   }
 
-  __syncthreads();
+  // Both CTAs of a pair leave together: the leader's MMAs read the follower's shared memory
+  // and write its TMEM, so neither may release them while the other still works.
+  if (PAIR) cluster_sync_all();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -429,19 +501,58 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-int smem_attr_set(int device) {
+struct DevState {
+  bool attrs = false;
+  int pair_clusters = 0;   // co-resident CTA pairs (0 = not queried / none)
+};
+
+int device_setup(int device, DevState** out) {
   static std::mutex mu;
-  static bool done[64] = {false};
+  static DevState st[64];
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return set_error(TTL_ERR_CUDA, "device index out of range");
-  if (!done[device]) {
-    int rc = cuda_check(cudaFuncSetAttribute(gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES),
+  DevState& s = st[device];
+  if (!s.attrs) {
+    int rc = cuda_check(cudaFuncSetAttribute(gemm_tcgen05_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<false>::SMEM),
                         "cudaFuncSetAttribute(gemm smem)");
     if (rc) return rc;
-    done[device] = true;
+    rc = cuda_check(cudaFuncSetAttribute(gemm_tcgen05_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<true>::SMEM),
+                    "cudaFuncSetAttribute(gemm pair smem)");
+    if (rc) return rc;
+    // How many CTA pairs can be resident at once (one CTA per SM).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * 512, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<true>::SMEM;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    s.pair_clusters = n;
+    s.attrs = true;
   }
+  *out = &s;
   return TTL_OK;
+}
+
+// TTL_GEMM_CTA_PAIR=0 selects the single-CTA tiles for every launch (for comparisons).
+bool pair_allowed() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("TTL_GEMM_CTA_PAIR");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
 }
 
 }  // namespace
@@ -548,7 +659,7 @@ int GemmBatch::flush(cudaStream_t stream) {
 
 int GemmBatch::launch(cudaStream_t stream) {
   if (err_) return err_;
-  int total = 0;
+  int max_m = 0;
   for (int i = 0; i < p_->nprob; ++i) {
     Problem& p = p_->probs[i];
     if (p.nseg == 0) return set_error(TTL_ERR_ARG, "GEMM problem %d has no K segment", i);
@@ -556,8 +667,22 @@ int GemmBatch::launch(cudaStream_t stream) {
     bool aligned = (p.a_m0 % 8 == 0) && (p.b_n0 % 8 == 0);
     for (int k = 0; k < p.nseg; ++k) aligned = aligned && p.seg[k].a_k0 % 8 == 0 && p.seg[k].b_k0 % 8 == 0;
     if (!aligned) return set_error(TTL_ERR_ALIGN, "GEMM problem %d: operand offsets must be multiples of 8", i);
+    if (p.M > max_m) max_m = p.M;
+  }
+  int rc = require_sm103();
+  if (rc) return rc;
+  int dev = 0;
+  if ((rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
+  DevState* ds = nullptr;
+  if ((rc = device_setup(dev, &ds))) return rc;
+  // CTA pairs (256-row tiles) unless every problem is at most 128 rows tall.
+  const bool pair = pair_allowed() && ds->pair_clusters > 0 && max_m > 128;
+  const int tile_m = pair ? Cfg<true>::TILE_M : Cfg<false>::TILE_M;
+  int total = 0;
+  for (int i = 0; i < p_->nprob; ++i) {
+    Problem& p = p_->probs[i];
     const int tn = p.paired ? BN / 2 : BN;
-    p.tiles_m = (p.M + BM - 1) / BM;
+    p.tiles_m = (p.M + tile_m - 1) / tile_m;
     p.tiles_n = (p.N + tn - 1) / tn;
     p.tile_start = total;
     total += p.tiles_m * p.tiles_n;
@@ -565,18 +690,29 @@ int GemmBatch::launch(cudaStream_t stream) {
   p_->total_tiles = total;
   p_->nmaps = nmaps_;
   if (total == 0) return TTL_OK;
-  int rc = require_sm103();
-  if (rc) return rc;
-  int dev = 0;
-  if ((rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
-  if ((rc = smem_attr_set(dev))) return rc;
   p_->status = device_status_ptr();
   if (!p_->status) return TTL_ERR_CUDA;
   p_->timeout_ns = 2000000000ull;  // 2 s per wait: far beyond any legitimate stall
-  const int grid = total < num_sms() ? total : num_sms();
   TraceScope trace(stream, TTL_K_GEMM, flops_, bytes_);
-  gemm_tcgen05_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(*p_);
-  return cuda_check(cudaGetLastError(), "gemm_tcgen05_kernel launch");
+  if (!pair) {
+    const int grid = total < num_sms() ? total : num_sms();
+    gemm_tcgen05_kernel<false><<<grid, NUM_THREADS, Cfg<false>::SMEM, stream>>>(*p_);
+    return cuda_check(cudaGetLastError(), "gemm_tcgen05_kernel launch");
+  }
+  const int pairs = total < ds->pair_clusters ? total : ds->pair_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<true>::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<true>, *p_), "gemm_tcgen05_kernel<pair> launch");
 }
 
 }  // namespace ttl
