@@ -199,7 +199,7 @@ extern "C" int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, con
     const int mh = batch.add_map(H, T, h, h, false);
     for (int i = 0; i < t; ++i) {
       const int mw = batch.add_map(W[i], Vs, h, h, false);
-      Problem* p = batch.add_problem(T, Vs, false, false, EPI_F32, false);
+      Problem* p = batch.add_problem(T, Vs, false, false, EPI_F32, false, i > 0);
       if (batch.error()) return batch.error();
       p->out0 = logits[i];
       p->ld_out = Vs;

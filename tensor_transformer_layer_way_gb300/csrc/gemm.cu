@@ -54,7 +54,7 @@ struct Cfg {
   static constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
   static constexpr int B_BYTES = B_COLS * BK * 2;     // 16 or 32 KiB
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int STAGES = PAIR ? 7 : 4;
   static constexpr int TX_BYTES = PAIR ? 2 * STAGE : STAGE;   // counted on the (leader's) full barrier
   static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
@@ -65,39 +65,52 @@ struct TileCoord {
   int p, tm, tn;
 };
 
+// Linear tile index -> (problem, m-tile, n-tile).  Inside a tile group the order is: bands
+// of GROUP_M m-tiles; within a band, n-tiles across all of the group's problems; within
+// an n-tile, the band's m-tiles.  Persistent workers taking consecutive indices therefore
+// share A rows (same band) and B columns (same n-tile) in L2.
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile) {
-  int p = 0;
+  int gi = 0;
 #pragma unroll 1
-  while (p + 1 < P.nprob && tile >= P.probs[p + 1].tile_start) ++p;
-  const Problem& pr = P.probs[p];
-  const int local = tile - pr.tile_start;
-  const int per_group = GROUP_M * pr.tiles_n;
-  const int group = local / per_group;
-  const int first_m = group * GROUP_M;
-  const int gm = min(GROUP_M, pr.tiles_m - first_m);
-  const int r = local - group * per_group;
+  while (gi + 1 < P.ngroups && tile >= P.groups[gi + 1].tile_start) ++gi;
+  const TileGroup& g = P.groups[gi];
+  const int local = tile - g.tile_start;
+  const int per_band = GROUP_M * g.tiles_n;
+  const int band = local / per_band;
+  const int first_m = band * GROUP_M;
+  const int gm = min(GROUP_M, g.tiles_m - first_m);
+  const int r = local - band * per_band;
+  const int tn = r / gm;
+  int p = g.first;
+#pragma unroll 1
+  while (p + 1 < g.first + g.count && tn >= P.probs[p + 1].tn0) ++p;
   TileCoord c;
   c.p = p;
   c.tm = first_m + r % gm;
-  c.tn = r / gm;
+  c.tn = tn - P.probs[p].tn0;
   return c;
 }
 
 // ------------------------------------------------------------------ epilogue math
 
+// The epilogue math uses the fast exponential intrinsic: its results are rounded to bf16
+// right after, so a few ulp of fp32 error are invisible.
+// tanh(u) = 1 - 2 / (exp(2u) + 1), which saturates correctly to +-1 at large |u|.
+__device__ __forceinline__ float tanh_fast(float u) { return 1.0f - __fdividef(2.0f, __expf(2.0f * u) + 1.0f); }
+
 __device__ __forceinline__ float gelu_tanh_f(float x) {
   const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  return 0.5f * x * (1.0f + tanhf(u));
+  return 0.5f * x * (1.0f + tanh_fast(u));
 }
 
 __device__ __forceinline__ float gelu_tanh_grad_f(float x) {
   const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  const float th = tanhf(u);
+  const float th = tanh_fast(u);
   const float du = 0.7978845608028654f * (1.0f + 3.0f * 0.044715f * x * x);
   return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
 }
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // Stores 32 consecutive bf16 values of one row (columns col0..col0+31), masking at N.
 __device__ __forceinline__ void store_row32_bf16(void* base, int64_t ld, int row, int col0, int N,
@@ -141,6 +154,22 @@ __device__ __forceinline__ void load_row32_bf16(const void* base, int64_t ld, in
     v[q * 8 + 5] = bf16_hi(w.z);
     v[q * 8 + 6] = bf16_lo(w.w);
     v[q * 8 + 7] = bf16_hi(w.w);
+  }
+}
+
+// Asks L2 to fetch this thread's row of the auxiliary inputs an epilogue will read (the
+// saved pre-activations of a backward epilogue), so those loads hit L2 when the tile's
+// accumulator is ready.  One 128-byte line per 64 bf16 columns.
+__device__ __forceinline__ void prefetch_aux_row(const Problem& pr, int row, int n_base) {
+  if (pr.epi != EPI_GELU_BWD && pr.epi != EPI_SWIGLU_BWD) return;
+  if (row >= pr.M) return;
+#pragma unroll
+  for (int c = 0; c < BN; c += 64) {
+    if (n_base + c >= pr.N) break;
+    const int64_t off = static_cast<int64_t>(row) * pr.ld_aux + n_base + c;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const __nv_bfloat16*>(pr.aux0) + off));
+    if (pr.epi == EPI_SWIGLU_BWD)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const __nv_bfloat16*>(pr.aux1) + off));
   }
 }
 
@@ -445,12 +474,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint32_t tempty_leader0 = PAIR ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
+    const int my_row0 = static_cast<int>(rank) * 128 + row_in_tile;
+    if (unit < P.total_tiles) {
+      const TileCoord c0 = decode_tile(P, unit);
+      prefetch_aux_row(P.probs[c0.p], c0.tm * C::TILE_M + my_row0, c0.tn * BN);
+    }
     for (int tile = unit; tile < P.total_tiles; tile += nunits) {
       const TileCoord c = decode_tile(P, tile);
       const Problem& pr = P.probs[c.p];
       const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
+      // The next tile's auxiliary rows travel to L2 while this tile's epilogue runs.
+      if (tile + nunits < P.total_tiles) {
+        const TileCoord cn = decode_tile(P, tile + nunits);
+        prefetch_aux_row(P.probs[cn.p], cn.tm * C::TILE_M + my_row0, cn.tn * BN);
+      }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const int row = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + row_in_tile;
       epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN);
@@ -602,8 +641,10 @@ int GemmBatch::add_map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, 
   return nmaps_++;
 }
 
-Problem* GemmBatch::add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired) {
+Problem* GemmBatch::add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired, bool join) {
   if (err_) return nullptr;
+  if (join && (p_->nprob == 0 || p_->probs[p_->nprob - 1].M != M || p_->probs[p_->nprob - 1].paired != paired))
+    join = false;   // a group needs the same M and tile width; otherwise start a new one
   if (p_->nprob >= kMaxProblems) {
     err_ = set_error(TTL_ERR_ARG, "GEMM batch: too many problems (max %d)", kMaxProblems);
     return nullptr;
@@ -620,6 +661,7 @@ Problem* GemmBatch::add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int 
   p->b_mn = b_mn;
   p->epi = static_cast<uint8_t>(epi);
   p->paired = paired;
+  p->join = join;
   return p;
 }
 
@@ -679,12 +721,24 @@ int GemmBatch::launch(cudaStream_t stream) {
   const bool pair = pair_allowed() && ds->pair_clusters > 0 && max_m > 128;
   const int tile_m = pair ? Cfg<true>::TILE_M : Cfg<false>::TILE_M;
   int total = 0;
+  p_->ngroups = 0;
   for (int i = 0; i < p_->nprob; ++i) {
     Problem& p = p_->probs[i];
     const int tn = p.paired ? BN / 2 : BN;
     p.tiles_m = (p.M + tile_m - 1) / tile_m;
     p.tiles_n = (p.N + tn - 1) / tn;
-    p.tile_start = total;
+    if (!p.join || p_->ngroups == 0) {
+      TileGroup& g = p_->groups[p_->ngroups++];
+      g.tile_start = total;
+      g.tiles_m = p.tiles_m;
+      g.tiles_n = 0;
+      g.first = i;
+      g.count = 0;
+    }
+    TileGroup& g = p_->groups[p_->ngroups - 1];
+    p.tn0 = g.tiles_n;
+    g.tiles_n += p.tiles_n;
+    g.count += 1;
     total += p.tiles_m * p.tiles_n;
   }
   p_->total_tiles = total;

@@ -211,7 +211,7 @@ extern "C" int ttl_gtp_gather_gemm(int g, int64_t M, int64_t K, int64_t N, const
       // Folded gather: output columns [j K/g, (j+1) K/g) come from shard j.
       for (int j = 0; j < g; ++j) {
         const int mw = batch.add_map(shards[j], Kg, N, N, false);
-        Problem* p = batch.add_problem(M, Kg, false, false, EPI_BF16, false);
+        Problem* p = batch.add_problem(M, Kg, false, false, EPI_BF16, false, j > 0);
         if (batch.error()) return batch.error();
         p->out0 = Y + j * Kg;
         p->ld_out = K;

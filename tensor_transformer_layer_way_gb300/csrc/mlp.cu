@@ -86,7 +86,7 @@ extern "C" int ttl_tp_mlp_fwd(int t, int act, int64_t T, int64_t h, int64_t f, c
     const int mx = batch.add_map(X, T, h, h, false);
     const int ma = batch.add_map(A[i], h, fs, fs, true);
     const int mu = swiglu ? batch.add_map(A_up[i], h, fs, fs, true) : -1;
-    Problem* p = batch.add_problem(T, fs, false, true, swiglu ? EPI_SWIGLU_FWD : EPI_GELU_FWD, swiglu);
+    Problem* p = batch.add_problem(T, fs, false, true, swiglu ? EPI_SWIGLU_FWD : EPI_GELU_FWD, swiglu, i > 0);
     if (batch.error()) return batch.error();
     p->out0 = U_save[i];
     p->out1 = swiglu ? static_cast<void*>(V_save[i]) : static_cast<void*>(Hact[i]);
@@ -184,7 +184,7 @@ extern "C" int ttl_tp_mlp_bwd(int t, int act, int64_t T, int64_t h, int64_t f, c
     if (!batch.has_room(2, 1) && (rc = batch.flush(s))) return rc;
     const int md = batch.add_map(dY, T, h, h, false);
     const int mb = batch.add_map(B[i], fs, h, h, false);
-    Problem* p = batch.add_problem(T, fs, false, false, swiglu ? EPI_SWIGLU_BWD : EPI_GELU_BWD, false);
+    Problem* p = batch.add_problem(T, fs, false, false, swiglu ? EPI_SWIGLU_BWD : EPI_GELU_BWD, false, i > 0);
     if (batch.error()) return batch.error();
     p->out0 = ws_slot(i);
     p->out1 = swiglu ? ws_slot(t + i) : nullptr;
@@ -196,35 +196,43 @@ extern "C" int ttl_tp_mlp_bwd(int t, int act, int64_t T, int64_t h, int64_t f, c
   }
   if ((rc = batch.flush(s))) return rc;
 
-  // Weight gradients (all local) and the dX partials, batched into as few launches as fit.
-  for (int i = 0; i < t; ++i) {
-    // dB_i = H_i^T dY: A = H_i stored [T, f/t] (M-major), B = dY stored [T, h] (N-major).
-    if (!batch.has_room(2, 1) && (rc = batch.flush(s))) return rc;
-    int ma = batch.add_map(Hact[i], T, fs, fs, true);
-    int mb = batch.add_map(dY, T, h, h, true);
-    Problem* p = batch.add_problem(fs, h, true, true, EPI_BF16, false);
-    if (batch.error()) return batch.error();
-    p->out0 = dB[i];
-    p->ld_out = h;
-    if ((rc = batch.add_seg(p, ma, 0, mb, -1, 0, T))) return rc;
-
-    // dA_i = X^T dU_i (SwiGLU: dWg_i = X^T dG_i and dWu_i = X^T dV_i).
-    for (int k = 0; k < (swiglu ? 2 : 1); ++k) {
+  // Weight gradients (all local), one launch for all shards.  Problems that share an operand
+  // sit next to each other in the tile order -- every X^T wgrad, then every dY one -- and all
+  // of them contract over the T tokens, so the persistent CTAs stay on neighbouring tiles of
+  // equal cost and the shared operand is served from L2.
+  // dA_i = X^T dU_i (SwiGLU: dWg_i = X^T dG_i and dWu_i = X^T dV_i).
+  for (int k = 0; k < (swiglu ? 2 : 1); ++k) {
+    for (int i = 0; i < t; ++i) {
       if (!batch.has_room(2, 1) && (rc = batch.flush(s))) return rc;
-      ma = batch.add_map(X, T, h, h, true);
-      mb = batch.add_map(ws_slot(k * t + i), T, fs, fs, true);
-      p = batch.add_problem(h, fs, true, true, EPI_BF16, false);
+      const int ma = batch.add_map(X, T, h, h, true);
+      const int mb = batch.add_map(ws_slot(k * t + i), T, fs, fs, true);
+      Problem* p = batch.add_problem(h, fs, true, true, EPI_BF16, false, k + i > 0);
       if (batch.error()) return batch.error();
       p->out0 = k == 0 ? static_cast<void*>(dA[i]) : static_cast<void*>(dA_up[i]);
       p->ld_out = fs;
       if ((rc = batch.add_seg(p, ma, 0, mb, -1, 0, T))) return rc;
     }
+  }
+  // dB_i = H_i^T dY: A = H_i stored [T, f/t] (M-major), B = dY stored [T, h] (N-major).
+  for (int i = 0; i < t; ++i) {
+    if (!batch.has_room(2, 1) && (rc = batch.flush(s))) return rc;
+    const int ma = batch.add_map(Hact[i], T, fs, fs, true);
+    const int mb = batch.add_map(dY, T, h, h, true);
+    Problem* p = batch.add_problem(fs, h, true, true, EPI_BF16, false);
+    if (batch.error()) return batch.error();
+    p->out0 = dB[i];
+    p->ld_out = h;
+    if ((rc = batch.add_seg(p, ma, 0, mb, -1, 0, T))) return rc;
+  }
+  if ((rc = batch.flush(s))) return rc;
 
-    // dX_i = dU_i A_i^T (SwiGLU: dG_i Wg_i^T + dV_i Wu_i^T, one accumulator, two K segments).
+  // dX partials, one launch: dX_i = dU_i A_i^T (SwiGLU: dG_i Wg_i^T + dV_i Wu_i^T, one
+  // accumulator, two K segments).
+  for (int i = 0; i < t; ++i) {
     if (!batch.has_room(swiglu ? 4 : 2, 1) && (rc = batch.flush(s))) return rc;
     const int mdu = batch.add_map(ws_slot(i), T, fs, fs, false);
     const int mwa = batch.add_map(A[i], h, fs, fs, false);
-    p = batch.add_problem(T, h, false, false, EPI_BF16, false);
+    Problem* p = batch.add_problem(T, h, false, false, EPI_BF16, false);
     if (batch.error()) return batch.error();
     p->out0 = dX[i];
     p->ld_out = h;

@@ -74,11 +74,13 @@ struct Seg {
 struct Problem {
   int32_t M, N;
   int32_t tiles_m, tiles_n;
-  int32_t tile_start;     // first linear tile index of this problem
+  int32_t tn0;            // first n-tile of this problem within its group's n-tile range
   int32_t a_m0, b_n0;     // offsets added to the M coordinate of A and N coordinate of B
   uint8_t a_mn, b_mn;     // 1 = operand stored MN-major (A as [K,M], B as [K,N])
   uint8_t epi, nseg;
-  uint8_t paired, pad[3];
+  uint8_t paired;
+  uint8_t join;           // 1 = same tile group as the previous problem (shares its A rows)
+  uint8_t pad[2];
   Seg seg[kMaxSegs];
   void* out0;
   void* out1;
@@ -90,9 +92,21 @@ struct Problem {
   int64_t ld_aux;         // row stride (elements) of aux0/aux1
 };
 
+// Consecutive problems with the same M that read the same A rows form one tile group: its
+// tiles are ordered band by band over M (GROUP_M tiles tall) and, inside a band, across the
+// n-tiles of every problem of the group, so the band's A rows are read from HBM once.
+struct TileGroup {
+  int32_t tile_start;     // first linear tile index of the group
+  int32_t tiles_m;        // m-tiles (common to the group's problems)
+  int32_t tiles_n;        // n-tiles summed over the group's problems
+  int32_t first, count;   // the group's problems: probs[first .. first + count)
+};
+
 struct GemmParams {
   CUtensorMap maps[kMaxMaps];
   Problem probs[kMaxProblems];
+  TileGroup groups[kMaxProblems];
+  int32_t ngroups;
   int32_t nprob;
   int32_t total_tiles;
   int32_t nmaps;
@@ -112,7 +126,9 @@ class GemmBatch {
   int add_map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool mn_major);
   // Adds a problem and returns it (nullptr if the batch is full).  Segments are appended
   // with add_seg(); tile counts are filled in by launch().
-  Problem* add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired);
+  // join = true puts the problem in the previous problem's tile group; use it when both
+  // read the same A rows (same A tensor, same a_m0, same M).
+  Problem* add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired, bool join = false);
   int add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K);
   int launch(cudaStream_t stream);
   int error() const { return err_; }
