@@ -94,6 +94,17 @@ def test_finalize_not_deferred_is_caught(monkeypatch):
     _expect_failure(tgce.test_deferred_finalize_visibility_and_result)
 
 
+def test_embedding_wrong_owner_offset_is_caught(monkeypatch):
+    import test_oracle_embedding as temb
+    from oracle import embedding
+    orig = embedding.shard_lookup
+
+    def bad(ids, E_shard, v0):
+        return orig(ids, E_shard, v0 + 1)                  # off-by-one id offset
+    monkeypatch.setattr(embedding, "shard_lookup", bad)
+    _expect_failure(temb.test_hand_worked_example)
+
+
 def test_bf16_rounding_by_truncation_is_caught(monkeypatch):
     def bad(x):
         f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
