@@ -254,6 +254,7 @@ def run_ours(args, dist):
         comps["shard_reduce"] = bench_shard_reduce(ttl, torch, dev, pk, args)
         comps["gtp_chain"] = bench_gtp(ttl, torch, dev, pk, args)
         comps["vocab_ce"] = bench_ce(ttl, torch, dev, pk, args)
+        comps["vocab_embedding"] = bench_embedding(ttl, torch, dev, pk, args)
 
     out = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": dist.world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
@@ -443,37 +444,78 @@ def bench_ce(ttl, torch, dev, pk, args):
     W = [(torch.randn((V // t, h), generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(t)]
     target = torch.randint(0, V, (T,), generator=g, device=dev)
     out = ttl.ce_buffers(t, T, h, V, dev)
-    for _ in range(2):
-        ttl.vocab_parallel_ce(H, W, target, out=out)
-    torch.cuda.synchronize()
-    reps = 3
-    ttl.trace_enable(True, 4096)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        ttl.vocab_parallel_ce(H, W, target, out=out)
-    e1.record()
-    torch.cuda.synchronize()
-    recs = ttl.trace_read(4096)
-    ttl.trace_enable(False)
-    wall = e0.elapsed_time(e1) / reps
+    res = {"workload": "vocab_parallel_ce_t8_T8192_h4096_V151936"}
+    for mode, fused in (("fused_stats", True), ("separate_stats", False)):
+        for _ in range(2):
+            ttl.vocab_parallel_ce(H, W, target, out=out, fused_stats=fused)
+        torch.cuda.synchronize()
+        reps = 3
+        ttl.trace_enable(True, 4096)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            ttl.vocab_parallel_ce(H, W, target, out=out, fused_stats=fused)
+        e1.record()
+        torch.cuda.synchronize()
+        recs = ttl.trace_read(4096)
+        ttl.trace_enable(False)
+        wall = e0.elapsed_time(e1) / reps
 
-    def agg(kind, flops=False):
-        rr = [r for r in recs if r[0] == kind]
-        if not rr:
-            return None
-        ms = sum(r[1] for r in rr)
-        if flops:
-            v = sum(r[2] for r in rr) / (ms * 1e-3) / 1e12
-            return {"tflops": round(v, 1), "frac": round(v / pk["bf16_tflops_sustained"], 4),
-                    "ms": round(ms / reps, 3)}
-        v = sum(r[3] for r in rr) / (ms * 1e-3) / 1e9
-        return {"gbs": round(v, 1), "frac": round(v / pk["hbm_gbs"], 4), "ms": round(ms / reps, 3)}
+        def agg(kind, flops=False):
+            rr = [r for r in recs if r[0] == kind]
+            if not rr:
+                return None
+            ms = sum(r[1] for r in rr)
+            if flops:
+                v = sum(r[2] for r in rr) / (ms * 1e-3) / 1e12
+                return {"tflops": round(v, 1), "frac": round(v / pk["bf16_tflops_sustained"], 4),
+                        "ms": round(ms / reps, 3)}
+            v = sum(r[3] for r in rr) / (ms * 1e-3) / 1e9
+            return {"gbs": round(v, 1), "frac": round(v / pk["hbm_gbs"], 4), "ms": round(ms / reps, 3)}
 
-    res = {"workload": "vocab_parallel_ce_t8_T8192_h4096_V151936", "ms_per_fwd_bwd": round(wall, 3),
-           "loss": float(out["loss"].item()), "gemm": agg("gemm", True), "stats": agg("ce_stats"),
-           "dlogits": agg("ce_dlogits"), "combine_mean": agg("ce_small")}
+        res[mode] = {"ms_per_fwd_bwd": round(wall, 3), "loss": float(out["loss"].item()),
+                     "gemm": agg("gemm", True), "stats": agg("ce_stats"), "dlogits": agg("ce_dlogits"),
+                     "combine_mean": agg("ce_small")}
     del H, W, target, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_embedding(ttl, torch, dev, pk, args):
+    """Vocab-parallel embedding: 151936 x 4096 table in 8 vocab shards, 8192 token ids."""
+    t, T, h, V = 8, 8192, 4096, 151936
+    g = torch.Generator(device=dev).manual_seed(6)
+    E = [(torch.randn((V // t, h), generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(t)]
+    ids = torch.randint(0, V, (T,), generator=g, device=dev)
+    dY = torch.randn((T, h), generator=g, device=dev).to(torch.bfloat16)
+    out = [torch.empty((T, h), device=dev, dtype=torch.bfloat16) for _ in range(t)]
+    dE = [torch.zeros((V // t, h), device=dev) for _ in range(t)]
+    flush = [torch.zeros(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev) for _ in range(2)]
+    reps = 5
+    res = {"workload": "vocab_parallel_embedding_t8_T8192_h4096_V151936",
+           "l2": "flushed before each timed launch by a 512 MiB write followed by a 512 MiB read"}
+    for name, fn in (("fwd_literal", lambda: ttl.vocab_parallel_embedding_fwd(ids, E, out=out, literal=True)),
+                     ("fwd_fused", lambda: ttl.vocab_parallel_embedding_fwd(ids, E, out=out, literal=False)),
+                     ("bwd", lambda: ttl.vocab_parallel_embedding_bwd(ids, dY, dE))):
+        fn()
+        torch.cuda.synchronize()
+        ttl.trace_enable(True, 1024)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ms = 0.0
+        for _ in range(reps):
+            _flush(torch, flush)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+        recs = ttl.trace_read(1024)
+        ttl.trace_enable(False)
+        by = sum(r[3] for r in recs) / reps
+        kms = sum(r[1] for r in recs) / reps
+        res[name] = {"ms": round(ms / reps, 4), "kernel_gbs": round(by / (kms * 1e-3) / 1e9, 1),
+                     "frac": round(by / (kms * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "launches": len(recs) // reps}
+    del E, ids, dY, out, dE, flush
     torch.cuda.empty_cache()
     return res
 

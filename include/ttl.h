@@ -87,6 +87,7 @@ int ttl_selftest_wait_timeout(int64_t timeout_us, void* stream);
 #define TTL_K_CE_SMALL 6    /* CE combine and mean                            */
 #define TTL_K_CE_DLOGITS 7  /* CE dlogits                                     */
 #define TTL_K_OTHER 8       /* column sums, zero fills                        */
+#define TTL_K_EMBED 9       /* vocab-parallel embedding lookup / gradient     */
 
 /* Starts (on != 0) or stops tracing on this process.  While on, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the launch stream, and
@@ -127,7 +128,8 @@ int ttl_shard_reduce_scatter(int t, int64_t rows, int64_t cols, ttl_bf16* const*
 int ttl_shard_all_gather(int t, int64_t rows, int64_t cols, ttl_bf16* const* bufs, void* stream);
 
 /* All-reduce = reduce-scatter + all-gather, fused into one pass: every buffer ends with
- * the same bits the two phases would give. */
+ * the same bits the two phases would give.  Having no slabs to own, it accepts any number of
+ * rows (t need not divide rows). */
 int ttl_shard_all_reduce(int t, int64_t rows, int64_t cols, ttl_bf16* const* bufs, const ttl_bf16* bias,
                          void* stream);
 
@@ -245,11 +247,40 @@ int ttl_gtp_wgrad_rs_finalize(int g, int64_t M, int64_t K, int64_t N, const ttl_
  *              target logit (0 if not owned); row 3t = log-sum-exp; row 3t+1 = loss per token
  *   loss       [1] fp32 out: mean over the T tokens
  *   dH         [T,h] bf16 out: sum_i dlogits_i W_i
+ *   ws         optional workspace of ttl_vocab_parallel_ce_workspace_size() bytes.  With it,
+ *              the LM-head GEMM's epilogue computes each row's max and sum of exponentials
+ *              tile by tile while it writes the logits, so the statistics never re-read the
+ *              fp32 logits; with ws = NULL a separate pass scans them.  Same results.
  * t in 1..TTL_MAX_SHARDS divides V; V/t a multiple of 8.  A target outside [0,V) sets
  * TTL_ERR_DEVICE in the status word and that token's loss to NaN. */
 int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, const ttl_bf16* H, const ttl_bf16* const* W,
                           const int64_t* target, float* const* logits, ttl_bf16* const* dlogits, float* stats,
-                          float* loss, ttl_bf16* dH, int flags, void* stream);
+                          float* loss, ttl_bf16* dH, void* ws, size_t ws_bytes, int flags, void* stream);
+
+/* Bytes of the optional ttl_vocab_parallel_ce workspace: per token, 8 bytes for each 256-wide
+ * column tile of every vocab shard, plus 4; 0 for invalid arguments. */
+size_t ttl_vocab_parallel_ce_workspace_size(int t, int64_t T, int64_t h, int64_t V);
+
+/* ------------------------------------------------------------------ vocab-parallel embedding */
+
+/* Embedding lookup with the table split by vocabulary rows.  [TPSP] "Embedding 和 LM head:按
+ * vocab 切": a shard outputs 0 for tokens whose id it does not own and the all-reduce of the
+ * t outputs gives every token its own row.  Shard i owns ids [i V/t, (i+1) V/t).
+ *   ids    [T] int64 in [0,V)   E[i] [V/t,h] bf16   out[i] [T,h] bf16 (every buffer ends
+ *   with the looked-up rows)
+ *   literal = 1: masked per-shard lookups, then the on-device all-reduce of the t buffers;
+ *   literal = 0: one pass that copies each token's row from its owning shard into all t
+ *                buffers (the same bits, without the all-reduce's traffic).
+ * An id outside [0,V) sets TTL_ERR_DEVICE in the status word and gives a zero row. */
+int ttl_vocab_parallel_embedding_fwd(int t, int64_t T, int64_t h, int64_t V, const int64_t* ids,
+                                     const ttl_bf16* const* E, ttl_bf16* const* out, int literal, void* stream);
+
+/* Backward: the all-reduce's backward is the identity, so shard i accumulates
+ *   dE[i][id - i V/t] += dY[tok]   for every token whose id it owns
+ * into fp32 dE[i] [V/t,h] (zero it first for a fresh gradient).  Tokens sharing an id are
+ * summed with atomic adds, so the fp32 summation order is not fixed. */
+int ttl_vocab_parallel_embedding_bwd(int t, int64_t T, int64_t h, int64_t V, const int64_t* ids,
+                                     const ttl_bf16* dY, float* const* dE, void* stream);
 
 #ifdef __cplusplus
 }

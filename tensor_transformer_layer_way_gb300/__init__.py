@@ -12,4 +12,4 @@ from ._binding import (  # noqa: F401
     exported_symbols, gemm, gtp_gather, gtp_gather_gemm, gtp_wgrad_rs_finalize, last_error, lib, mlp_bwd_buffers,
     mlp_fwd_buffers, selftest_wait_timeout, shard_all_gather, shard_all_reduce, shard_reduce_scatter, tp_mlp_bwd,
     tp_mlp_bwd_static_ws, tp_mlp_bwd_workspace_size, tp_mlp_fwd, trace_enable, trace_read, version,
-    vocab_parallel_ce)
+    vocab_parallel_ce, vocab_parallel_embedding_bwd, vocab_parallel_embedding_fwd)

@@ -55,7 +55,11 @@ _SIGS = {
     "ttl_gtp_gather": (_int, [_int, _i64, _i64, _vp, _vp, _vp, _vp]),
     "ttl_gtp_gather_gemm": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp]),
     "ttl_gtp_wgrad_rs_finalize": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp, _vp]),
-    "ttl_vocab_parallel_ce": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp]),
+    "ttl_vocab_parallel_ce": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     ctypes.c_size_t, _int, _vp]),
+    "ttl_vocab_parallel_ce_workspace_size": (ctypes.c_size_t, [_int, _i64, _i64, _i64]),
+    "ttl_vocab_parallel_embedding_fwd": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _int, _vp]),
+    "ttl_vocab_parallel_embedding_bwd": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -152,7 +156,8 @@ def selftest_wait_timeout(timeout_us: int, stream=None) -> int:
     return lib().ttl_selftest_wait_timeout(int(timeout_us), _stream(stream))
 
 
-KERNEL_KINDS = ["gemm", "reduce", "gather", "gtp_gather", "finalize", "ce_stats", "ce_small", "ce_dlogits", "other"]
+KERNEL_KINDS = ["gemm", "reduce", "gather", "gtp_gather", "finalize", "ce_stats", "ce_small", "ce_dlogits", "other",
+                "embed"]
 
 
 def trace_enable(on: bool = True, capacity: int = 65536):
@@ -369,18 +374,28 @@ def gtp_wgrad_rs_finalize(X, dY, staging_cur, *, staging_prev=None, main_grad_pr
 
 # ------------------------------------------------------------------ vocab-parallel CE
 
-def ce_buffers(t, T, h, V, device="cuda"):
+def ce_workspace_size(t, T, h, V) -> int:
+    return int(lib().ttl_vocab_parallel_ce_workspace_size(t, T, h, V))
+
+
+def ce_buffers(t, T, h, V, device="cuda", fused_stats=True):
+    """Allocates (with torch) the CE outputs and, for fused statistics, its workspace."""
     Vs = V // t
-    return {"logits": [torch.empty(T, Vs, device=device, dtype=torch.float32) for _ in range(t)],
-            "dlogits": [torch.empty(T, Vs, device=device, dtype=torch.bfloat16) for _ in range(t)],
-            "stats": torch.empty((3 * t + 2) * T, device=device, dtype=torch.float32),
-            "loss": torch.empty(1, device=device, dtype=torch.float32),
-            "dH": torch.empty(T, h, device=device, dtype=torch.bfloat16)}
+    out = {"logits": [torch.empty(T, Vs, device=device, dtype=torch.float32) for _ in range(t)],
+           "dlogits": [torch.empty(T, Vs, device=device, dtype=torch.bfloat16) for _ in range(t)],
+           "stats": torch.empty((3 * t + 2) * T, device=device, dtype=torch.float32),
+           "loss": torch.empty(1, device=device, dtype=torch.float32),
+           "dH": torch.empty(T, h, device=device, dtype=torch.bfloat16), "ws": None}
+    if fused_stats:
+        out["ws"] = torch.empty(max(ce_workspace_size(t, T, h, V), 16), device=device, dtype=torch.uint8)
+    return out
 
 
-def vocab_parallel_ce(H, W, target, *, out=None, flags=0, stream=None):
-    """Vocab-parallel LM head + CE over len(W) vocab shards (each [V/t, h]).
-    Returns dict logits, dlogits, stats, loss, dH."""
+def vocab_parallel_ce(H, W, target, *, out=None, flags=0, fused_stats=True, stream=None):
+    """Vocab-parallel LM head + CE over len(W) vocab shards (each [V/t, h]).  fused_stats: the
+    LM-head GEMM epilogue computes the per-row statistics (needs the workspace ce_buffers
+    allocates); otherwise a separate pass re-reads the logits.
+    Returns dict logits, dlogits, stats, loss, dH (and ws)."""
     t = len(W)
     T, h = H.shape
     Vs = W[0].shape[0]
@@ -389,10 +404,42 @@ def vocab_parallel_ce(H, W, target, *, out=None, flags=0, stream=None):
     _need_list(W, "W", t, shape=(Vs, h))
     _need(target, "target", torch.int64, (T,))
     if out is None:
-        out = ce_buffers(t, T, h, V, H.device)
+        out = ce_buffers(t, T, h, V, H.device, fused_stats)
     fwd_only = bool(flags & CE_FORWARD_ONLY)
+    ws = out.get("ws") if fused_stats else None
     _check(lib().ttl_vocab_parallel_ce(t, T, h, V, _p(H), _arr(W), _p(target), _arr(out["logits"]),
                                        None if fwd_only else _arr(out["dlogits"]), _p(out["stats"]),
-                                       _p(out["loss"]), None if fwd_only else _p(out["dH"]), int(flags),
-                                       _stream(stream)))
+                                       _p(out["loss"]), None if fwd_only else _p(out["dH"]), _p(ws),
+                                       0 if ws is None else ws.numel(), int(flags), _stream(stream)))
     return out
+
+
+# ------------------------------------------------------------------ vocab-parallel embedding
+
+def vocab_parallel_embedding_fwd(ids, E, *, out=None, literal=True, stream=None):
+    """Lookup with the table split into len(E) vocab shards ([V/t, h] each).  Returns the t
+    output buffers [T, h], each holding every token's row (literal: masked lookups + the
+    all-reduce; otherwise one fused gather pass with the same bits)."""
+    t = len(E)
+    Vs, h = E[0].shape
+    T = ids.shape[0]
+    _need(ids, "ids", torch.int64, (T,))
+    _need_list(E, "E", t, shape=(Vs, h))
+    if out is None:
+        out = [torch.empty((T, h), device=ids.device, dtype=torch.bfloat16) for _ in range(t)]
+    _need_list(out, "out", t, shape=(T, h))
+    _check(lib().ttl_vocab_parallel_embedding_fwd(t, T, h, Vs * t, _p(ids), _arr(E), _arr(out), int(bool(literal)),
+                                                  _stream(stream)))
+    return out
+
+
+def vocab_parallel_embedding_bwd(ids, dY, dE, *, stream=None):
+    """Accumulates dY rows into the owning shard's fp32 gradient dE[i] ([V/t, h])."""
+    t = len(dE)
+    Vs, h = dE[0].shape
+    T = ids.shape[0]
+    _need(ids, "ids", torch.int64, (T,))
+    _need(dY, "dY", shape=(T, h))
+    _need_list(dE, "dE", t, torch.float32, (Vs, h))
+    _check(lib().ttl_vocab_parallel_embedding_bwd(t, T, h, Vs * t, _p(ids), _p(dY), _arr(dE), _stream(stream)))
+    return dE

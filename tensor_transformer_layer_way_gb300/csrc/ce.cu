@@ -87,6 +87,35 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const __grid_constant__ C
   }
 }
 
+// Fused path, grid (T, t), one warp: shard i's statistics for token `tok` from the per-tile
+// partials the LM-head GEMM epilogue left (tps tiles per shard, ntot per token row), and the
+// target logit the owning tile wrote.
+__global__ void __launch_bounds__(32) ce_stats_from_partials_kernel(const float2* part, const float* ztarget,
+                                                                    const int64_t* target, int64_t T, int64_t Vs,
+                                                                    int64_t V, int tps, int64_t ntot, float* stats) {
+  const int64_t tok = blockIdx.x;
+  const int i = blockIdx.y;
+  const float2* p = part + tok * ntot + static_cast<int64_t>(i) * tps;
+  float m = -INFINITY, s = 0.0f;
+  for (int j = threadIdx.x; j < tps; j += 32) {
+    const float2 q = p[j];
+    online_merge(m, s, q.x, q.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    online_merge(m, s, m2, s2);
+  }
+  if (threadIdx.x == 0) {
+    const int64_t tg = target[tok];
+    const bool own = tg >= 0 && tg < V && tg / Vs == i;
+    stats[(3 * i + 0) * T + tok] = m;
+    stats[(3 * i + 1) * T + tok] = s;
+    stats[(3 * i + 2) * T + tok] = own ? ztarget[tok] : 0.0f;
+  }
+}
+
 __global__ void ce_combine_kernel(int t, int64_t T, int64_t V, const int64_t* target, float* stats, int* status) {
   const int64_t tok = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (tok >= T) return;
@@ -157,10 +186,25 @@ __global__ void __launch_bounds__(256) ce_dlogits_kernel(const __grid_constant__
 
 using namespace ttl;
 
+namespace {
+// Fused-statistics workspace: per token, one (max, sum exp) pair per GEMM n-tile of every
+// shard, then one target logit per token.
+int64_t ce_tiles_per_shard(int64_t Vs) { return (Vs + kGemmBN - 1) / kGemmBN; }
+size_t ce_part_bytes(int t, int64_t T, int64_t Vs) {
+  return (static_cast<size_t>(T) * static_cast<size_t>(t * ce_tiles_per_shard(Vs)) * 8 + 255) & ~size_t(255);
+}
+}  // namespace
+
+extern "C" size_t ttl_vocab_parallel_ce_workspace_size(int t, int64_t T, int64_t h, int64_t V) {
+  (void)h;
+  if (t < 1 || t > kMaxShards || T < 0 || V < 0 || V % t) return 0;
+  return ce_part_bytes(t, T, V / t) + static_cast<size_t>(T) * 4;
+}
+
 extern "C" int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, const ttl_bf16* H,
                                      const ttl_bf16* const* W, const int64_t* target, float* const* logits,
-                                     ttl_bf16* const* dlogits, float* stats, float* loss, ttl_bf16* dH, int flags,
-                                     void* stream) {
+                                     ttl_bf16* const* dlogits, float* stats, float* loss, ttl_bf16* dH, void* ws,
+                                     size_t ws_bytes, int flags, void* stream) {
   const char* name = "ttl_vocab_parallel_ce";
   if (t < 1 || t > kMaxShards) return set_error(TTL_ERR_ARG, "%s: t=%d outside [1,%d]", name, t, kMaxShards);
   if (T < 0 || h < 0 || V < 0) return set_error(TTL_ERR_ARG, "%s: negative shape", name);
@@ -182,6 +226,13 @@ extern "C" int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, con
     if (!aligned16(W[i]) || !aligned16(logits[i]) || (!fwd_only && !aligned16(dlogits[i])))
       return set_error(TTL_ERR_ALIGN, "%s: shard %d pointer not 16-byte aligned", name, i);
   }
+  const bool fused = ws != nullptr;
+  if (fused) {
+    const size_t need = ttl_vocab_parallel_ce_workspace_size(t, T, h, V);
+    if (ws_bytes < need)
+      return set_error(TTL_ERR_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
+    if (!aligned16(ws)) return set_error(TTL_ERR_ALIGN, "%s: workspace not 16-byte aligned", name);
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int rc;
   if (T == 0) {
@@ -192,26 +243,43 @@ extern "C" int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, con
   if ((rc = require_sm103())) return rc;
   int* status = device_status_ptr();
   if (!status) return TTL_ERR_CUDA;
+  const int tps = static_cast<int>(ce_tiles_per_shard(Vs));
+  const int64_t ntot = static_cast<int64_t>(t) * tps;
+  float2* part = fused ? static_cast<float2*>(ws) : nullptr;
+  float* ztarget = fused ? reinterpret_cast<float*>(static_cast<char*>(ws) + ce_part_bytes(t, T, Vs)) : nullptr;
 
-  // 1. logits Z_i = H W_i^T (fp32).
+  // 1. logits Z_i = H W_i^T (fp32).  With a workspace, the epilogue also leaves per-tile
+  //    (max, sum exp) partials and the target logit, so step 2 need not re-read the logits.
   {
     GemmBatch batch;
     const int mh = batch.add_map(H, T, h, h, false);
     for (int i = 0; i < t; ++i) {
       const int mw = batch.add_map(W[i], Vs, h, h, false);
-      Problem* p = batch.add_problem(T, Vs, false, false, EPI_F32, false, i > 0);
+      Problem* p = batch.add_problem(T, Vs, false, false, fused ? EPI_F32_CE : EPI_F32, false, i > 0);
       if (batch.error()) return batch.error();
       p->out0 = logits[i];
       p->ld_out = Vs;
+      if (fused) {
+        p->aux0 = target;
+        p->ext0 = static_cast<int64_t>(i) * Vs;
+        p->out1 = part;
+        p->ext1 = ntot;
+        p->out2 = ztarget;
+      }
       if ((rc = batch.add_seg(p, mh, 0, mw, -1, 0, h))) return rc;
     }
     if ((rc = batch.launch(s))) return rc;
   }
 
   // 2. per-shard statistics.
-  CeShards cs;
-  for (int i = 0; i < kMaxShards; ++i) cs.z[i] = i < t ? logits[i] : nullptr;
-  {
+  if (fused) {
+    TraceScope trace(s, TTL_K_CE_STATS, 0.0, static_cast<double>(T) * (ntot * 8.0 + 4.0 + 3.0 * t * 4.0));
+    ce_stats_from_partials_kernel<<<dim3(static_cast<unsigned>(T), t), 32, 0, s>>>(part, ztarget, target, T, Vs, V,
+                                                                                  tps, ntot, stats);
+    if ((rc = cuda_check(cudaGetLastError(), "ce_stats_from_partials_kernel launch"))) return rc;
+  } else {
+    CeShards cs;
+    for (int i = 0; i < kMaxShards; ++i) cs.z[i] = i < t ? logits[i] : nullptr;
     TraceScope trace(s, TTL_K_CE_STATS, 0.0, static_cast<double>(T) * V * 4.0);
     ce_stats_kernel<<<dim3(static_cast<unsigned>(T), t), 256, 0, s>>>(cs, target, T, Vs, stats);
     if ((rc = cuda_check(cudaGetLastError(), "ce_stats_kernel launch"))) return rc;

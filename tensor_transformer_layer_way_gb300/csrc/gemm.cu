@@ -41,7 +41,7 @@
 
 namespace ttl {
 
-constexpr int BN = 256;            // accumulator columns per tile
+constexpr int BN = kGemmBN;        // accumulator columns per tile
 constexpr int BK = 64;             // K per stage
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int GROUP_M = 16;
@@ -203,6 +203,11 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
     }
     return;
   }
+  // EPI_F32_CE state: this row's running max and sum of exponentials over the tile, and the
+  // target's column relative to this tile's first column.
+  float ce_m = -INFINITY, ce_s = 0.0f;
+  int64_t ce_tgt = -1;
+  if (epi == EPI_F32_CE && row_ok) ce_tgt = reinterpret_cast<const int64_t*>(pr.aux0)[row] - pr.ext0 - n_base;
 #pragma unroll 1
   for (int ch = 0; ch < BN / 32; ++ch) {
     uint32_t r[32];
@@ -216,6 +221,24 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
       if (epi == EPI_F32) {
         store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
+      } else if (epi == EPI_F32_CE) {
+        store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
+        const int nv = min(32, pr.N - col0);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nv) mx = fmaxf(mx, v[j]);
+        if (mx > ce_m) {
+          ce_s *= __expf(ce_m - mx);
+          ce_m = mx;
+        }
+        float se = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < nv) se += __expf(v[j] - ce_m);
+          if (ce_tgt == ch * 32 + j && j < nv) reinterpret_cast<float*>(pr.out2)[row] = v[j];
+        }
+        ce_s += se;
       } else if (epi == EPI_BF16 || epi == EPI_GELU_FWD) {
         if (pr.bias0) {
           float b[32];
@@ -249,6 +272,10 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
         store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
       }
     }
+  }
+  if (epi == EPI_F32_CE && row_ok) {
+    const int64_t gt = pr.tn0 + n_base / BN;   // this tile's index among the group's n-tiles
+    reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + gt] = make_float2(ce_m, ce_s);
   }
 }
 
@@ -683,7 +710,7 @@ int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b
   if (p->nseg == 1) {
     const int nout = p->epi == EPI_SWIGLU_FWD ? 3 : (p->epi == EPI_GELU_FWD || p->epi == EPI_SWIGLU_BWD) ? 2 : 1;
     const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : p->epi == EPI_GELU_BWD ? 1 : 0;
-    const double esz = p->epi == EPI_F32 ? 4.0 : 2.0;
+    const double esz = (p->epi == EPI_F32 || p->epi == EPI_F32_CE) ? 4.0 : 2.0;
     bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux);
   }
   return TTL_OK;

@@ -176,7 +176,10 @@ int run(Mode m, int t, int64_t rows, int64_t cols, ttl_bf16* const* bufs, const 
   if (rows < 0 || cols < 0) return set_error(TTL_ERR_ARG, "%s: negative shape", name);
   if (!bufs) return set_error(TTL_ERR_ARG, "%s: null buffer array", name);
   if (cols % 8) return set_error(TTL_ERR_SHAPE, "%s: cols=%lld must be a multiple of 8", name, (long long)cols);
-  if (rows % t) return set_error(TTL_ERR_SHAPE, "%s: t=%d must divide rows=%lld", name, t, (long long)rows);
+  // Slab ownership needs t | rows; the fused all-reduce writes every row of every buffer and
+  // accepts any row count.
+  if (m != Mode::AR && rows % t)
+    return set_error(TTL_ERR_SHAPE, "%s: t=%d must divide rows=%lld", name, t, (long long)rows);
   if (rows == 0 || cols == 0) return TTL_OK;   // empty buffers (their pointers may be null)
   ShardSet S;
   for (int j = 0; j < kMaxShards; ++j) S.p[j] = nullptr;

@@ -48,6 +48,7 @@ struct TraceScope {
 
 // ------------------------------------------------------------------ GEMM problem block
 
+constexpr int kGemmBN = 256;   // accumulator columns per GEMM tile
 constexpr int kMaxMaps = 40;
 constexpr int kMaxProblems = 32;
 constexpr int kMaxSegs = kMaxShards;
@@ -59,6 +60,10 @@ enum Epilogue : int {
   EPI_SWIGLU_FWD = 3,  // paired tile: out0 = G, out1 = V, out2 = SiLU(G) * V
   EPI_GELU_BWD = 4,    // out0 = bf16(acc * GeLU'(aux0))                          (dU)
   EPI_SWIGLU_BWD = 5,  // out0 = bf16(acc * aux1 * SiLU'(aux0)), out1 = bf16(acc * SiLU(aux0))
+  EPI_F32_CE = 6,      // out0 = acc (fp32 logits) and, per row and tile, the cross-entropy
+                       // partials: out1[row * ext1 + tn0 + tn] = (max, sum exp(z - max)) over
+                       // the tile's columns; out2[row] = the logit at target aux0[row] - ext0
+                       // when that column is in the tile
 };
 
 // One K-range of a problem: k-blocks of 64 read from map_a at K offset a_k0 and from
@@ -90,6 +95,7 @@ struct Problem {
   const void* bias0;
   int64_t ld_out;         // row stride (elements) of out0/out1/out2
   int64_t ld_aux;         // row stride (elements) of aux0/aux1
+  int64_t ext0, ext1;     // epilogue-specific integers (EPI_F32_CE: vocab offset, row stride of out1)
 };
 
 // Consecutive problems with the same M that read the same A rows form one tile group: its

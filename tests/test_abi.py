@@ -95,9 +95,20 @@ def test_gtp_and_ce_validation(lib):
     W = _arr(0x10000, 0x20000)
     L = _arr(0x30000, 0x40000)
     # t does not divide V
-    assert lib.ttl_vocab_parallel_ce(2, 8, 64, 33, 0x90000, W, 0xA0000, L, L, 0xB0000, 0xC0000, 0xD0000, 0, None) == 2
+    assert lib.ttl_vocab_parallel_ce(2, 8, 64, 33, 0x90000, W, 0xA0000, L, L, 0xB0000, 0xC0000, 0xD0000,
+                                     None, 0, 0, None) == 2
     # unknown flag
-    assert lib.ttl_vocab_parallel_ce(2, 8, 64, 32, 0x90000, W, 0xA0000, L, L, 0xB0000, 0xC0000, 0xD0000, 8, None) == 1
+    assert lib.ttl_vocab_parallel_ce(2, 8, 64, 32, 0x90000, W, 0xA0000, L, L, 0xB0000, 0xC0000, 0xD0000,
+                                     None, 0, 8, None) == 1
+    # workspace too small for the fused statistics
+    need = lib.ttl_vocab_parallel_ce_workspace_size(2, 8, 64, 32)
+    assert need == 256 + 8 * 4        # 8 tokens x 2 tiles x 8 bytes, rounded to 256, + 8 target logits
+    assert lib.ttl_vocab_parallel_ce(2, 8, 64, 32, 0x90000, W, 0xA0000, L, L, 0xB0000, 0xC0000, 0xD0000,
+                                     0xE0000, need - 1, 0, None) == 1
+    # embedding: t does not divide V, misaligned ids
+    assert lib.ttl_vocab_parallel_embedding_fwd(2, 8, 64, 33, 0x10000, W, L, 1, None) == 2
+    assert lib.ttl_vocab_parallel_embedding_fwd(2, 8, 64, 32, 0x10004, W, L, 1, None) == 3
+    assert lib.ttl_vocab_parallel_embedding_bwd(2, 8, 64, 32, 0x10000, 0x20000, None, None) == 1
     # zero tokens would write the loss with a device copy: not on a CPU host, so only shape checks here
     assert lib.ttl_gemm(8, 12, 16, 0x10000, 16, 1, 0x20000, 16, 1, 0x30000, 12, 0, None) == 2
 

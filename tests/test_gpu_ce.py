@@ -11,16 +11,18 @@ from parity import assert_fp32_close, assert_gemm_close, dev, f32, f64
 pytestmark = pytest.mark.gpu
 
 
-def _run(H, W, target, t, flags=0):
+def _run(H, W, target, t, flags=0, fused=True):
     Ws = dev([w.contiguous() for w in W.chunk(t, 0)])
-    out = ttl.vocab_parallel_ce(dev(H), Ws, dev(target), flags=flags)
+    out = ttl.vocab_parallel_ce(dev(H), Ws, dev(target), flags=flags, fused_stats=fused)
     return out
 
 
-@pytest.mark.parametrize("t,T,h,V", [(1, 64, 64, 512), (4, 100, 64, 4 * 296), (8, 130, 136, 8 * 48)])
-def test_small_full_parity(t, T, h, V):
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("t,T,h,V", [(1, 64, 64, 512), (4, 100, 64, 4 * 296), (8, 130, 136, 8 * 48),
+                                     (2, 300, 64, 2 * 600)])
+def test_small_full_parity(t, T, h, V, fused):
     inp = si.ce_inputs(T, h, V, seed=t + T)
-    out = _run(inp["H"], inp["W"], inp["target"], t)
+    out = _run(inp["H"], inp["W"], inp["target"], t, fused=fused)
     assert ttl.device_status() == 0
     ref = vocab_ce.vocab_parallel_ce(f64(inp["H"]), f64(inp["W"]), inp["target"].numpy(), t)
     Vs = V // t
@@ -64,11 +66,29 @@ def test_all_zero_logits_give_log_v():
     assert dZ.sum(1).abs().max().item() <= 2.0 ** -8 / T
 
 
-def test_vocab_parallel_ce_full_size_sampled():
+def test_fused_and_separate_statistics_agree():
+    t, T, h, V = 8, 256, 128, 8 * 520
+    inp = si.ce_inputs(T, h, V, seed=3)
+    a = _run(inp["H"], inp["W"], inp["target"], t, fused=True)
+    b = _run(inp["H"], inp["W"], inp["target"], t, fused=False)
+    assert ttl.device_status() == 0
+    for i in range(t):
+        assert torch.equal(a["logits"][i], b["logits"][i])
+    sa = f32(a["stats"]).reshape(3 * t + 2, T)
+    sb = f32(b["stats"]).reshape(3 * t + 2, T)
+    for i in range(t):
+        np.testing.assert_array_equal(sa[3 * i], sb[3 * i])            # maxima are exact
+        np.testing.assert_array_equal(sa[3 * i + 2], sb[3 * i + 2])    # target logits are copies
+        assert_fp32_close(sa[3 * i + 1], sb[3 * i + 1], f"sumexp[{i}]")
+    assert abs(a["loss"].item() - b["loss"].item()) <= 1e-5 * abs(b["loss"].item())
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_vocab_parallel_ce_full_size_sampled(fused):
     """H [8192, 4096], W [151936, 4096] in 8 vocab shards of 18992 rows (fp32 logits 4.98 GB)."""
     cfg = si.VOCAB_CE_T8
     inp = si.ce_inputs(cfg.T, cfg.h, cfg.V, cfg.seed)
-    out = _run(inp["H"], inp["W"], inp["target"], cfg.t)
+    out = _run(inp["H"], inp["W"], inp["target"], cfg.t, fused=fused)
     assert ttl.device_status() == 0
     rows = si.sample_indices(cfg.T, 48, cfg.seed).numpy()
     ref = vocab_ce.vocab_parallel_ce(f64(inp["H"]), f64(inp["W"]), inp["target"].numpy(), cfg.t, rows=rows)
