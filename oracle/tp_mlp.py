@@ -244,6 +244,46 @@ def mlp_backward_unsharded(X, weights: dict, act: str, dY, b1=None) -> dict:
             "db2": dY.sum(axis=0)}
 
 
+def sp_mlp_forward(X_slabs, weights: dict, t: int, act: str) -> dict:
+    """Sequence-parallel MLP block, literal: the block's input arrives as t token slabs; an
+    all-gather rebuilds the full sequence before the column layer, the row layer's partial
+    sums are reduce-scattered so shard r keeps only the sum of its own token slab.
+
+    Source: the TP/SP page, section "SP": after the row-parallel layer the all-reduce
+    becomes a reduce-scatter that leaves each card its own s/t tokens, and an all-gather
+    before the next column-parallel layer rebuilds the full sequence.
+    Returns the tp_mlp_forward intermediates plus ``Z_slabs``."""
+    X = np.concatenate([_f64(x) for x in X_slabs], axis=0)          # all-gather
+    fwd = tp_mlp_forward(X, weights, t, act)
+    T = X.shape[0]
+    w = T // t
+    fwd["Z_slabs"] = []
+    for r in range(t):                                                # reduce-scatter
+        acc = fwd["P"][0][r * w:(r + 1) * w].copy()
+        for P in fwd["P"][1:]:
+            acc = acc + P[r * w:(r + 1) * w]
+        fwd["Z_slabs"].append(acc)
+    return fwd
+
+
+def sp_mlp_backward(X_slabs, weights: dict, t: int, act: str, dZ_slabs, fwd: dict) -> dict:
+    """Backward of :func:`sp_mlp_forward`: the reduce-scatter's backward is an all-gather of
+    the output-gradient slabs, the all-gather's backward a reduce-scatter of the dX partials.
+    Returns the tp_mlp_backward results plus ``dX_slabs``."""
+    X = np.concatenate([_f64(x) for x in X_slabs], axis=0)
+    dZ = np.concatenate([_f64(d) for d in dZ_slabs], axis=0)         # all-gather of dZ
+    bwd = tp_mlp_backward(X, weights, t, act, dZ, fwd)
+    T = X.shape[0]
+    w = T // t
+    bwd["dX_slabs"] = []
+    for r in range(t):                                                # reduce-scatter of dX
+        acc = bwd["dX_part"][0][r * w:(r + 1) * w].copy()
+        for p in bwd["dX_part"][1:]:
+            acc = acc + p[r * w:(r + 1) * w]
+        bwd["dX_slabs"].append(acc)
+    return bwd
+
+
 def row_then_column_wrong(partials, act):
     """The order the "MLP:先 column,再 row" section rules out: the activation applied to
     each rank's partial sum and the results added, instead of to the sum."""

@@ -213,6 +213,39 @@ def test_backward_matches_finite_differences(act):
                                    rtol=1e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("act", ["gelu_tanh", "swiglu"])
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_sequence_parallel_block_equals_tensor_parallel_block(act, t):
+    """SP only changes how the all-reduce is split (reduce-scatter + all-gather), so its slabs
+    are the slabs of the TP block's results, and the slab traffic per card is the same."""
+    from oracle import accounting
+    rng = np.random.default_rng(40 + t)
+    T, h, f = 4 * t, 6, 8
+    X = rng.standard_normal((T, h))
+    dZ = rng.standard_normal((T, h))
+    if act == "gelu_tanh":
+        W = {"A": rng.standard_normal((h, f)), "B": rng.standard_normal((f, h))}
+    else:
+        W = {"Wg": rng.standard_normal((h, f)), "Wu": rng.standard_normal((h, f)), "Wd": rng.standard_normal((f, h))}
+    w = T // t
+    Xs = [X[r * w:(r + 1) * w] for r in range(t)]
+    dZs = [dZ[r * w:(r + 1) * w] for r in range(t)]
+    sp = tp_mlp.sp_mlp_forward(Xs, W, t, act)
+    ref = tp_mlp.mlp_forward_unsharded(X, W, act)
+    for r in range(t):
+        np.testing.assert_allclose(sp["Z_slabs"][r], ref[r * w:(r + 1) * w], rtol=1e-12, atol=1e-12)
+    spb = tp_mlp.sp_mlp_backward(Xs, W, t, act, dZs, sp)
+    refb = tp_mlp.mlp_backward_unsharded(X, W, act, dZ)
+    for r in range(t):
+        np.testing.assert_allclose(spb["dX_slabs"][r], refb["dX"][r * w:(r + 1) * w], rtol=1e-12, atol=1e-12)
+    name = "dA" if act == "gelu_tanh" else "dWg"
+    np.testing.assert_allclose(np.concatenate(spb[name], axis=1), refb[name], rtol=1e-12, atol=1e-12)
+    # all-reduce = reduce-scatter + all-gather: 56 + 56 = 112 MiB per card at t = 8
+    g = golden("tp_comm_table.json")
+    S = accounting.partial_sum_bytes(1, 4096, 8192)
+    assert accounting.ring_bytes_per_rank(8, S) / 2 / 2 ** 20 == g["sp_split_MiB_t8"][0]
+
+
 def test_sampled_evaluation_equals_full():
     rng = np.random.default_rng(9)
     T, h, f = 16, 8, 24
