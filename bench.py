@@ -251,6 +251,7 @@ def run_ours(args, dist):
 
     comps = {}
     if not args.no_components:
+        comps["sp_mlp"] = bench_sp_mlp(ttl, torch, dev, pk, args)
         comps["shard_reduce"] = bench_shard_reduce(ttl, torch, dev, pk, args)
         comps["gtp_chain"] = bench_gtp(ttl, torch, dev, pk, args)
         comps["vocab_ce"] = bench_ce(ttl, torch, dev, pk, args)
@@ -477,6 +478,53 @@ def bench_ce(ttl, torch, dev, pk, args):
                      "gemm": agg("gemm", True), "stats": agg("ce_stats"), "dlogits": agg("ce_dlogits"),
                      "combine_mean": agg("ce_small")}
     del H, W, target, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_sp_mlp(ttl, torch, dev, pk, args):
+    """The headline workload with sequence parallelism: X and dZ as 8 token slabs of 1024 rows,
+    the all-gather and reduce-scatter folded into the GEMMs (no collective kernel runs)."""
+    t, T, h, f, act = MLP["t"], MLP["T"], MLP["h"], MLP["f"], MLP["act"]
+    fs, slab = f // t, T // t
+    g = torch.Generator(device=dev).manual_seed(MLP["seed"])
+
+    def rnd(shape, std):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    Xs = [rnd((slab, h), 1.0) for _ in range(t)]
+    dZs = [rnd((slab, h), 1.0) for _ in range(t)]
+    Wg = [rnd((h, fs), 0.02) for _ in range(t)]
+    Wu = [rnd((h, fs), 0.02) for _ in range(t)]
+    Wd = [rnd((fs, h), 0.02) for _ in range(t)]
+    fo = ttl.sp_mlp_fwd(Xs, Wg, Wd, act=act, A_up=Wu)
+    bo = ttl.sp_mlp_bwd(Xs, dZs, Wg, Wd, fo, act=act, A_up=Wu)
+
+    def step():
+        ttl.sp_mlp_fwd(Xs, Wg, Wd, act=act, A_up=Wu, out=fo)
+        ttl.sp_mlp_bwd(Xs, dZs, Wg, Wd, fo, act=act, A_up=Wu, out=bo)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 50))
+    ttl.trace_enable(True, 1 << 14)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    recs = ttl.trace_read(1 << 14)
+    ttl.trace_enable(False)
+    ms = e0.elapsed_time(e1) / n
+    gm = [r for r in recs if r[0] == "gemm"]
+    res = {"workload": "qwen3_8b_swiglu_mlp_t8_T8192_sequence_parallel_fwd_bwd", "ms_per_step": round(ms, 4),
+           "tflops": round(MLP_FLOPS / (ms * 1e-3) / 1e12, 1),
+           "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
+           "launches_per_step": len(recs) / n, "collective_kernels_per_step": 0,
+           "frac_of_sustained_bf16": round(MLP_FLOPS / (ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4)}
+    del Xs, dZs, Wg, Wu, Wd, fo, bo
     torch.cuda.empty_cache()
     return res
 

@@ -173,6 +173,36 @@ int ttl_tp_mlp_bwd(int t, int act, int64_t T, int64_t h, int64_t f, const ttl_bf
                    ttl_bf16* const* dA, ttl_bf16* const* dA_up, ttl_bf16* const* dB, ttl_bf16* const* db1,
                    ttl_bf16* db2, ttl_bf16* const* dX, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------ sequence-parallel MLP block */
+
+/* The MLP block with sequence parallelism ([TPSP] "SP"): its input and output are t token
+ * slabs of T/t rows (slab r = rows [r T/t, (r+1) T/t)), held by shard r.  The all-gather
+ * before fc1 and the reduce-scatter after fc2 run inside the GEMMs: fc1 reads X slab by slab
+ * through one tensor map per slab, and output slab r is one accumulator over the t shards'
+ * H_i[slab r] B_i, so no full-shape partial sum is written.  The shard sums are taken in
+ * fp32 inside that accumulator (the literal block rounds each partial to bf16 first).
+ *   X_slabs[r] [T/t,h]; A, A_up, B, U_save, V_save, Hact as for ttl_tp_mlp_fwd (full T rows)
+ *   Z_slabs[r] [T/t,h] out: slab r of the block output
+ * t | T, T/t a multiple of 128, no biases. */
+int ttl_sp_mlp_fwd(int t, int act, int64_t T, int64_t h, int64_t f, const ttl_bf16* const* X_slabs,
+                   const ttl_bf16* const* A, const ttl_bf16* const* A_up, const ttl_bf16* const* B,
+                   ttl_bf16* const* U_save, ttl_bf16* const* V_save, ttl_bf16* const* Hact,
+                   ttl_bf16* const* Z_slabs, void* stream);
+
+/* Workspace bytes of ttl_sp_mlp_bwd (the same per-shard activation gradients as the TP block). */
+size_t ttl_sp_mlp_bwd_workspace_size(int t, int act, int64_t T, int64_t h, int64_t f);
+
+/* Backward of ttl_sp_mlp_fwd: dZ_slabs[r] [T/t,h] in, dX_slabs[r] [T/t,h] out.  The
+ * all-gather of dZ (the reduce-scatter's backward) is folded into the dgrad's operand loads
+ * and the weight gradients' K segments; the reduce-scatter of the dX partials (the
+ * all-gather's backward) into the dX GEMM's K loop over shards.  dA, dA_up, dB as for
+ * ttl_tp_mlp_bwd.  SwiGLU needs 2t <= 16. */
+int ttl_sp_mlp_bwd(int t, int act, int64_t T, int64_t h, int64_t f, const ttl_bf16* const* X_slabs,
+                   const ttl_bf16* const* dZ_slabs, const ttl_bf16* const* A, const ttl_bf16* const* A_up,
+                   const ttl_bf16* const* B, const ttl_bf16* const* U_save, const ttl_bf16* const* V_save,
+                   const ttl_bf16* const* Hact, ttl_bf16* const* dA, ttl_bf16* const* dA_up, ttl_bf16* const* dB,
+                   ttl_bf16* const* dX_slabs, void* ws, size_t ws_bytes, void* stream);
+
 /* Size of the library's own scratch area used by ttl_tp_mlp_bwd_static_ws: 16 MiB. */
 #define TTL_STATIC_WS_BYTES (16u << 20)
 

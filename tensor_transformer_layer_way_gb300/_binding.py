@@ -58,6 +58,10 @@ _SIGS = {
     "ttl_vocab_parallel_ce": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _int, _vp]),
     "ttl_vocab_parallel_ce_workspace_size": (ctypes.c_size_t, [_int, _i64, _i64, _i64]),
+    "ttl_sp_mlp_fwd": (_int, [_int, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ttl_sp_mlp_bwd_workspace_size": (ctypes.c_size_t, [_int, _int, _i64, _i64, _i64]),
+    "ttl_sp_mlp_bwd": (_int, [_int, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                              _vp, _vp, ctypes.c_size_t, _vp]),
     "ttl_vocab_parallel_embedding_fwd": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _int, _vp]),
     "ttl_vocab_parallel_embedding_bwd": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
 }
@@ -295,6 +299,51 @@ def tp_mlp_bwd(X, dY, A, B, fwd, *, act="gelu_tanh", A_up=None, out=None, bias=F
                                 _arr(fwd["V"]), _arr(fwd["H"]), _arr(out["dA"]), _arr(out["dA_up"]), _arr(out["dB"]),
                                 _arr(out["db1"]), _p(out["db2"]), _arr(out["dX"]), _p(ws), ws.numel(),
                                 _stream(stream)))
+    return out
+
+
+def sp_mlp_fwd(X_slabs, A, B, *, act="gelu_tanh", A_up=None, out=None, stream=None):
+    """Sequence-parallel MLP forward: token slabs in ([T/t, h] each), token slabs out, the
+    all-gather and reduce-scatter folded into the GEMMs.  Returns dict U, V, H, Z_slabs."""
+    t = len(A)
+    slab, h = X_slabs[0].shape
+    T = slab * t
+    fs = A[0].shape[1]
+    f = fs * t
+    _need_list(X_slabs, "X_slabs", t, shape=(slab, h))
+    _need_list(A, "A", t, shape=(h, fs))
+    _need_list(B, "B", t, shape=(fs, h))
+    if act == "swiglu":
+        _need_list(A_up, "A_up", t, shape=(h, fs))
+    if out is None:
+        out = mlp_fwd_buffers(t, act, T, h, f, X_slabs[0].device)
+        del out["Z"]                      # SP writes only the t output slabs
+        out["Z_slabs"] = [torch.empty((slab, h), device=X_slabs[0].device, dtype=torch.bfloat16) for _ in range(t)]
+    _check(lib().ttl_sp_mlp_fwd(t, ACT[act], T, h, f, _arr(X_slabs), _arr(A), _arr(A_up), _arr(B), _arr(out["U"]),
+                                _arr(out["V"]), _arr(out["H"]), _arr(out["Z_slabs"]), _stream(stream)))
+    return out
+
+
+def sp_mlp_bwd(X_slabs, dZ_slabs, A, B, fwd, *, act="gelu_tanh", A_up=None, out=None, stream=None):
+    """Sequence-parallel MLP backward.  Returns dict dA, dA_up, dB, dX_slabs."""
+    t = len(A)
+    slab, h = X_slabs[0].shape
+    T = slab * t
+    fs = A[0].shape[1]
+    f = fs * t
+    _need_list(dZ_slabs, "dZ_slabs", t, shape=(slab, h))
+    dev = X_slabs[0].device
+    if out is None:
+        e = dict(device=dev, dtype=torch.bfloat16)
+        out = {"dA": [torch.empty(h, fs, **e) for _ in range(t)], "dB": [torch.empty(fs, h, **e) for _ in range(t)],
+               "dA_up": [torch.empty(h, fs, **e) for _ in range(t)] if act == "swiglu" else None,
+               "dX_slabs": [torch.empty(slab, h, **e) for _ in range(t)]}
+        ws = int(lib().ttl_sp_mlp_bwd_workspace_size(t, ACT[act], T, h, f))
+        out["ws"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+    ws = out["ws"]
+    _check(lib().ttl_sp_mlp_bwd(t, ACT[act], T, h, f, _arr(X_slabs), _arr(dZ_slabs), _arr(A), _arr(A_up), _arr(B),
+                                _arr(fwd["U"]), _arr(fwd["V"]), _arr(fwd["H"]), _arr(out["dA"]), _arr(out["dA_up"]),
+                                _arr(out["dB"]), _arr(out["dX_slabs"]), _p(ws), ws.numel(), _stream(stream)))
     return out
 
 

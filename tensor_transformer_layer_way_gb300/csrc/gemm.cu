@@ -347,10 +347,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.probs[c.p];
-        const int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
+        int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
+        int slab = 0;
+        if (pr.a_slab_rows > 0) {   // rows of token slab `slab` come from its own map
+          slab = am / pr.a_slab_rows;
+          am -= slab * pr.a_slab_rows;
+        }
         for (int s = 0; ok && s < pr.nseg; ++s) {
           const Seg& sg = pr.seg[s];
-          const CUtensorMap* ma = &P.maps[sg.map_a];
+          const CUtensorMap* ma = &P.maps[sg.map_a + slab];
           const CUtensorMap* mb0 = &P.maps[sg.map_b];
           const CUtensorMap* mb1 = pr.paired ? &P.maps[sg.map_b2] : mb0;
           const int bn0 = pr.paired ? pr.b_n0 + c.tn * (BN / 2) : pr.b_n0 + c.tn * BN;
@@ -668,6 +673,29 @@ int GemmBatch::add_map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, 
   return nmaps_++;
 }
 
+int GemmBatch::add_maps_consecutive(const void* const* ptrs, int n, int64_t rows, int64_t cols, int64_t ld,
+                                    bool mn_major) {
+  if (err_) return -1;
+  if (n < 1 || nmaps_ + n > kMaxMaps) {
+    err_ = set_error(TTL_ERR_ARG, "GEMM batch: no room for %d consecutive operands", n);
+    return -1;
+  }
+  const int first = nmaps_;
+  for (int i = 0; i < n; ++i) {
+    // A distinct key per slot keeps add_map's de-duplication from folding these together.
+    const int before = nmaps_;
+    keys_[nmaps_] = MapKey{nullptr, -1, -1, -1, false};
+    const int idx = add_map(ptrs[i], rows, cols, ld, mn_major);
+    if (idx < 0) return -1;
+    if (idx != before) {   // de-duplicated onto an earlier map: encode a private copy here
+      p_->maps[nmaps_] = p_->maps[idx];
+      keys_[nmaps_] = MapKey{nullptr, -1, -1, -1, false};
+      ++nmaps_;
+    }
+  }
+  return first;
+}
+
 Problem* GemmBatch::add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired, bool join) {
   if (err_) return nullptr;
   if (join && (p_->nprob == 0 || p_->probs[p_->nprob - 1].M != M || p_->probs[p_->nprob - 1].paired != paired))
@@ -744,8 +772,17 @@ int GemmBatch::launch(cudaStream_t stream) {
   if ((rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
   DevState* ds = nullptr;
   if ((rc = device_setup(dev, &ds))) return rc;
-  // CTA pairs (256-row tiles) unless every problem is at most 128 rows tall.
-  const bool pair = pair_allowed() && ds->pair_clusters > 0 && max_m > 128;
+  // CTA pairs (256-row tiles) unless every problem is at most 128 rows tall, or a problem's
+  // A rows come in token slabs that a 256-row tile would straddle.
+  bool pair = pair_allowed() && ds->pair_clusters > 0 && max_m > 128;
+  for (int i = 0; i < p_->nprob; ++i) {
+    const Problem& p = p_->probs[i];
+    if (p.a_slab_rows <= 0) continue;
+    if (p.a_slab_rows % 128 || (p.a_m0 + p.M) > p.a_slab_rows * kMaxShards || p.a_m0 % p.a_slab_rows)
+      return set_error(TTL_ERR_SHAPE, "GEMM problem %d: token slabs of %d rows must be multiples of 128", i,
+                       p.a_slab_rows);
+    if (p.a_slab_rows % 256) pair = false;
+  }
   const int tile_m = pair ? Cfg<true>::TILE_M : Cfg<false>::TILE_M;
   int total = 0;
   p_->ngroups = 0;

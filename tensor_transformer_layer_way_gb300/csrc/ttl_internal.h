@@ -81,6 +81,8 @@ struct Problem {
   int32_t tiles_m, tiles_n;
   int32_t tn0;            // first n-tile of this problem within its group's n-tile range
   int32_t a_m0, b_n0;     // offsets added to the M coordinate of A and N coordinate of B
+  int32_t a_slab_rows;    // > 0: A's rows live in consecutive maps seg.map_a + r, r = row / a_slab_rows
+                          // (token slabs, e.g. an all-gather folded into the operand loads)
   uint8_t a_mn, b_mn;     // 1 = operand stored MN-major (A as [K,M], B as [K,N])
   uint8_t epi, nseg;
   uint8_t paired;
@@ -130,6 +132,9 @@ class GemmBatch {
   // mn_major selects the 64x64 box of an MN-major operand; otherwise the 64x128 box of a
   // K-major one.  Returns the map index or -1 (error recorded).
   int add_map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool mn_major);
+  // Registers n operands as n consecutive maps (no de-duplication), e.g. the t token slabs
+  // of an operand whose all-gather is folded into the loads.  Returns the first index or -1.
+  int add_maps_consecutive(const void* const* ptrs, int n, int64_t rows, int64_t cols, int64_t ld, bool mn_major);
   // Adds a problem and returns it (nullptr if the batch is full).  Segments are appended
   // with add_seg(); tile counts are filled in by launch().
   // join = true puts the problem in the previous problem's tile group; use it when both
