@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-components", action="store_true", help="skip the shard_reduce/gtp/ce legs")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="token rows of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["sp_mlp", "shard_reduce", "gtp_chain", "vocab_ce", "vocab_embedding"],
+                    help="run just one secondary component (for profiling); prints its JSON object")
     return ap.parse_args()
 
 
@@ -629,7 +631,15 @@ def main():
     args = parse()
     dist = Dist(args.gpus)
     try:
-        if args.impl == "reference":
+        if args.only:
+            import torch
+            import tensor_transformer_layer_way_gb300 as ttl
+            torch.cuda.set_device(dist.local)
+            fn = {"sp_mlp": bench_sp_mlp, "shard_reduce": bench_shard_reduce, "gtp_chain": bench_gtp,
+                  "vocab_ce": bench_ce, "vocab_embedding": bench_embedding}[args.only]
+            out = {"component": args.only,
+                   args.only: fn(ttl, torch, torch.device("cuda", dist.local), peaks(), args)}
+        elif args.impl == "reference":
             out = run_reference(args, dist)
         else:
             out = run_ours(args, dist)
