@@ -24,4 +24,4 @@ Parity status: every public function is pinned by a ``-m "not gpu"`` test
 against the pages' worked examples, closed forms, brute force or finite
 differences; see ``tests/test_oracle_*.py``.
 """
-from . import accounting, collectives, embedding, gtp, numerics, tp_mlp, vocab_ce  # noqa: F401
+from . import accounting, attention, collectives, embedding, gtp, numerics, tp_mlp, vocab_ce  # noqa: F401

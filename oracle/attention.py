@@ -1,0 +1,142 @@
+"""Tensor-parallel attention block (heads split across shards), forward and backward, float64.
+
+Test infrastructure only (see the package docstring).
+
+Source: the TP/SP page "v4:Tensor Parallel 与 Sequence Parallel", section "Attention:按 head 切":
+every head is computed on its own; W_Q, W_K, W_V are column-parallel by head so each card
+finishes its heads' attention without communication; W_O is row-parallel, followed by one
+all-reduce; the head counts must be divisible by t.  Qwen3 has 32 query heads and 8 KV heads
+(GQA), so at t = 8 each card holds 4 query heads and 1 KV head.  The TP-communication page's
+Fig. 1 draws the same f -> column -> local -> row -> g shape for attention.
+
+Readings where the pages are silent: scaled dot-product attention with scale 1/sqrt(d) and a
+causal mask (a decoder language model), one sequence of T tokens, no rotary embedding, no
+QK-normalisation, no biases; query head j uses KV head j // (n_q / n_kv); shard i owns query
+heads [i n_q/t, (i+1) n_q/t) and KV heads [i n_kv/t, (i+1) n_kv/t) (contiguous blocks of
+head-major columns, head c at columns [c d, (c+1) d)).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def causal_softmax(S) -> np.ndarray:
+    """Row softmax of S [T, T] over the keys j <= i (the rest get probability 0)."""
+    S = _f64(S)
+    T = S.shape[0]
+    mask = np.tril(np.ones((T, T), dtype=bool))
+    Z = np.where(mask, S, -np.inf)
+    m = Z.max(axis=1, keepdims=True)
+    E = np.where(mask, np.exp(Z - m), 0.0)
+    return E / E.sum(axis=1, keepdims=True)
+
+
+def attention_core(Q, K, V, n_q: int, n_kv: int, d: int) -> dict:
+    """Causal multi-head attention with grouped KV heads.  Q [T, n_q d], K/V [T, n_kv d].
+    Returns per-head probabilities ``P[c]`` [T, T] and the output O [T, n_q d]."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    T = Q.shape[0]
+    grp = n_q // n_kv
+    O = np.zeros((T, n_q * d))
+    P = []
+    for c in range(n_q):
+        g = c // grp
+        q = Q[:, c * d:(c + 1) * d]
+        k = K[:, g * d:(g + 1) * d]
+        v = V[:, g * d:(g + 1) * d]
+        p = causal_softmax(q @ k.T / np.sqrt(d))
+        P.append(p)
+        O[:, c * d:(c + 1) * d] = p @ v
+    return {"P": P, "O": O}
+
+
+def attention_core_backward(Q, K, V, P, dO, n_q: int, n_kv: int, d: int) -> dict:
+    """Backward of :func:`attention_core`: dP = dO_c V_g^T, dS = P (dP - rowsum(dO_c O_c)) / sqrt(d)
+    (softmax backward, the masked entries have P = 0), dQ_c = dS K_g, and the KV gradients
+    summed over the query heads of each group: dK_g += dS^T Q_c, dV_g += P^T dO_c."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    T = Q.shape[0]
+    grp = n_q // n_kv
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for c in range(n_q):
+        g = c // grp
+        cs, gs = slice(c * d, (c + 1) * d), slice(g * d, (g + 1) * d)
+        p = _f64(P[c])
+        do = dO[:, cs]
+        o = p @ V[:, gs]
+        dp = do @ V[:, gs].T
+        Dr = (do * o).sum(axis=1, keepdims=True)
+        ds = p * (dp - Dr) / np.sqrt(d)
+        dQ[:, cs] = ds @ K[:, gs]
+        dK[:, gs] += ds.T @ Q[:, cs]
+        dV[:, gs] += p.T @ do
+    return {"dQ": dQ, "dK": dK, "dV": dV}
+
+
+def head_columns(n_heads: int, d: int, t: int, i: int) -> slice:
+    """Columns of shard i's heads in a head-major [*, n_heads d] matrix."""
+    w = n_heads // t
+    return slice(i * w * d, (i + 1) * w * d)
+
+
+def tp_attention_forward(X, W: dict, t: int, n_q: int, n_kv: int, d: int) -> dict:
+    """Literal sharded block: per shard i, Q_i K_i V_i = X W{q,k,v}_i (its heads), local attention
+    over its 4 query heads and 1 KV head, the partial P_i = O_i Wo_i; the g all-reduce sums them."""
+    if n_q % t or n_kv % t:
+        raise ValueError("t must divide both head counts")
+    X = _f64(X)
+    out = {"Q": [], "K": [], "V": [], "P": [], "O": [], "part": []}
+    for i in range(t):
+        cq, ck = head_columns(n_q, d, t, i), head_columns(n_kv, d, t, i)
+        Qi = X @ _f64(W["Wq"])[:, cq]
+        Ki = X @ _f64(W["Wk"])[:, ck]
+        Vi = X @ _f64(W["Wv"])[:, ck]
+        core = attention_core(Qi, Ki, Vi, n_q // t, n_kv // t, d)
+        out["Q"].append(Qi)
+        out["K"].append(Ki)
+        out["V"].append(Vi)
+        out["P"].append(core["P"])
+        out["O"].append(core["O"])
+        out["part"].append(core["O"] @ _f64(W["Wo"])[cq, :])
+    Y = out["part"][0].copy()
+    for p in out["part"][1:]:
+        Y = Y + p
+    out["Y"] = Y
+    return out
+
+
+def tp_attention_backward(X, W: dict, t: int, n_q: int, n_kv: int, d: int, dY, fwd: dict) -> dict:
+    """Backward: g is the identity (dY full on every shard); dWo_i = O_i^T dY, dO_i = dY Wo_i^T;
+    the local attention backward; dW{q,k,v}_i = X^T d{Q,K,V}_i; the dX partials
+    d{Q,K,V}_i W{q,k,v}_i^T are all-reduced (f backward)."""
+    X, dY = _f64(X), _f64(dY)
+    res = {"dWq": [], "dWk": [], "dWv": [], "dWo": [], "dX_part": []}
+    for i in range(t):
+        cq, ck = head_columns(n_q, d, t, i), head_columns(n_kv, d, t, i)
+        Woi = _f64(W["Wo"])[cq, :]
+        res["dWo"].append(fwd["O"][i].T @ dY)
+        dO = dY @ Woi.T
+        g = attention_core_backward(fwd["Q"][i], fwd["K"][i], fwd["V"][i], fwd["P"][i], dO, n_q // t, n_kv // t, d)
+        res["dWq"].append(X.T @ g["dQ"])
+        res["dWk"].append(X.T @ g["dK"])
+        res["dWv"].append(X.T @ g["dV"])
+        res["dX_part"].append(g["dQ"] @ _f64(W["Wq"])[:, cq].T + g["dK"] @ _f64(W["Wk"])[:, ck].T
+                              + g["dV"] @ _f64(W["Wv"])[:, ck].T)
+    dX = res["dX_part"][0].copy()
+    for p in res["dX_part"][1:]:
+        dX = dX + p
+    res["dX"] = dX
+    return res
+
+
+def attention_unsharded(X, W: dict, n_q: int, n_kv: int, d: int) -> np.ndarray:
+    """The single-device block ``attention(X Wq, X Wk, X Wv) Wo``."""
+    X = _f64(X)
+    core = attention_core(X @ _f64(W["Wq"]), X @ _f64(W["Wk"]), X @ _f64(W["Wv"]), n_q, n_kv, d)
+    return core["O"] @ _f64(W["Wo"])

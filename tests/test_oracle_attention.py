@@ -1,0 +1,71 @@
+"""Pins of the oracle's tensor-parallel attention block (CPU only)."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import golden
+from oracle import attention
+
+
+def test_core_matches_torch_sdpa_and_its_gradients():
+    rng = np.random.default_rng(0)
+    T, n_q, n_kv, d = 9, 4, 2, 8
+    Q = rng.standard_normal((T, n_q * d))
+    K = rng.standard_normal((T, n_kv * d))
+    V = rng.standard_normal((T, n_kv * d))
+    dO = rng.standard_normal((T, n_q * d))
+    core = attention.attention_core(Q, K, V, n_q, n_kv, d)
+    Qt = torch.tensor(Q, requires_grad=True)
+    Kt = torch.tensor(K, requires_grad=True)
+    Vt = torch.tensor(V, requires_grad=True)
+    q = Qt.reshape(T, n_q, d).transpose(0, 1)
+    k = Kt.reshape(T, n_kv, d).transpose(0, 1).repeat_interleave(n_q // n_kv, 0)
+    v = Vt.reshape(T, n_kv, d).transpose(0, 1).repeat_interleave(n_q // n_kv, 0)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    O = o.transpose(0, 1).reshape(T, n_q * d)
+    np.testing.assert_allclose(core["O"], O.detach().numpy(), rtol=1e-12, atol=1e-12)
+    (O * torch.tensor(dO)).sum().backward()
+    g = attention.attention_core_backward(Q, K, V, core["P"], dO, n_q, n_kv, d)
+    np.testing.assert_allclose(g["dQ"], Qt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dK"], Kt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dV"], Vt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    # causal: the first token attends only to itself
+    np.testing.assert_allclose(core["O"][0, :d], V[0, :d], rtol=1e-14)
+    for p in core["P"]:
+        assert np.all(np.triu(p, 1) == 0) and np.allclose(p.sum(1), 1.0)
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_sharded_block_equals_unsharded(t):
+    rng = np.random.default_rng(t)
+    T, h, n_q, n_kv, d = 10, 12, 8, 4, 4
+    W = {"Wq": rng.standard_normal((h, n_q * d)) * 0.5, "Wk": rng.standard_normal((h, n_kv * d)) * 0.5,
+         "Wv": rng.standard_normal((h, n_kv * d)) * 0.5, "Wo": rng.standard_normal((n_q * d, h)) * 0.5}
+    X = rng.standard_normal((T, h))
+    dY = rng.standard_normal((T, h))
+    fwd = attention.tp_attention_forward(X, W, t, n_q, n_kv, d)
+    np.testing.assert_allclose(fwd["Y"], attention.attention_unsharded(X, W, n_q, n_kv, d), rtol=1e-12, atol=1e-12)
+    bwd = attention.tp_attention_backward(X, W, t, n_q, n_kv, d, dY, fwd)
+    Xt = torch.tensor(X, requires_grad=True)
+    Wt = {k: torch.tensor(v, requires_grad=True) for k, v in W.items()}
+    q = (Xt @ Wt["Wq"]).reshape(T, n_q, d).transpose(0, 1)
+    k = (Xt @ Wt["Wk"]).reshape(T, n_kv, d).transpose(0, 1).repeat_interleave(n_q // n_kv, 0)
+    v = (Xt @ Wt["Wv"]).reshape(T, n_kv, d).transpose(0, 1).repeat_interleave(n_q // n_kv, 0)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True).transpose(0, 1).reshape(T, -1)
+    ((o @ Wt["Wo"]) * torch.tensor(dY)).sum().backward()
+    np.testing.assert_allclose(bwd["dX"], Xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    for name, axis in (("Wq", 1), ("Wk", 1), ("Wv", 1), ("Wo", 0)):
+        np.testing.assert_allclose(np.concatenate(bwd["d" + name], axis=axis), Wt[name].grad.numpy(),
+                                   rtol=1e-10, atol=1e-12)
+
+
+def test_heads_per_shard_printed_counts():
+    g = golden("attention_heads_qwen3.json")
+    d = 128
+    for row in g["per_shard"]:
+        cq = attention.head_columns(g["n_q"], d, row["t"], 0)
+        ck = attention.head_columns(g["n_kv"], d, row["t"], 0)
+        assert (cq.stop - cq.start) // d == row["q_heads"]
+        assert (ck.stop - ck.start) // d == row["kv_heads"]
+    with pytest.raises(ValueError):
+        attention.tp_attention_forward(np.zeros((2, 4)), {}, 3, 32, 8, 1)   # 3 does not divide 32

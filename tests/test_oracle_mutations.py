@@ -105,6 +105,39 @@ def test_embedding_wrong_owner_offset_is_caught(monkeypatch):
     _expect_failure(temb.test_hand_worked_example)
 
 
+def test_attention_without_causal_mask_is_caught(monkeypatch):
+    import test_oracle_attention as tatt
+    from oracle import attention
+
+    def bad(S):
+        S = np.asarray(S, dtype=np.float64)
+        E = np.exp(S - S.max(axis=1, keepdims=True))
+        return E / E.sum(axis=1, keepdims=True)               # every key, no mask
+    monkeypatch.setattr(attention, "causal_softmax", bad)
+    _expect_failure(tatt.test_core_matches_torch_sdpa_and_its_gradients)
+
+
+def test_attention_backward_missing_rowsum_term_is_caught(monkeypatch):
+    import test_oracle_attention as tatt
+    from oracle import attention
+    def bad(Q, K, V, P, dO, n_q, n_kv, d):
+        # softmax backward written as dS = P dP / sqrt(d): the - rowsum(dO O) term dropped
+        Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
+        grp = n_q // n_kv
+        dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+        for c in range(n_q):
+            g = c // grp
+            cs, gs = slice(c * d, (c + 1) * d), slice(g * d, (g + 1) * d)
+            p = np.asarray(P[c])
+            ds = p * (dO[:, cs] @ V[:, gs].T) / np.sqrt(d)
+            dQ[:, cs] = ds @ K[:, gs]
+            dK[:, gs] += ds.T @ Q[:, cs]
+            dV[:, gs] += p.T @ dO[:, cs]
+        return {"dQ": dQ, "dK": dK, "dV": dV}
+    monkeypatch.setattr(attention, "attention_core_backward", bad)
+    _expect_failure(tatt.test_core_matches_torch_sdpa_and_its_gradients)
+
+
 def test_bf16_rounding_by_truncation_is_caught(monkeypatch):
     def bad(x):
         f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
