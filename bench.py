@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--no-components", action="store_true", help="skip the shard_reduce/gtp/ce legs")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="token rows of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["sp_mlp", "shard_reduce", "gtp_chain", "vocab_ce", "vocab_embedding"],
+    ap.add_argument("--only", choices=["sp_mlp", "shard_reduce", "gtp_chain", "vocab_ce", "vocab_embedding",
+                                       "tp_attention"],
                     help="run just one secondary component (for profiling); prints its JSON object")
     return ap.parse_args()
 
@@ -258,6 +259,7 @@ def run_ours(args, dist):
         comps["gtp_chain"] = bench_gtp(ttl, torch, dev, pk, args)
         comps["vocab_ce"] = bench_ce(ttl, torch, dev, pk, args)
         comps["vocab_embedding"] = bench_embedding(ttl, torch, dev, pk, args)
+        comps["tp_attention"] = bench_attention(ttl, torch, dev, pk, args)
 
     out = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": dist.world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
@@ -570,6 +572,63 @@ def bench_embedding(ttl, torch, dev, pk, args):
     return res
 
 
+def bench_attention(ttl, torch, dev, pk, args):
+    """Head-split TP attention block forward + backward at the Qwen3-8B shape: T=8192 tokens,
+    h=4096, 32 query / 8 KV heads of 128, t=8 (4 query heads + 1 KV head per shard)."""
+    t, T, h, n_q, n_kv, d = 8, 8192, 4096, 32, 8, 128
+    qc, kc = n_q // t * d, n_kv // t * d
+    g = torch.Generator(device=dev).manual_seed(7)
+
+    def rnd(shape, std):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    X, dY = rnd((T, h), 1.0), rnd((T, h), 1.0)
+    Wq = [rnd((h, qc), h ** -0.5) for _ in range(t)]
+    Wk = [rnd((h, kc), h ** -0.5) for _ in range(t)]
+    Wv = [rnd((h, kc), h ** -0.5) for _ in range(t)]
+    Wo = [rnd((qc, h), (n_q * d) ** -0.5) for _ in range(t)]
+    kw = dict(n_q=n_q, n_kv=n_kv, d=d)
+    fo = ttl.tp_attn_fwd(X, Wq, Wk, Wv, Wo, **kw)
+    bo = ttl.tp_attn_bwd(X, dY, Wq, Wk, Wv, Wo, fo, **kw)
+
+    def step():
+        ttl.tp_attn_fwd(X, Wq, Wk, Wv, Wo, out=fo, **kw)
+        ttl.tp_attn_bwd(X, dY, Wq, Wk, Wv, Wo, fo, out=bo, **kw)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(5, min(args.steps, 20))
+    ttl.trace_enable(True, 1 << 14)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    recs = ttl.trace_read(1 << 14)
+    ttl.trace_enable(False)
+    ms = e0.elapsed_time(e1) / n
+    flops = sum(r[2] for r in recs) / n        # algorithmic: causal contractions count their triangle
+    gm = [r for r in recs if r[0] == "gemm"]
+    sm = [r for r in recs if r[0] == "softmax"]
+    sm_gbs = sum(r[3] for r in sm) / (sum(r[1] for r in sm) * 1e-3) / 1e9
+    res = {"workload": "qwen3_8b_attention_t8_T8192_h4096_q32_kv8_d128_fwd_bwd", "ms_per_step": round(ms, 4),
+           "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "flops_per_step": flops,
+           "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
+           "frac_of_sustained_bf16": round(flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4),
+           "softmax_gbs": round(sm_gbs, 1), "softmax_frac_of_hbm": round(sm_gbs / pk["hbm_gbs"], 4),
+           "softmax_share_of_step": round(sum(r[1] for r in sm) / n / ms, 4),
+           "launches_per_step": len(recs) / n,
+           "launches": [{"kind": r[0], "ms": round(r[1], 4),
+                         "tflops": round(r[2] / (r[1] * 1e-3) / 1e12, 1) if r[2] else None,
+                         "gbs": round(r[3] / (r[1] * 1e-3) / 1e9, 1) if not r[2] else None}
+                        for r in recs[-(len(recs) // n):]]}
+    del X, dY, Wq, Wk, Wv, Wo, fo, bo
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)
 
 def oracle_sample(tokens: int):
@@ -636,7 +695,8 @@ def main():
             import tensor_transformer_layer_way_gb300 as ttl
             torch.cuda.set_device(dist.local)
             fn = {"sp_mlp": bench_sp_mlp, "shard_reduce": bench_shard_reduce, "gtp_chain": bench_gtp,
-                  "vocab_ce": bench_ce, "vocab_embedding": bench_embedding}[args.only]
+                  "vocab_ce": bench_ce, "vocab_embedding": bench_embedding,
+                  "tp_attention": bench_attention}[args.only]
             out = {"component": args.only,
                    args.only: fn(ttl, torch, torch.device("cuda", dist.local), peaks(), args)}
         elif args.impl == "reference":

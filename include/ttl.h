@@ -88,6 +88,7 @@ int ttl_selftest_wait_timeout(int64_t timeout_us, void* stream);
 #define TTL_K_CE_DLOGITS 7  /* CE dlogits                                     */
 #define TTL_K_OTHER 8       /* column sums, zero fills                        */
 #define TTL_K_EMBED 9       /* vocab-parallel embedding lookup / gradient     */
+#define TTL_K_SOFTMAX 10    /* attention row softmax / softmax backward       */
 
 /* Starts (on != 0) or stops tracing on this process.  While on, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the launch stream, and
@@ -311,6 +312,48 @@ int ttl_vocab_parallel_embedding_fwd(int t, int64_t T, int64_t h, int64_t V, con
  * summed with atomic adds, so the fp32 summation order is not fixed. */
 int ttl_vocab_parallel_embedding_bwd(int t, int64_t T, int64_t h, int64_t V, const int64_t* ids,
                                      const ttl_bf16* dY, float* const* dE, void* stream);
+
+/* ------------------------------------------------------------------ TP attention block */
+
+/* Attention split by heads ([TPSP] "Attention:按 head 切"; [COMM] Fig. 1): shard i holds
+ * query heads [i n_q/t, (i+1) n_q/t) and KV heads [i n_kv/t, (i+1) n_kv/t) (grouped-query
+ * attention: query head j reads KV head j / (n_q / n_kv)); W_Q, W_K, W_V are column-parallel
+ * by head, each shard computes its heads' attention alone, W_O is row-parallel and g
+ * all-reduces the t partials.  The attention is causal scaled dot-product attention with
+ * scale 1/sqrt(d) over one sequence of T tokens (no rotary embedding, no biases).  Matrices
+ * are row-major bf16, head-major columns (head c at columns [c d, (c+1) d)).
+ *   X [T,h]; Wq[i] [h, n_q/t d]; Wk[i], Wv[i] [h, n_kv/t d]; Wo[i] [n_q/t d, h]
+ *   Q_save[i] [T, n_q/t d], K_save[i], V_save[i] [T, n_kv/t d], O_save[i] [T, n_q/t d]  out
+ *   P_save[i] [n_q/t, T, T] out: the probabilities, head-major; row q is written for keys
+ *             j < min(T, round_up(q+1, 256)) (zeros above the diagonal), the rest is untouched
+ *   Y[i] [T,h] out: partial O_i Wo_i, then the all-reduced block output in every buffer
+ *   ws   workspace of ttl_tp_attn_fwd_workspace_size() bytes (the fp32 scores)
+ * t | n_q, t | n_kv, n_kv | n_q, d a multiple of 64, T and h multiples of 8.  Errors:
+ * TTL_ERR_ARG (null or short arguments), TTL_ERR_SHAPE, TTL_ERR_ALIGN (pointers not 16-byte
+ * aligned); nothing is launched when the call returns an error. */
+size_t ttl_tp_attn_fwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d);
+int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const ttl_bf16* X,
+                    const ttl_bf16* const* Wq, const ttl_bf16* const* Wk, const ttl_bf16* const* Wv,
+                    const ttl_bf16* const* Wo, ttl_bf16* const* Q_save, ttl_bf16* const* K_save,
+                    ttl_bf16* const* V_save, ttl_bf16* const* P_save, ttl_bf16* const* O_save,
+                    ttl_bf16* const* Y, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of ttl_tp_attn_fwd: g backward is the identity (dY full on every shard), the heads'
+ * attention backward is local (dS = P (dP - rowsum(dO O)) / sqrt(d), the KV gradients summed
+ * over each group's query heads), f backward all-reduces dX.
+ *   dY [T,h]; X, W*, *_save as given to / written by ttl_tp_attn_fwd
+ *   dWq[i], dWk[i], dWv[i], dWo[i] out, shaped like the weights
+ *   dX[i] [T,h] out: partial, then the all-reduced dX in every buffer
+ *   ws   workspace of ttl_tp_attn_bwd_workspace_size() bytes
+ * T = 0 writes zero weight gradients (token-sized pointers may then be null). */
+size_t ttl_tp_attn_bwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d);
+int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const ttl_bf16* X,
+                    const ttl_bf16* dY, const ttl_bf16* const* Wq, const ttl_bf16* const* Wk,
+                    const ttl_bf16* const* Wv, const ttl_bf16* const* Wo, const ttl_bf16* const* Q_save,
+                    const ttl_bf16* const* K_save, const ttl_bf16* const* V_save,
+                    const ttl_bf16* const* P_save, const ttl_bf16* const* O_save, ttl_bf16* const* dWq,
+                    ttl_bf16* const* dWk, ttl_bf16* const* dWv, ttl_bf16* const* dWo, ttl_bf16* const* dX,
+                    void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -140,3 +140,65 @@ def attention_unsharded(X, W: dict, n_q: int, n_kv: int, d: int) -> np.ndarray:
     X = _f64(X)
     core = attention_core(X @ _f64(W["Wq"]), X @ _f64(W["Wk"]), X @ _f64(W["Wv"]), n_q, n_kv, d)
     return core["O"] @ _f64(W["Wo"])
+
+
+def _softmax_vec(s) -> np.ndarray:
+    e = np.exp(s - s.max())
+    return e / e.sum()
+
+
+def forward_rows(X, W: dict, n_q: int, n_kv: int, d: int, rows) -> np.ndarray:
+    """Rows ``rows`` of the block output, each on its own: under the causal mask output row i
+    depends on the tokens 0..i only, so it needs query i, the keys and values up to i and W_O.
+    For sampled checks of shapes too large for :func:`attention_unsharded`."""
+    X = _f64(X)
+    rows = np.asarray(rows, dtype=np.int64)
+    m = int(rows.max()) + 1
+    K = X[:m] @ _f64(W["Wk"])
+    V = X[:m] @ _f64(W["Wv"])
+    Wq, Wo = _f64(W["Wq"]), _f64(W["Wo"])
+    grp = n_q // n_kv
+    out = np.zeros((len(rows), Wo.shape[1]))
+    for r, i in enumerate(rows):
+        q = X[i] @ Wq
+        o = np.zeros(n_q * d)
+        for c in range(n_q):
+            g = c // grp
+            cs, gs = slice(c * d, (c + 1) * d), slice(g * d, (g + 1) * d)
+            p = _softmax_vec(K[:i + 1, gs] @ q[cs] / np.sqrt(d))
+            o[cs] = p @ V[:i + 1, gs]
+        out[r] = o @ Wo
+    return out
+
+
+def backward_rows_dx(X, W: dict, dY, n_q: int, n_kv: int, d: int, rows) -> np.ndarray:
+    """Rows ``rows`` of the input gradient dX = dQ Wq^T + dK Wk^T + dV Wv^T, each on its own.
+    Row i of dQ needs query i's softmax row; rows i of dK and dV collect, over every query
+    q >= i, the entries dS_c[q, i] Q_c[q] and P_c[q, i] dO_c[q] of the group's query heads.
+    The work grows with T - min(rows): sample rows near the end of long sequences."""
+    X, dY = _f64(X), _f64(dY)
+    rows = np.asarray(rows, dtype=np.int64)
+    T = X.shape[0]
+    Wq, Wk, Wv, Wo = (_f64(W[k]) for k in ("Wq", "Wk", "Wv", "Wo"))
+    K, V = X @ Wk, X @ Wv
+    grp = n_q // n_kv
+    dQ = {int(i): np.zeros(n_q * d) for i in rows}
+    dK = {int(i): np.zeros(n_kv * d) for i in rows}
+    dV = {int(i): np.zeros(n_kv * d) for i in rows}
+    for q in range(int(rows.min()), T):
+        Qq = X[q] @ Wq
+        dOq = dY[q] @ Wo.T
+        for c in range(n_q):
+            g = c // grp
+            cs, gs = slice(c * d, (c + 1) * d), slice(g * d, (g + 1) * d)
+            Kg, Vg = K[:q + 1, gs], V[:q + 1, gs]
+            p = _softmax_vec(Kg @ Qq[cs] / np.sqrt(d))
+            o = p @ Vg
+            ds = p * (Vg @ dOq[cs] - dOq[cs] @ o) / np.sqrt(d)
+            if q in dQ:
+                dQ[q][cs] = ds @ Kg
+            for i in dK:
+                if i <= q:
+                    dK[i][gs] += ds[i] * Qq[cs]
+                    dV[i][gs] += p[i] * dOq[cs]
+    return np.stack([dQ[int(i)] @ Wq.T + dK[int(i)] @ Wk.T + dV[int(i)] @ Wv.T for i in rows])

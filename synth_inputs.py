@@ -11,8 +11,8 @@ targets), as ``randn * std`` rounded once to bf16.  The shapes follow the
 pages' workloads: the toy MLP of the "MLP: column then row" section
 (h=256, 4h=1024), the b=1, s=4096, h=8192 layer output of the TP
 communication page's worked table, the Qwen3-8B layer (h=4096, SwiGLU width
-12288, vocab 151936) of the TP/SP page, and the h=8192, TP=4, GTP_remat=8
-square weight of the GTP page's memory example.
+12288, vocab 151936, 32 query and 8 KV heads of dimension 128) of the TP/SP page, and
+the h=8192, TP=4, GTP_remat=8 square weight of the GTP page's memory example.
 """
 from __future__ import annotations
 
@@ -73,6 +73,22 @@ QWEN3_8B_SWIGLU_T8 = MlpShape("qwen3_8b_swiglu_mlp_t8_T8192_h4096_f12288", t=8, 
                               f=12288, act="swiglu", seed=3)
 GTP_CHAIN = GtpShape("gtp_chain_L8_h8192_tp4_g8_T4096", L=8, h=8192, tp=4, g=8, T=4096, seed=4)
 VOCAB_CE_T8 = CeShape("vocab_parallel_ce_t8_T8192_h4096_V151936", t=8, T=8192, h=4096, V=151936, seed=5)
+
+
+@dataclasses.dataclass(frozen=True)
+class AttnShape:
+    name: str
+    t: int
+    T: int
+    h: int
+    n_q: int          # query heads
+    n_kv: int         # key/value heads (grouped-query attention)
+    d: int            # head dimension
+    seed: int
+
+
+QWEN3_8B_ATTN_T8 = AttnShape("qwen3_8b_attention_t8_T8192_h4096_q32_kv8_d128", t=8, T=8192, h=4096,
+                             n_q=32, n_kv=8, d=128, seed=6)
 
 
 # --------------------------------------------------------------------------
@@ -162,6 +178,25 @@ def ce_inputs(T: int, h: int, V: int, seed: int, *, w_std: float = 0.02) -> dict
     W = randn_bf16(g, (V, h), w_std)
     target = torch.randint(0, V, (T,), generator=g, dtype=torch.int64)
     return {"H": H, "W": W, "target": target}
+
+
+def attn_inputs(T: int, h: int, n_q: int, n_kv: int, d: int, seed: int, *, w_std: float | None = None,
+                dY_rows: int | None = None) -> dict:
+    """Attention block: ``X [T,h]`` ~N(0,1), ``Wq [h,n_q d]``, ``Wk``, ``Wv [h,n_kv d]``,
+    ``Wo [n_q d,h]`` ~N(0,w_std) (default 1/sqrt(h), so projected entries are ~N(0,1)) and
+    ``dY [T,h]`` ~N(0,1).  ``dY_rows = m`` keeps dY only on the first m rows (zeros below)."""
+    g = generator(seed)
+    w_std = h ** -0.5 if w_std is None else w_std
+    out = {"X": randn_bf16(g, (T, h), 1.0)}
+    out["Wq"] = randn_bf16(g, (h, n_q * d), w_std)
+    out["Wk"] = randn_bf16(g, (h, n_kv * d), w_std)
+    out["Wv"] = randn_bf16(g, (h, n_kv * d), w_std)
+    out["Wo"] = randn_bf16(g, (n_q * d, h), (n_q * d) ** -0.5)
+    dY = randn_bf16(g, (T, h), 1.0)
+    if dY_rows is not None:
+        dY[dY_rows:] = 0
+    out["dY"] = dY
+    return out
 
 
 def sample_indices(n_total: int, n_sample: int, seed: int) -> torch.Tensor:

@@ -64,6 +64,10 @@ _SIGS = {
                               _vp, _vp, ctypes.c_size_t, _vp]),
     "ttl_vocab_parallel_embedding_fwd": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _int, _vp]),
     "ttl_vocab_parallel_embedding_bwd": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "ttl_tp_attn_fwd_workspace_size": (ctypes.c_size_t, [_int, _i64, _int, _int, _int]),
+    "ttl_tp_attn_fwd": (_int, [_int, _i64, _i64, _int, _int, _int] + [_vp] * 11 + [_vp, ctypes.c_size_t, _vp]),
+    "ttl_tp_attn_bwd_workspace_size": (ctypes.c_size_t, [_int, _i64, _int, _int, _int]),
+    "ttl_tp_attn_bwd": (_int, [_int, _i64, _i64, _int, _int, _int] + [_vp] * 16 + [_vp, ctypes.c_size_t, _vp]),
 }
 
 _lib = None
@@ -161,7 +165,7 @@ def selftest_wait_timeout(timeout_us: int, stream=None) -> int:
 
 
 KERNEL_KINDS = ["gemm", "reduce", "gather", "gtp_gather", "finalize", "ce_stats", "ce_small", "ce_dlogits", "other",
-                "embed"]
+                "embed", "softmax"]
 
 
 def trace_enable(on: bool = True, capacity: int = 65536):
@@ -492,3 +496,65 @@ def vocab_parallel_embedding_bwd(ids, dY, dE, *, stream=None):
     _need_list(dE, "dE", t, torch.float32, (Vs, h))
     _check(lib().ttl_vocab_parallel_embedding_bwd(t, T, h, Vs * t, _p(ids), _p(dY), _arr(dE), _stream(stream)))
     return dE
+
+
+# ------------------------------------------------------------------ TP attention block
+
+def attn_fwd_buffers(t, T, h, n_q, n_kv, d, device="cuda"):
+    """Output, saved-activation and workspace buffers of tp_attn_fwd."""
+    qc, kc = n_q // t * d, n_kv // t * d
+    e = dict(device=device, dtype=torch.bfloat16)
+    out = {"Q": [torch.empty(T, qc, **e) for _ in range(t)], "K": [torch.empty(T, kc, **e) for _ in range(t)],
+           "V": [torch.empty(T, kc, **e) for _ in range(t)], "O": [torch.empty(T, qc, **e) for _ in range(t)],
+           "P": [torch.empty(n_q // t, T, T, **e) for _ in range(t)], "Y": [torch.empty(T, h, **e) for _ in range(t)]}
+    ws = int(lib().ttl_tp_attn_fwd_workspace_size(t, T, n_q, n_kv, d))
+    out["ws"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+    return out
+
+
+def tp_attn_fwd(X, Wq, Wk, Wv, Wo, *, n_q, n_kv, d, out=None, stream=None):
+    """Forward of the head-split attention block over len(Wq) shards.
+    Returns dict Q, K, V, P, O (saved per shard) and Y (all-reduced in every buffer)."""
+    t = len(Wq)
+    T, h = X.shape
+    qc, kc = n_q // t * d, n_kv // t * d
+    _need(X, "X")
+    _need_list(Wq, "Wq", t, shape=(h, qc))
+    _need_list(Wk, "Wk", t, shape=(h, kc))
+    _need_list(Wv, "Wv", t, shape=(h, kc))
+    _need_list(Wo, "Wo", t, shape=(qc, h))
+    if out is None:
+        out = attn_fwd_buffers(t, T, h, n_q, n_kv, d, X.device)
+    ws = out["ws"]
+    _check(lib().ttl_tp_attn_fwd(t, T, h, n_q, n_kv, d, _p(X), _arr(Wq), _arr(Wk), _arr(Wv), _arr(Wo),
+                                 _arr(out["Q"]), _arr(out["K"]), _arr(out["V"]), _arr(out["P"]), _arr(out["O"]),
+                                 _arr(out["Y"]), _p(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def attn_bwd_buffers(t, T, h, n_q, n_kv, d, device="cuda"):
+    qc, kc = n_q // t * d, n_kv // t * d
+    e = dict(device=device, dtype=torch.bfloat16)
+    out = {"dWq": [torch.empty(h, qc, **e) for _ in range(t)], "dWk": [torch.empty(h, kc, **e) for _ in range(t)],
+           "dWv": [torch.empty(h, kc, **e) for _ in range(t)], "dWo": [torch.empty(qc, h, **e) for _ in range(t)],
+           "dX": [torch.empty(T, h, **e) for _ in range(t)]}
+    ws = int(lib().ttl_tp_attn_bwd_workspace_size(t, T, n_q, n_kv, d))
+    out["ws"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+    return out
+
+
+def tp_attn_bwd(X, dY, Wq, Wk, Wv, Wo, fwd, *, n_q, n_kv, d, out=None, stream=None):
+    """Backward of tp_attn_fwd (``fwd`` is the dict it returned).
+    Returns dict dWq, dWk, dWv, dWo and dX (all-reduced in every buffer)."""
+    t = len(Wq)
+    T, h = X.shape
+    _need(X, "X")
+    _need(dY, "dY", shape=(T, h))
+    if out is None:
+        out = attn_bwd_buffers(t, T, h, n_q, n_kv, d, X.device)
+    ws = out["ws"]
+    _check(lib().ttl_tp_attn_bwd(t, T, h, n_q, n_kv, d, _p(X), _p(dY), _arr(Wq), _arr(Wk), _arr(Wv), _arr(Wo),
+                                 _arr(fwd["Q"]), _arr(fwd["K"]), _arr(fwd["V"]), _arr(fwd["P"]), _arr(fwd["O"]),
+                                 _arr(out["dWq"]), _arr(out["dWk"]), _arr(out["dWv"]), _arr(out["dWo"]),
+                                 _arr(out["dX"]), _p(ws), ws.numel(), _stream(stream)))
+    return out

@@ -1,0 +1,548 @@
+// Tensor-parallel attention block on t logical shards of one GPU, heads split across shards.
+//
+// Source: "v4:Tensor Parallel 与 Sequence Parallel", section "Attention:按 head 切": heads are
+// independent, so W_Q, W_K, W_V are column-split by head and each shard finishes the attention
+// of its own heads without communication; W_O is row-split and followed by one all-reduce;
+// the head counts must be divisible by t (Qwen3: 32 query / 8 KV heads, 4 + 1 per shard at
+// t = 8).  The TP-communication page's Fig. 1 draws the same f -> column -> local -> row -> g
+// shape.  The pages do not spell out the attention itself; this file computes causal scaled
+// dot-product attention with scale 1/sqrt(d), query head j reading KV head j / (n_q / n_kv).
+//
+// Every contraction runs in the tcgen05 GEMM; the causal structure is handled there (score
+// tiles above the diagonal are skipped, P V and dS K stop their K loop at the tile's last
+// query, dS^T Q and P^T dO start theirs at the tile's first key).  The scores are materialised
+// in fp32 and the row softmax and its backward are warp-per-row HBM streams:
+//   forward : QKV (3t problems) -> S = Q_c K_g^T (fp32) -> P = softmax(S / sqrt(d)) (bf16)
+//             -> O_c = P_c V_g -> partial Y_i = O_i Wo_i -> all-reduce
+//   backward: {dO_i = dY Wo_i^T, dWo_i = O_i^T dY} -> dP = dO_c V_g^T (fp32)
+//             -> dS = P (dP - rowsum(dO_c O_c)) / sqrt(d) (bf16)
+//             -> {dQ_c = dS_c K_g, dK_g = sum_c dS_c^T Q_c, dV_g = sum_c P_c^T dO_c}
+//             -> {dW_i = X^T d{Q,K,V}_i, dX_i = dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T} -> all-reduce
+//
+// Zero fill: row q of P and of dS is written for every key j < min(T, round_up(q + 1, 256));
+// the keys above the diagonal get exact zeros.  That covers every element the causal GEMMs read
+// with either tile height (128 or 256 rows), so no full-size mask pass is needed.
+
+#include <cmath>
+
+#include "ttl_device.cuh"
+#include "ttl_internal.h"
+
+namespace ttl {
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int kRowWarps = 8;   // rows (one per warp) per CTA of the row kernels
+
+// Per-shard pointers of the row kernels; every [n_q/t, T, T] block is head-major and dense.
+struct AttnRows {
+  const float* s[kMaxShards];            // fp32 scores (forward) or score gradients dP (backward)
+  const __nv_bfloat16* p[kMaxShards];    // backward: saved probabilities
+  __nv_bfloat16* out[kMaxShards];        // P (forward) or dS (backward)
+  const __nv_bfloat16* dO[kMaxShards];   // backward: [T, n_q/t d]
+  const __nv_bfloat16* o[kMaxShards];    // backward: [T, n_q/t d]
+};
+
+__device__ __forceinline__ void load8_f32(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void unpack8_bf16(uint4 w, float* v) {
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+// exp2((x - m) * k) with an empty side (m = -inf) weighing nothing.
+__device__ __forceinline__ float rescale(float m, float M, float k) {
+  return m == -INFINITY ? 0.0f : exp2f((m - M) * k);
+}
+
+// One warp per (shard, head, query) row q: P[q, j] = exp(S[q, j] / sqrt(d) - max) / sum over
+// the keys j <= q, zeros for q < j < min(T, round_up(q + 1, 256)).  k = log2(e) / sqrt(d).
+__global__ void __launch_bounds__(kRowWarps * 32) attn_softmax_fwd_kernel(const __grid_constant__ AttnRows R,
+                                                                          int64_t rows, int64_t T, int64_t nql,
+                                                                          float k) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t per_shard = nql * T;
+  const int i = static_cast<int>(row / per_shard);
+  const int64_t r = row - i * per_shard;   // head * T + q
+  const int64_t q = r % T;
+  const float* srow = R.s[i] + r * T;
+  __nv_bfloat16* prow = R.out[i] + r * T;
+
+  float m = -INFINITY, l = 0.0f;
+  for (int64_t j0 = lane * 8; j0 <= q; j0 += 256) {
+    float v[8];
+    load8_f32(srow + j0, v);
+    float mx = m;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j0 + j <= q) mx = fmaxf(mx, v[j]);
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j0 + j <= q) acc += exp2f((v[j] - mx) * k);
+    l = l * rescale(m, mx, k) + acc;
+    m = mx;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    const float M = fmaxf(m, m2);
+    l = l * rescale(m, M, k) + l2 * rescale(m2, M, k);
+    m = M;
+  }
+  const float inv_l = 1.0f / l;
+  const int64_t z = min(T, ((q + 256) / 256) * 256);
+  for (int64_t j0 = lane * 8; j0 < z; j0 += 256) {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (j0 <= q) {
+      float v[8];
+      load8_f32(srow + j0, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = (j0 + j <= q) ? exp2f((v[j] - m) * k) * inv_l : 0.0f;
+      w = pack8_bf16(v);
+    }
+    *reinterpret_cast<uint4*>(prow + j0) = w;
+  }
+}
+
+// One warp per row: D = sum_k dO[q, k] O[q, k] over the head's d columns, then
+// dS[q, j] = P[q, j] (dP[q, j] - D) / sqrt(d) for j <= q and zeros up to the same bound as P.
+__global__ void __launch_bounds__(kRowWarps * 32) attn_softmax_bwd_kernel(const __grid_constant__ AttnRows R,
+                                                                          int64_t rows, int64_t T, int64_t nql,
+                                                                          int d, float scale) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t per_shard = nql * T;
+  const int i = static_cast<int>(row / per_shard);
+  const int64_t r = row - i * per_shard;
+  const int64_t c = r / T;
+  const int64_t q = r - c * T;
+  const int64_t hcol = q * nql * d + c * d;
+  float D = 0.0f;
+  for (int k0 = lane * 8; k0 < d; k0 += 256) {
+    float a[8], b[8];
+    unpack8_bf16(*reinterpret_cast<const uint4*>(R.dO[i] + hcol + k0), a);
+    unpack8_bf16(*reinterpret_cast<const uint4*>(R.o[i] + hcol + k0), b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) D = fmaf(a[j], b[j], D);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) D += __shfl_xor_sync(0xffffffffu, D, off);
+
+  const float* dprow = R.s[i] + r * T;
+  const __nv_bfloat16* prow = R.p[i] + r * T;
+  __nv_bfloat16* dsrow = R.out[i] + r * T;
+  const int64_t z = min(T, ((q + 256) / 256) * 256);
+  for (int64_t j0 = lane * 8; j0 < z; j0 += 256) {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (j0 <= q) {
+      float p[8], dp[8];
+      unpack8_bf16(*reinterpret_cast<const uint4*>(prow + j0), p);
+      load8_f32(dprow + j0, dp);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) p[j] = (j0 + j <= q) ? p[j] * (dp[j] - D) * scale : 0.0f;
+      w = pack8_bf16(p);
+    }
+    *reinterpret_cast<uint4*>(dsrow + j0) = w;
+  }
+}
+
+struct Shape {
+  int t;
+  int64_t T, h;
+  int n_q, n_kv, d;
+  int64_t nql, nkvl, grp;   // query heads, KV heads per shard; query heads per KV head
+  int64_t qc, kc;           // columns of Q_i and of K_i / V_i
+};
+
+int check_shape(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const char* name, Shape* out) {
+  if (t < 1 || t > kMaxShards) return set_error(TTL_ERR_ARG, "%s: t=%d outside [1,%d]", name, t, kMaxShards);
+  if (T < 0 || h < 0 || n_q < 1 || n_kv < 1 || d < 1) return set_error(TTL_ERR_ARG, "%s: bad shape", name);
+  if (n_q % t || n_kv % t)
+    return set_error(TTL_ERR_SHAPE, "%s: t=%d must divide the head counts %d and %d", name, t, n_q, n_kv);
+  if (n_q % n_kv) return set_error(TTL_ERR_SHAPE, "%s: n_kv=%d must divide n_q=%d", name, n_kv, n_q);
+  if (d % 64) return set_error(TTL_ERR_SHAPE, "%s: head dimension %d must be a multiple of 64", name, d);
+  if (T % 8 || h % 8 || h == 0)
+    return set_error(TTL_ERR_SHAPE, "%s: T and h must be multiples of 8 (16-byte rows), h > 0", name);
+  if (T >= (int64_t(1) << 28) || h >= (int64_t(1) << 31) || static_cast<int64_t>(n_q / t) * T >= (int64_t(1) << 31))
+    return set_error(TTL_ERR_SHAPE, "%s: extent beyond 2^31", name);
+  Shape& s = *out;
+  s.t = t; s.T = T; s.h = h; s.n_q = n_q; s.n_kv = n_kv; s.d = d;
+  s.nql = n_q / t; s.nkvl = n_kv / t; s.grp = n_q / n_kv;
+  s.qc = s.nql * d; s.kc = s.nkvl * d;
+  return TTL_OK;
+}
+
+int check_ptrs(const void* const* arr, int t, const char* what) {
+  if (!arr) return set_error(TTL_ERR_ARG, "%s: null shard array", what);
+  for (int i = 0; i < t; ++i) {
+    if (!arr[i]) return set_error(TTL_ERR_ARG, "%s[%d] is null", what, i);
+    if (!aligned16(arr[i])) return set_error(TTL_ERR_ALIGN, "%s[%d] not 16-byte aligned", what, i);
+  }
+  return TTL_OK;
+}
+
+size_t score_bytes(const Shape& s, size_t esz) {   // one shard's [n_q/t, T, T] block
+  return round256(static_cast<size_t>(s.nql) * static_cast<size_t>(s.T) * static_cast<size_t>(s.T) * esz);
+}
+
+// MN-major operand rows [T queries, T keys] of head c in a shard's head-major [n_q/t, T, T]
+// block.  When T is a multiple of 64 no k-block crosses into the next head, so one map with a
+// K offset serves every head; otherwise each head gets its own map, whose edge reads as zeros.
+int head_block_map(GemmBatch& b, const __nv_bfloat16* base, const Shape& s, int64_t c, int64_t* k0) {
+  if (s.T % 64 == 0) {
+    *k0 = c * s.T;
+    return b.add_map(base, s.nql * s.T, s.T, s.T, true);
+  }
+  *k0 = 0;
+  return b.add_map(base + c * s.T * s.T, s.T, s.T, s.T, true);
+}
+
+const __nv_bfloat16* bf(const ttl_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
+
+}  // namespace
+}  // namespace ttl
+
+using namespace ttl;
+
+extern "C" size_t ttl_tp_attn_fwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d) {
+  Shape s;
+  if (check_shape(t, T, 8, n_q, n_kv, d, "ttl_tp_attn_fwd_workspace_size", &s)) return 0;
+  return score_bytes(s, 4) * static_cast<size_t>(t);
+}
+
+extern "C" size_t ttl_tp_attn_bwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d) {
+  Shape s;
+  if (check_shape(t, T, 8, n_q, n_kv, d, "ttl_tp_attn_bwd_workspace_size", &s)) return 0;
+  const size_t tok = static_cast<size_t>(T) * 2;
+  const size_t per = score_bytes(s, 4) + score_bytes(s, 2) + 2 * round256(tok * s.qc) + 2 * round256(tok * s.kc);
+  return per * static_cast<size_t>(t);
+}
+
+extern "C" int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const ttl_bf16* X,
+                               const ttl_bf16* const* Wq, const ttl_bf16* const* Wk, const ttl_bf16* const* Wv,
+                               const ttl_bf16* const* Wo, ttl_bf16* const* Q_save, ttl_bf16* const* K_save,
+                               ttl_bf16* const* V_save, ttl_bf16* const* P_save, ttl_bf16* const* O_save,
+                               ttl_bf16* const* Y, void* ws, size_t ws_bytes, void* stream) {
+  const char* name = "ttl_tp_attn_fwd";
+  Shape s;
+  int rc = check_shape(t, T, h, n_q, n_kv, d, name, &s);
+  if (rc) return rc;
+  if (T == 0) return TTL_OK;   // no tokens: every output is empty
+  if (!X) return set_error(TTL_ERR_ARG, "%s: X is null", name);
+  if (!aligned16(X)) return set_error(TTL_ERR_ALIGN, "%s: X not 16-byte aligned", name);
+  using CP = const void* const*;
+  const struct { CP p; const char* n; } arrs[] = {
+      {reinterpret_cast<CP>(Wq), "Wq"},         {reinterpret_cast<CP>(Wk), "Wk"},
+      {reinterpret_cast<CP>(Wv), "Wv"},         {reinterpret_cast<CP>(Wo), "Wo"},
+      {reinterpret_cast<CP>(Q_save), "Q_save"}, {reinterpret_cast<CP>(K_save), "K_save"},
+      {reinterpret_cast<CP>(V_save), "V_save"}, {reinterpret_cast<CP>(P_save), "P_save"},
+      {reinterpret_cast<CP>(O_save), "O_save"}, {reinterpret_cast<CP>(Y), "Y"}};
+  for (const auto& a : arrs)
+    if ((rc = check_ptrs(a.p, t, a.n))) return rc;
+  const size_t need = ttl_tp_attn_fwd_workspace_size(t, T, n_q, n_kv, d);
+  if (!ws || ws_bytes < need)
+    return set_error(TTL_ERR_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
+  if (!aligned16(ws)) return set_error(TTL_ERR_ALIGN, "%s: workspace not 16-byte aligned", name);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t sb = score_bytes(s, 4);
+  auto S_of = [&](int i) { return reinterpret_cast<float*>(static_cast<char*>(ws) + sb * static_cast<size_t>(i)); };
+  GemmBatch batch;
+
+  // Column-parallel projections: Q_i, K_i, V_i = X W{q,k,v}_i, one tile group over X.
+  for (int i = 0; i < t; ++i) {
+    const ttl_bf16* const* Ws[3] = {Wq, Wk, Wv};
+    ttl_bf16* const* Os[3] = {Q_save, K_save, V_save};
+    for (int w = 0; w < 3; ++w) {
+      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+      const int64_t cols = w == 0 ? s.qc : s.kc;
+      const int mx = batch.add_map(X, T, h, h, false);
+      const int mw = batch.add_map(Ws[w][i], h, cols, cols, true);
+      Problem* p = batch.add_problem(T, cols, false, true, EPI_BF16, false, true);
+      if (batch.error()) return batch.error();
+      p->out0 = Os[w][i];
+      p->ld_out = cols;
+      if ((rc = batch.add_seg(p, mx, 0, mw, -1, 0, h))) return rc;
+    }
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // Scores S_c = Q_c K_g^T (fp32), tiles above the diagonal skipped.
+  for (int i = 0; i < t; ++i) {
+    for (int64_t c = 0; c < s.nql; ++c) {
+      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+      const int mq = batch.add_map(Q_save[i], T, s.qc, s.qc, false);
+      const int mk = batch.add_map(K_save[i], T, s.kc, s.kc, false);
+      Problem* p = batch.add_problem(T, T, false, false, EPI_F32, false);
+      if (batch.error()) return batch.error();
+      p->causal = CAUSAL_SKIP_UPPER;
+      p->out0 = S_of(i) + c * T * T;
+      p->ld_out = T;
+      if ((rc = batch.add_seg(p, mq, c * d, mk, -1, (c / s.grp) * d, d))) return rc;
+    }
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // Row softmax into the saved probabilities.
+  {
+    AttnRows R = {};
+    for (int i = 0; i < t; ++i) {
+      R.s[i] = S_of(i);
+      R.out[i] = reinterpret_cast<__nv_bfloat16*>(P_save[i]);
+    }
+    const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
+    const double tri = static_cast<double>(rows) * (T + 1) / 2.0;
+    TraceScope tr(st, TTL_K_SOFTMAX, 0.0, tri * (4.0 + 2.0));
+    const float k = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    attn_softmax_fwd_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
+        R, rows, T, s.nql, k);
+    if ((rc = cuda_check(cudaGetLastError(), "attn_softmax_fwd_kernel launch"))) return rc;
+  }
+
+  // O_c = P_c V_g into head c's columns of O_i; the K loop stops at the tile's last query.
+  for (int i = 0; i < t; ++i) {
+    for (int64_t c = 0; c < s.nql; ++c) {
+      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+      const int mp = batch.add_map(P_save[i], s.nql * T, T, T, false);
+      const int mv = batch.add_map(V_save[i], T, s.kc, s.kc, true);
+      Problem* p = batch.add_problem(T, d, false, true, EPI_BF16, false);
+      if (batch.error()) return batch.error();
+      p->causal = CAUSAL_K_UPTO_ROW;
+      p->a_m0 = static_cast<int32_t>(c * T);
+      p->b_n0 = static_cast<int32_t>((c / s.grp) * d);
+      p->out0 = O_save[i] + c * d;
+      p->ld_out = s.qc;
+      if ((rc = batch.add_seg(p, mp, 0, mv, -1, 0, T))) return rc;
+    }
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // Row-parallel W_O: the full-shape partial Y_i = O_i Wo_i.
+  for (int i = 0; i < t; ++i) {
+    if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+    const int mo = batch.add_map(O_save[i], T, s.qc, s.qc, false);
+    const int mw = batch.add_map(Wo[i], s.qc, h, h, true);
+    Problem* p = batch.add_problem(T, h, false, true, EPI_BF16, false);
+    if (batch.error()) return batch.error();
+    p->out0 = Y[i];
+    p->ld_out = h;
+    if ((rc = batch.add_seg(p, mo, 0, mw, -1, 0, s.qc))) return rc;
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // g forward: all-reduce of the partials.
+  return shard_all_reduce_internal(t, T, h, Y, nullptr, st);
+}
+
+extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const ttl_bf16* X,
+                               const ttl_bf16* dY, const ttl_bf16* const* Wq, const ttl_bf16* const* Wk,
+                               const ttl_bf16* const* Wv, const ttl_bf16* const* Wo, const ttl_bf16* const* Q_save,
+                               const ttl_bf16* const* K_save, const ttl_bf16* const* V_save,
+                               const ttl_bf16* const* P_save, const ttl_bf16* const* O_save, ttl_bf16* const* dWq,
+                               ttl_bf16* const* dWk, ttl_bf16* const* dWv, ttl_bf16* const* dWo,
+                               ttl_bf16* const* dX, void* ws, size_t ws_bytes, void* stream) {
+  const char* name = "ttl_tp_attn_bwd";
+  Shape s;
+  int rc = check_shape(t, T, h, n_q, n_kv, d, name, &s);
+  if (rc) return rc;
+  using CP = const void* const*;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  {
+    const struct { CP p; const char* n; } outs[] = {{reinterpret_cast<CP>(dWq), "dWq"},
+                                                    {reinterpret_cast<CP>(dWk), "dWk"},
+                                                    {reinterpret_cast<CP>(dWv), "dWv"},
+                                                    {reinterpret_cast<CP>(dWo), "dWo"}};
+    for (const auto& a : outs)
+      if ((rc = check_ptrs(a.p, t, a.n))) return rc;
+  }
+  if (T == 0) {   // no tokens: the weight gradients are empty sums
+    for (int i = 0; i < t; ++i) {
+      if ((rc = fill_zero(dWq[i], h * s.qc * 2, st))) return rc;
+      if ((rc = fill_zero(dWk[i], h * s.kc * 2, st))) return rc;
+      if ((rc = fill_zero(dWv[i], h * s.kc * 2, st))) return rc;
+      if ((rc = fill_zero(dWo[i], s.qc * h * 2, st))) return rc;
+    }
+    return TTL_OK;
+  }
+  if (!X || !dY) return set_error(TTL_ERR_ARG, "%s: X or dY is null", name);
+  if (!aligned16(X) || !aligned16(dY)) return set_error(TTL_ERR_ALIGN, "%s: X or dY not 16-byte aligned", name);
+  {
+    const struct { CP p; const char* n; } arrs[] = {
+        {reinterpret_cast<CP>(Wq), "Wq"},         {reinterpret_cast<CP>(Wk), "Wk"},
+        {reinterpret_cast<CP>(Wv), "Wv"},         {reinterpret_cast<CP>(Wo), "Wo"},
+        {reinterpret_cast<CP>(Q_save), "Q_save"}, {reinterpret_cast<CP>(K_save), "K_save"},
+        {reinterpret_cast<CP>(V_save), "V_save"}, {reinterpret_cast<CP>(P_save), "P_save"},
+        {reinterpret_cast<CP>(O_save), "O_save"}, {reinterpret_cast<CP>(dX), "dX"}};
+    for (const auto& a : arrs)
+      if ((rc = check_ptrs(a.p, t, a.n))) return rc;
+  }
+  const size_t need = ttl_tp_attn_bwd_workspace_size(t, T, n_q, n_kv, d);
+  if (!ws || ws_bytes < need)
+    return set_error(TTL_ERR_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
+  if (!aligned16(ws)) return set_error(TTL_ERR_ALIGN, "%s: workspace not 16-byte aligned", name);
+
+  // Workspace, per shard: dP (fp32 scores), dS (bf16 scores), dO_i, dQ_i, dK_i, dV_i.
+  const size_t b_dp = score_bytes(s, 4), b_ds = score_bytes(s, 2);
+  const size_t b_q = round256(static_cast<size_t>(T) * 2 * s.qc), b_k = round256(static_cast<size_t>(T) * 2 * s.kc);
+  const size_t per = b_dp + b_ds + 2 * b_q + 2 * b_k;
+  auto base = [&](int i) { return static_cast<char*>(ws) + per * static_cast<size_t>(i); };
+  auto dP_of = [&](int i) { return reinterpret_cast<float*>(base(i)); };
+  auto dS_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp); };
+  auto dO_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds); };
+  auto dQ_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds + b_q); };
+  auto dK_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds + 2 * b_q); };
+  auto dV_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds + 2 * b_q + b_k); };
+  GemmBatch batch;
+
+  // g backward is the identity: dO_i = dY Wo_i^T (one tile group over dY) and dWo_i = O_i^T dY.
+  for (int i = 0; i < t; ++i) {
+    if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+    const int md = batch.add_map(dY, T, h, h, false);
+    const int mw = batch.add_map(Wo[i], s.qc, h, h, false);
+    Problem* p = batch.add_problem(T, s.qc, false, false, EPI_BF16, false, true);
+    if (batch.error()) return batch.error();
+    p->out0 = dO_of(i);
+    p->ld_out = s.qc;
+    if ((rc = batch.add_seg(p, md, 0, mw, -1, 0, h))) return rc;
+  }
+  for (int i = 0; i < t; ++i) {
+    if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+    const int mo = batch.add_map(O_save[i], T, s.qc, s.qc, true);
+    const int md = batch.add_map(dY, T, h, h, true);
+    Problem* p = batch.add_problem(s.qc, h, true, true, EPI_BF16, false);
+    if (batch.error()) return batch.error();
+    p->out0 = dWo[i];
+    p->ld_out = h;
+    if ((rc = batch.add_seg(p, mo, 0, md, -1, 0, T))) return rc;
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // dP_c = dO_c V_g^T (fp32), tiles above the diagonal skipped.
+  for (int i = 0; i < t; ++i) {
+    for (int64_t c = 0; c < s.nql; ++c) {
+      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+      const int mdo = batch.add_map(dO_of(i), T, s.qc, s.qc, false);
+      const int mv = batch.add_map(V_save[i], T, s.kc, s.kc, false);
+      Problem* p = batch.add_problem(T, T, false, false, EPI_F32, false);
+      if (batch.error()) return batch.error();
+      p->causal = CAUSAL_SKIP_UPPER;
+      p->out0 = dP_of(i) + c * T * T;
+      p->ld_out = T;
+      if ((rc = batch.add_seg(p, mdo, c * d, mv, -1, (c / s.grp) * d, d))) return rc;
+    }
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // Softmax backward into dS.
+  {
+    AttnRows R = {};
+    for (int i = 0; i < t; ++i) {
+      R.s[i] = dP_of(i);
+      R.p[i] = bf(P_save[i]);
+      R.out[i] = dS_of(i);
+      R.dO[i] = dO_of(i);
+      R.o[i] = bf(O_save[i]);
+    }
+    const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
+    const double tri = static_cast<double>(rows) * (T + 1) / 2.0;
+    TraceScope tr(st, TTL_K_SOFTMAX, 0.0, tri * (4.0 + 2.0 + 2.0) + static_cast<double>(rows) * d * 4.0);
+    attn_softmax_bwd_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
+        R, rows, T, s.nql, d, static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))));
+    if ((rc = cuda_check(cudaGetLastError(), "attn_softmax_bwd_kernel launch"))) return rc;
+  }
+
+  // dQ_c = dS_c K_g: the K loop stops at the tile's last query.
+  for (int i = 0; i < t; ++i) {
+    for (int64_t c = 0; c < s.nql; ++c) {
+      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+      const int ms = batch.add_map(dS_of(i), s.nql * T, T, T, false);
+      const int mk = batch.add_map(K_save[i], T, s.kc, s.kc, true);
+      Problem* p = batch.add_problem(T, d, false, true, EPI_BF16, false);
+      if (batch.error()) return batch.error();
+      p->causal = CAUSAL_K_UPTO_ROW;
+      p->a_m0 = static_cast<int32_t>(c * T);
+      p->b_n0 = static_cast<int32_t>((c / s.grp) * d);
+      p->out0 = dQ_of(i) + c * d;
+      p->ld_out = s.qc;
+      if ((rc = batch.add_seg(p, ms, 0, mk, -1, 0, T))) return rc;
+    }
+  }
+  // dK_g = sum_c dS_c^T Q_c and dV_g = sum_c P_c^T dO_c over the group's query heads, one K
+  // segment per head; the K loop (queries) starts at the tile's first key.
+  for (int i = 0; i < t; ++i) {
+    for (int64_t g = 0; g < s.nkvl; ++g) {
+      for (int w = 0; w < 2; ++w) {
+        if (!batch.has_room(static_cast<int>(2 * s.grp), 1) && (rc = batch.flush(st))) return rc;
+        const __nv_bfloat16* a_base = w == 0 ? dS_of(i) : bf(P_save[i]);
+        const void* b_base = w == 0 ? static_cast<const void*>(Q_save[i]) : static_cast<const void*>(dO_of(i));
+        const int mb = batch.add_map(b_base, T, s.qc, s.qc, true);
+        Problem* p = batch.add_problem(T, d, true, true, EPI_BF16, false);
+        if (batch.error()) return batch.error();
+        p->causal = CAUSAL_K_FROM_ROW;
+        p->out0 = (w == 0 ? dK_of(i) : dV_of(i)) + g * d;
+        p->ld_out = s.kc;
+        for (int64_t c = g * s.grp; c < (g + 1) * s.grp; ++c) {
+          int64_t k0 = 0;
+          const int ma = head_block_map(batch, a_base, s, c, &k0);
+          if (batch.error()) return batch.error();
+          if ((rc = batch.add_seg(p, ma, k0, mb, -1, 0, T, c * d))) return rc;
+        }
+      }
+    }
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // Column-parallel projections backward: dW{q,k,v}_i = X^T d{Q,K,V}_i (one tile group over
+  // X^T) and the dX partials dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T (three K segments).
+  for (int i = 0; i < t; ++i) {
+    const __nv_bfloat16* G[3] = {dQ_of(i), dK_of(i), dV_of(i)};
+    ttl_bf16* const* dW[3] = {dWq, dWk, dWv};
+    for (int w = 0; w < 3; ++w) {
+      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+      const int64_t cols = w == 0 ? s.qc : s.kc;
+      const int mx = batch.add_map(X, T, h, h, true);
+      const int mg = batch.add_map(G[w], T, cols, cols, true);
+      Problem* p = batch.add_problem(h, cols, true, true, EPI_BF16, false, true);
+      if (batch.error()) return batch.error();
+      p->out0 = dW[w][i];
+      p->ld_out = cols;
+      if ((rc = batch.add_seg(p, mx, 0, mg, -1, 0, T))) return rc;
+    }
+  }
+  for (int i = 0; i < t; ++i) {
+    const __nv_bfloat16* G[3] = {dQ_of(i), dK_of(i), dV_of(i)};
+    const ttl_bf16* const* W[3] = {Wq, Wk, Wv};
+    if (!batch.has_room(6, 1) && (rc = batch.flush(st))) return rc;
+    Problem* p = batch.add_problem(T, h, false, false, EPI_BF16, false);
+    if (batch.error()) return batch.error();
+    p->out0 = dX[i];
+    p->ld_out = h;
+    for (int w = 0; w < 3; ++w) {
+      const int64_t cols = w == 0 ? s.qc : s.kc;
+      const int mg = batch.add_map(G[w], T, cols, cols, false);
+      const int mw = batch.add_map(W[w][i], h, cols, cols, false);
+      if (batch.error()) return batch.error();
+      if ((rc = batch.add_seg(p, mg, 0, mw, -1, 0, cols))) return rc;
+    }
+  }
+  if ((rc = batch.flush(st))) return rc;
+
+  // f backward: all-reduce of the dX partials.
+  return shard_all_reduce_internal(t, T, h, dX, nullptr, st);
+}

@@ -91,6 +91,24 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile) 
   return c;
 }
 
+// Causal structure: whether a tile has any work, and the k-block range of one segment.
+template <int TILE_M>
+__device__ __forceinline__ bool tile_skipped(const Problem& pr, const TileCoord& c) {
+  return pr.causal == CAUSAL_SKIP_UPPER && c.tn * BN >= (c.tm + 1) * TILE_M;
+}
+
+template <int TILE_M>
+__device__ __forceinline__ void seg_kblocks(const Problem& pr, const Seg& sg, const TileCoord& c, int& kb0,
+                                            int& kb1) {
+  kb0 = 0;
+  kb1 = sg.kblocks;
+  if (pr.causal == CAUSAL_K_UPTO_ROW) {
+    kb1 = min(kb1, ((c.tm + 1) * TILE_M + BK - 1) / BK);
+  } else if (pr.causal == CAUSAL_K_FROM_ROW) {
+    kb0 = min(kb1, (c.tm * TILE_M) / BK);
+  }
+}
+
 // ------------------------------------------------------------------ epilogue math
 
 // The epilogue math uses the fast exponential intrinsic: its results are rounded to bf16
@@ -210,11 +228,12 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
   if (epi == EPI_F32_CE && row_ok) ce_tgt = reinterpret_cast<const int64_t*>(pr.aux0)[row] - pr.ext0 - n_base;
 #pragma unroll 1
   for (int ch = 0; ch < BN / 32; ++ch) {
+    const int col0 = n_base + ch * 32;
+    if (col0 >= pr.N) break;   // the same for the whole warp: nothing left to store
     uint32_t r[32];
     __syncwarp();
     tmem_ld_32x32b_x32(tbase + ch * 32, r);
     tmem_ld_wait();
-    const int col0 = n_base + ch * 32;
     if (row_ok && col0 < pr.N) {
       float v[32];
 #pragma unroll
@@ -347,6 +366,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.probs[c.p];
+        if (tile_skipped<C::TILE_M>(pr, c)) continue;
         int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
         int slab = 0;
         if (pr.a_slab_rows > 0) {   // rows of token slab `slab` come from its own map
@@ -358,9 +378,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
           const CUtensorMap* ma = &P.maps[sg.map_a + slab];
           const CUtensorMap* mb0 = &P.maps[sg.map_b];
           const CUtensorMap* mb1 = pr.paired ? &P.maps[sg.map_b2] : mb0;
-          const int bn0 = pr.paired ? pr.b_n0 + c.tn * (BN / 2) : pr.b_n0 + c.tn * BN;
-          const int bn1 = pr.paired ? bn0 : bn0 + BN / 2;
-          for (int kb = 0; kb < sg.kblocks; ++kb) {
+          const int bnb = pr.b_n0 + sg.b_n1;
+          const int bn0 = pr.paired ? bnb + c.tn * (BN / 2) : bnb + c.tn * BN;
+          // The second half of the B columns: a pair's second CTA supplies columns
+          // [N/2, N) of the MMA (64 of a 128-column one); paired tiles share coordinates.
+          const int bn1 = pr.paired ? bn0 : bn0 + (pr.half_n ? BN / 4 : BN / 2);
+          const bool b_half = !PAIR && pr.half_n;   // one CTA, 128 columns: no second B box
+          int kb0, kb1;
+          seg_kblocks<C::TILE_M>(pr, sg, c, kb0, kb1);
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, status, tmo)) {
               ok = false;
               break;
@@ -389,7 +415,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
                 tma_load_2d_pair(sb + 8192, mb, fb, bn + 64, kbb);
               }
             } else {
-              mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+              mbar_arrive_expect_tx(&full_bar[stage], b_half ? C::TX_BYTES - 16384 : C::TX_BYTES);
               if (!pr.a_mn) {
                 tma_load_2d(sa, ma, &full_bar[stage], ka, am);
               } else {
@@ -398,12 +424,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
               }
               if (!pr.b_mn) {
                 tma_load_2d(sb, mb0, &full_bar[stage], kbb, bn0);
-                tma_load_2d(sb + 16384, mb1, &full_bar[stage], kbb, bn1);
+                if (!b_half) tma_load_2d(sb + 16384, mb1, &full_bar[stage], kbb, bn1);
               } else {
                 tma_load_2d(sb, mb0, &full_bar[stage], bn0, kbb);
                 tma_load_2d(sb + 8192, mb0, &full_bar[stage], bn0 + 64, kbb);
-                tma_load_2d(sb + 16384, mb1, &full_bar[stage], bn1, kbb);
-                tma_load_2d(sb + 24576, mb1, &full_bar[stage], bn1 + 64, kbb);
+                if (!b_half) {
+                  tma_load_2d(sb + 16384, mb1, &full_bar[stage], bn1, kbb);
+                  tma_load_2d(sb + 24576, mb1, &full_bar[stage], bn1 + 64, kbb);
+                }
               }
             }
             ++issued;
@@ -445,21 +473,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.probs[c.p];
+        if (tile_skipped<C::TILE_M>(pr, c)) continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        const uint32_t idesc = idesc_bf16_f32(C::TILE_M, BN, pr.a_mn != 0, pr.b_mn != 0);
+        const uint32_t idesc = idesc_bf16_f32(C::TILE_M, pr.half_n ? BN / 2 : BN, pr.a_mn != 0, pr.b_mn != 0);
         const uint32_t a_step = pr.a_mn ? 2048u : 32u;
         const uint32_t b_step = pr.b_mn ? 2048u : 32u;
         const uint32_t a_lbo = pr.a_mn ? 8192u : 16u;
         const uint32_t b_lbo = pr.b_mn ? 8192u : 16u;
         uint32_t accumulate = 0;
         for (int s = 0; ok && s < pr.nseg; ++s) {
-          const int nkb = pr.seg[s].kblocks;
-          for (int kb = 0; kb < nkb; ++kb) {
+          int kb0, kb1;
+          seg_kblocks<C::TILE_M>(pr, pr.seg[s], c, kb0, kb1);
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full_bar[stage], phase, abort_flag, status, tmo)) {
               ok = false;
               break;
@@ -514,6 +544,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     for (int tile = unit; tile < P.total_tiles; tile += nunits) {
       const TileCoord c = decode_tile(P, tile);
       const Problem& pr = P.probs[c.p];
+      if (tile_skipped<C::TILE_M>(pr, c)) continue;
       const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
@@ -720,7 +751,8 @@ Problem* GemmBatch::add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int 
   return p;
 }
 
-int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K) {
+int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K,
+                       int64_t b_n1) {
   if (err_) return err_;
   if (!p || map_a < 0 || map_b < 0 || (p->paired && map_b2 < 0)) return err_ = set_error(TTL_ERR_ARG, "bad GEMM segment");
   if (p->nseg >= kMaxSegs) return err_ = set_error(TTL_ERR_ARG, "GEMM problem: too many K segments");
@@ -732,14 +764,18 @@ int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b
   s.a_k0 = static_cast<int32_t>(a_k0);
   s.b_k0 = static_cast<int32_t>(b_k0);
   s.kblocks = static_cast<int32_t>((K + BK - 1) / BK);
+  s.b_n1 = static_cast<int32_t>(b_n1);
   const double ncols = p->paired ? 2.0 * p->N : static_cast<double>(p->N);
-  flops_ += 2.0 * p->M * ncols * static_cast<double>(K);
-  bytes_ += 2.0 * (static_cast<double>(p->M) * K + ncols * K);
+  // A causal problem is square in its token dimension (M = T queries or keys): only the
+  // (T + 1) / (2 T) of it on or below the diagonal is work.
+  const double tri = p->causal != CAUSAL_NONE ? (p->M + 1.0) / (2.0 * p->M) : 1.0;
+  flops_ += 2.0 * p->M * ncols * static_cast<double>(K) * tri;
+  bytes_ += 2.0 * (static_cast<double>(p->M) * K + ncols * K) * tri;
   if (p->nseg == 1) {
     const int nout = p->epi == EPI_SWIGLU_FWD ? 3 : (p->epi == EPI_GELU_FWD || p->epi == EPI_SWIGLU_BWD) ? 2 : 1;
     const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : p->epi == EPI_GELU_BWD ? 1 : 0;
     const double esz = (p->epi == EPI_F32 || p->epi == EPI_F32_CE) ? 4.0 : 2.0;
-    bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux);
+    bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux) * (p->causal == CAUSAL_SKIP_UPPER ? tri : 1.0);
   }
   return TTL_OK;
 }
@@ -762,7 +798,8 @@ int GemmBatch::launch(cudaStream_t stream) {
     if (p.nseg == 0) return set_error(TTL_ERR_ARG, "GEMM problem %d has no K segment", i);
     // Every TMA x coordinate (innermost, in elements) must be a multiple of 8 bf16 = 16 bytes.
     bool aligned = (p.a_m0 % 8 == 0) && (p.b_n0 % 8 == 0);
-    for (int k = 0; k < p.nseg; ++k) aligned = aligned && p.seg[k].a_k0 % 8 == 0 && p.seg[k].b_k0 % 8 == 0;
+    for (int k = 0; k < p.nseg; ++k)
+      aligned = aligned && p.seg[k].a_k0 % 8 == 0 && p.seg[k].b_k0 % 8 == 0 && p.seg[k].b_n1 % 8 == 0;
     if (!aligned) return set_error(TTL_ERR_ALIGN, "GEMM problem %d: operand offsets must be multiples of 8", i);
     if (p.M > max_m) max_m = p.M;
   }
@@ -791,6 +828,7 @@ int GemmBatch::launch(cudaStream_t stream) {
     const int tn = p.paired ? BN / 2 : BN;
     p.tiles_m = (p.M + tile_m - 1) / tile_m;
     p.tiles_n = (p.N + tn - 1) / tn;
+    p.half_n = !p.paired && p.N <= BN / 2;
     if (!p.join || p_->ngroups == 0) {
       TileGroup& g = p_->groups[p_->ngroups++];
       g.tile_start = total;

@@ -49,7 +49,7 @@ struct TraceScope {
 // ------------------------------------------------------------------ GEMM problem block
 
 constexpr int kGemmBN = 256;   // accumulator columns per GEMM tile
-constexpr int kMaxMaps = 40;
+constexpr int kMaxMaps = 64;
 constexpr int kMaxProblems = 32;
 constexpr int kMaxSegs = kMaxShards;
 
@@ -66,11 +66,20 @@ enum Epilogue : int {
                        // when that column is in the tile
 };
 
+// Causal structure of a problem whose rows or columns are token positions (attention).
+enum Causal : int {
+  CAUSAL_NONE = 0,
+  CAUSAL_SKIP_UPPER = 1,   // rows = queries, cols = keys: tiles wholly above the diagonal are skipped
+  CAUSAL_K_UPTO_ROW = 2,   // rows = queries, K = keys: each segment's K loop stops after the tile's last row
+  CAUSAL_K_FROM_ROW = 3,   // rows = keys, K = queries: each segment's K loop starts at the tile's first row
+};
+
 // One K-range of a problem: k-blocks of 64 read from map_a at K offset a_k0 and from
-// map_b (and, for a paired tile, map_b2) at K offset b_k0.
+// map_b (and, for a paired tile, map_b2) at K offset b_k0; b_n1 is added to B's N
+// coordinate for this segment only (e.g. one head's columns of a head-major operand).
 struct Seg {
   int16_t map_a, map_b, map_b2, pad;
-  int32_t a_k0, b_k0, kblocks, pad2;
+  int32_t a_k0, b_k0, kblocks, b_n1;
 };
 
 // One output matrix [M, N]; tiles of 128 rows x 256 accumulator columns.  A paired tile
@@ -87,7 +96,8 @@ struct Problem {
   uint8_t epi, nseg;
   uint8_t paired;
   uint8_t join;           // 1 = same tile group as the previous problem (shares its A rows)
-  uint8_t pad[2];
+  uint8_t causal;         // CAUSAL_*: work a lower-triangular (query x key) structure skips
+  uint8_t half_n;         // set by launch() when N <= 128 (unpaired): the MMAs are 128 columns wide
   Seg seg[kMaxSegs];
   void* out0;
   void* out1;
@@ -121,6 +131,8 @@ struct GemmParams {
   int* status;
   uint64_t timeout_ns;
 };
+// The block travels as a __grid_constant__ kernel parameter (at most 32764 bytes).
+static_assert(sizeof(GemmParams) <= 32764, "GEMM parameter block exceeds the kernel parameter limit");
 
 // Host-side builder: collects tensor maps and problems, then launches the persistent
 // tcgen05 GEMM kernel once for all of them.
@@ -140,7 +152,9 @@ class GemmBatch {
   // join = true puts the problem in the previous problem's tile group; use it when both
   // read the same A rows (same A tensor, same a_m0, same M).
   Problem* add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired, bool join = false);
-  int add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K);
+  // Set p->causal before adding its segments: the FLOP and byte counts of the trace follow it.
+  int add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K,
+              int64_t b_n1 = 0);
   int launch(cudaStream_t stream);
   int error() const { return err_; }
   // True if `maps` more operands and `probs` more problems still fit in this launch.

@@ -113,6 +113,33 @@ def test_gtp_and_ce_validation(lib):
     assert lib.ttl_gemm(8, 12, 16, 0x10000, 16, 1, 0x20000, 16, 1, 0x30000, 12, 0, None) == 2
 
 
+def test_attention_validation(lib):
+    sh = _arr(0x10000, 0x20000)
+    X, ws = 0x90000, 0xA0000
+    fwd = lib.ttl_tp_attn_fwd
+    ten = [sh] * 10   # Wq Wk Wv Wo Q K V P O Y
+
+    def call(t, T, h, nq, nkv, d, x=X, arrs=ten, w=ws, wb=1 << 40):
+        return fwd(t, T, h, nq, nkv, d, x, *arrs, w, wb, None)
+    assert call(3, 64, 64, 32, 8, 128) == 2          # t does not divide the head counts
+    assert call(2, 64, 64, 8, 3, 128) == 2           # t does not divide n_kv
+    assert call(2, 64, 64, 6, 4, 128) == 2           # n_kv does not divide n_q
+    assert call(2, 64, 64, 8, 2, 96) == 2            # head dimension not a multiple of 64
+    assert call(2, 60, 64, 8, 2, 128) == 2           # T not a multiple of 8
+    assert call(2, 64, 64, 8, 2, 128, x=X + 2) == 3  # misaligned X
+    assert call(2, 64, 64, 8, 2, 128, arrs=[sh] * 9 + [None]) == 1   # Y missing
+    assert call(2, 64, 64, 8, 2, 128, wb=16) == 1    # workspace too small
+    assert call(2, 0, 64, 8, 2, 128) == 0            # no tokens: nothing to do
+    # fp32 scores, one [n_q/t, T, T] block per shard
+    assert lib.ttl_tp_attn_fwd_workspace_size(2, 64, 8, 2, 128) == 2 * 4 * 64 * 64 * 4
+    per = 4 * 64 * 64 * 4 + 4 * 64 * 64 * 2 + 2 * (64 * 512 * 2) + 2 * (64 * 128 * 2)
+    assert lib.ttl_tp_attn_bwd_workspace_size(2, 64, 8, 2, 128) == 2 * per
+    assert lib.ttl_tp_attn_bwd_workspace_size(3, 64, 8, 2, 128) == 0    # invalid shape
+    bwd = lib.ttl_tp_attn_bwd
+    assert bwd(2, 64, 64, 8, 2, 128, X, X, *([sh] * 9), sh, sh, sh, None, sh, ws, 1 << 40, None) == 1  # dWo missing
+    assert bwd(2, 64, 64, 8, 2, 128, X, X, *([sh] * 9), sh, sh, sh, sh, sh, ws, 16, None) == 1         # workspace
+
+
 def test_selftest_bounds(lib):
     assert lib.ttl_selftest_wait_timeout(0, None) == 1
     assert lib.ttl_selftest_wait_timeout(2_000_000, None) == 1

@@ -69,3 +69,56 @@ def test_heads_per_shard_printed_counts():
         assert (ck.stop - ck.start) // d == row["kv_heads"]
     with pytest.raises(ValueError):
         attention.tp_attention_forward(np.zeros((2, 4)), {}, 3, 32, 8, 1)   # 3 does not divide 32
+
+
+def _torch_block_grads(X, W, dY, n_q, n_kv):
+    """Autograd of the unsharded block through torch's causal scaled_dot_product_attention."""
+    T = X.shape[0]
+    d = W["Wq"].shape[1] // n_q
+    Xt = torch.tensor(X, requires_grad=True)
+    Wt = {k: torch.tensor(v) for k, v in W.items()}
+    q = (Xt @ Wt["Wq"]).reshape(T, n_q, d).transpose(0, 1)
+    k = (Xt @ Wt["Wk"]).reshape(T, n_kv, d).transpose(0, 1).repeat_interleave(n_q // n_kv, 0)
+    v = (Xt @ Wt["Wv"]).reshape(T, n_kv, d).transpose(0, 1).repeat_interleave(n_q // n_kv, 0)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True).transpose(0, 1).reshape(T, -1)
+    Y = o @ Wt["Wo"]
+    (Y * torch.tensor(dY)).sum().backward()
+    return Y.detach().numpy(), Xt.grad.numpy()
+
+
+def test_row_functions_match_torch_autograd():
+    rng = np.random.default_rng(5)
+    T, h, n_q, n_kv, d = 11, 10, 6, 2, 4
+    W = {"Wq": rng.standard_normal((h, n_q * d)) * 0.5, "Wk": rng.standard_normal((h, n_kv * d)) * 0.5,
+         "Wv": rng.standard_normal((h, n_kv * d)) * 0.5, "Wo": rng.standard_normal((n_q * d, h)) * 0.5}
+    X = rng.standard_normal((T, h))
+    dY = rng.standard_normal((T, h))
+    Y, dX = _torch_block_grads(X, W, dY, n_q, n_kv)
+    rows = np.array([0, 3, 7, 10])
+    np.testing.assert_allclose(attention.forward_rows(X, W, n_q, n_kv, d, rows), Y[rows], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(attention.backward_rows_dx(X, W, dY, n_q, n_kv, d, rows), dX[rows],
+                               rtol=1e-10, atol=1e-12)
+    # the first query sees only itself: its output is its own value row through W_O
+    V0 = X[0] @ W["Wv"]
+    o0 = np.concatenate([V0[(c // (n_q // n_kv)) * d:(c // (n_q // n_kv) + 1) * d] for c in range(n_q)])
+    np.testing.assert_allclose(attention.forward_rows(X, W, n_q, n_kv, d, [0])[0], o0 @ W["Wo"], rtol=1e-13)
+
+
+def test_gradient_of_rows_beyond_the_last_nonzero_dY_row_is_zero():
+    """With dY zero below row m the block's gradients equal those of the first m tokens alone
+    (causality): dX rows >= m vanish and the weight gradients match the truncated block."""
+    rng = np.random.default_rng(6)
+    T, m, h, n_q, n_kv, d, t = 12, 5, 8, 4, 2, 4, 2
+    W = {"Wq": rng.standard_normal((h, n_q * d)), "Wk": rng.standard_normal((h, n_kv * d)),
+         "Wv": rng.standard_normal((h, n_kv * d)), "Wo": rng.standard_normal((n_q * d, h))}
+    X = rng.standard_normal((T, h))
+    dY = rng.standard_normal((T, h))
+    dY[m:] = 0
+    full = attention.tp_attention_backward(X, W, t, n_q, n_kv, d, dY, attention.tp_attention_forward(X, W, t, n_q, n_kv, d))
+    cut = attention.tp_attention_backward(X[:m], W, t, n_q, n_kv, d, dY[:m],
+                                          attention.tp_attention_forward(X[:m], W, t, n_q, n_kv, d))
+    assert np.all(full["dX"][m:] == 0)
+    np.testing.assert_allclose(full["dX"][:m], cut["dX"], rtol=1e-10, atol=1e-12)
+    for k in ("dWq", "dWk", "dWv", "dWo"):
+        for i in range(t):
+            np.testing.assert_allclose(full[k][i], cut[k][i], rtol=1e-10, atol=1e-12)

@@ -144,3 +144,13 @@ def test_bf16_rounding_by_truncation_is_caught(monkeypatch):
         return ((f.view(np.uint32) >> 16) << 16).astype(np.uint32).view(np.float32)
     monkeypatch.setattr(numerics, "round_to_bf16", bad)
     _expect_failure(ttp.test_round_to_bf16_matches_torch_and_ties_to_even)
+
+
+def test_row_softmax_without_normalisation_is_caught(monkeypatch):
+    import test_oracle_attention as tatt
+    from oracle import attention
+
+    def bad(s):
+        return np.exp(s - s.max())                                # the division by the sum dropped
+    monkeypatch.setattr(attention, "_softmax_vec", bad)
+    _expect_failure(tatt.test_row_functions_match_torch_autograd)
