@@ -327,7 +327,10 @@ int ttl_vocab_parallel_embedding_bwd(int t, int64_t T, int64_t h, int64_t V, con
  *   P_save[i] [n_q/t, T, T] out: the probabilities, head-major; row q is written for keys
  *             j < min(T, round_up(q+1, 256)) (zeros above the diagonal), the rest is untouched
  *   Y[i] [T,h] out: partial O_i Wo_i, then the all-reduced block output in every buffer
- *   ws   workspace of ttl_tp_attn_fwd_workspace_size() bytes (the fp32 scores)
+ *   ws   workspace of ttl_tp_attn_fwd_workspace_size() bytes: the softmax row statistics
+ *        (a (max, sum) pair per query row and 256-key tile, then (max, 1/sum) per row); the
+ *        scores themselves never reach memory (the score GEMM runs twice, its epilogues
+ *        computing the statistics, then the probabilities)
  * t | n_q, t | n_kv, n_kv | n_q, d a multiple of 64, T and h multiples of 8.  Errors:
  * TTL_ERR_ARG (null or short arguments), TTL_ERR_SHAPE, TTL_ERR_ALIGN (pointers not 16-byte
  * aligned); nothing is launched when the call returns an error. */
@@ -344,7 +347,8 @@ int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const
  *   dY [T,h]; X, W*, *_save as given to / written by ttl_tp_attn_fwd
  *   dWq[i], dWk[i], dWv[i], dWo[i] out, shaped like the weights
  *   dX[i] [T,h] out: partial, then the all-reduced dX in every buffer
- *   ws   workspace of ttl_tp_attn_bwd_workspace_size() bytes
+ *   ws   workspace of ttl_tp_attn_bwd_workspace_size() bytes: rowsum(dO O) per query row,
+ *        then per shard dS [n_q/t, T, T] bf16 (written by the dP GEMM's epilogue), dO, dQ, dK, dV
  * T = 0 writes zero weight gradients (token-sized pointers may then be null). */
 size_t ttl_tp_attn_bwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d);
 int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const ttl_bf16* X,

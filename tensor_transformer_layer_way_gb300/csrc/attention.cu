@@ -10,18 +10,23 @@
 //
 // Every contraction runs in the tcgen05 GEMM; the causal structure is handled there (score
 // tiles above the diagonal are skipped, P V and dS K stop their K loop at the tile's last
-// query, dS^T Q and P^T dO start theirs at the tile's first key).  The scores are materialised
-// in fp32 and the row softmax and its backward are warp-per-row HBM streams:
-//   forward : QKV (3t problems) -> S = Q_c K_g^T (fp32) -> P = softmax(S / sqrt(d)) (bf16)
+// query, dS^T Q and P^T dO start theirs at the tile's first key).  The softmax lives in the
+// score GEMMs' epilogues, so no fp32 score matrix reaches HBM:
+//   forward : QKV (3t problems) -> S = Q_c K_g^T, epilogue: per row and 256-key tile the max and
+//             sum of exp2 of the scaled scores -> combine per row into (max, 1 / sum)
+//             -> S again, epilogue: P = exp2(S log2(e) / sqrt(d) - max) / sum as bf16
 //             -> O_c = P_c V_g -> partial Y_i = O_i Wo_i -> all-reduce
-//   backward: {dO_i = dY Wo_i^T, dWo_i = O_i^T dY} -> dP = dO_c V_g^T (fp32)
-//             -> dS = P (dP - rowsum(dO_c O_c)) / sqrt(d) (bf16)
+//   backward: {dO_i = dY Wo_i^T, dWo_i = O_i^T dY} -> D = rowsum(dO_c O_c)
+//             -> dP = dO_c V_g^T, epilogue: dS = P (dP - D) / sqrt(d) as bf16
 //             -> {dQ_c = dS_c K_g, dK_g = sum_c dS_c^T Q_c, dV_g = sum_c P_c^T dO_c}
 //             -> {dW_i = X^T d{Q,K,V}_i, dX_i = dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T} -> all-reduce
+// The score GEMM runs twice in the forward (its K is only d): recomputing it costs less than
+// writing and re-reading T^2/2 fp32 scores per head.
 //
-// Zero fill: row q of P and of dS is written for every key j < min(T, round_up(q + 1, 256));
-// the keys above the diagonal get exact zeros.  That covers every element the causal GEMMs read
-// with either tile height (128 or 256 rows), so no full-size mask pass is needed.
+// Zero fill: row q of P and of dS is written for every key j < min(T, round_up(q + 1, 256)),
+// the span of the score tiles that are not skipped with either tile height (128 or 256 rows);
+// the keys above the diagonal get exact zeros.  That covers every element the causal GEMMs
+// read, so no full-size mask pass is needed.
 
 #include <cmath>
 
@@ -35,95 +40,56 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kRowWarps = 8;   // rows (one per warp) per CTA of the row kernels
 
-// Per-shard pointers of the row kernels; every [n_q/t, T, T] block is head-major and dense.
+// Per-shard pointers of the row kernels.
 struct AttnRows {
-  const float* s[kMaxShards];            // fp32 scores (forward) or score gradients dP (backward)
-  const __nv_bfloat16* p[kMaxShards];    // backward: saved probabilities
-  __nv_bfloat16* out[kMaxShards];        // P (forward) or dS (backward)
-  const __nv_bfloat16* dO[kMaxShards];   // backward: [T, n_q/t d]
-  const __nv_bfloat16* o[kMaxShards];    // backward: [T, n_q/t d]
+  const __nv_bfloat16* dO[kMaxShards];   // [T, n_q/t d]
+  const __nv_bfloat16* o[kMaxShards];    // [T, n_q/t d]
 };
-
-__device__ __forceinline__ void load8_f32(const float* p, float* v) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
 
 __device__ __forceinline__ void unpack8_bf16(uint4 w, float* v) {
   v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
   v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
 }
 
-__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
-  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                    pack_bf16x2(v[6], v[7]));
+// Combines (max, sum) pairs: sum of both sides rescaled to the larger max; an empty side
+// (m = -inf) weighs nothing.
+__device__ __forceinline__ void combine(float& m, float& l, float m2, float l2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  l = (m == -INFINITY ? 0.0f : l * exp2f(m - M)) + (m2 == -INFINITY ? 0.0f : l2 * exp2f(m2 - M));
+  m = M;
 }
 
-// exp2((x - m) * k) with an empty side (m = -inf) weighing nothing.
-__device__ __forceinline__ float rescale(float m, float M, float k) {
-  return m == -INFINITY ? 0.0f : exp2f((m - M) * k);
-}
-
-// One warp per (shard, head, query) row q: P[q, j] = exp(S[q, j] / sqrt(d) - max) / sum over
-// the keys j <= q, zeros for q < j < min(T, round_up(q + 1, 256)).  k = log2(e) / sqrt(d).
-__global__ void __launch_bounds__(kRowWarps * 32) attn_softmax_fwd_kernel(const __grid_constant__ AttnRows R,
-                                                                          int64_t rows, int64_t T, int64_t nql,
-                                                                          float k) {
+// One warp per (shard, head, query) row q: folds the (max, sum) partials of the score tiles
+// that hold keys 0..q (half tiles of 128 keys 0..2 (q/256) + 1; a half with no key <= q holds
+// (-inf, 0)) into (max, 1 / sum), the row statistics of the probabilities.
+__global__ void __launch_bounds__(kRowWarps * 32) attn_row_stats_kernel(const float2* __restrict__ part,
+                                                                        float2* __restrict__ stats, int64_t rows,
+                                                                        int64_t T, int ntiles) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
-  const int64_t per_shard = nql * T;
-  const int i = static_cast<int>(row / per_shard);
-  const int64_t r = row - i * per_shard;   // head * T + q
-  const int64_t q = r % T;
-  const float* srow = R.s[i] + r * T;
-  __nv_bfloat16* prow = R.out[i] + r * T;
-
+  const int64_t q = row % T;
+  const int n = 2 * (static_cast<int>(q / kGemmBN) + 1);
   float m = -INFINITY, l = 0.0f;
-  for (int64_t j0 = lane * 8; j0 <= q; j0 += 256) {
-    float v[8];
-    load8_f32(srow + j0, v);
-    float mx = m;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j0 + j <= q) mx = fmaxf(mx, v[j]);
-    float acc = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j0 + j <= q) acc += exp2f((v[j] - mx) * k);
-    l = l * rescale(m, mx, k) + acc;
-    m = mx;
+  for (int k = lane; k < n; k += 32) {
+    const float2 p = part[row * ntiles + k];
+    combine(m, l, p.x, p.y);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
     const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
-    const float M = fmaxf(m, m2);
-    l = l * rescale(m, M, k) + l2 * rescale(m2, M, k);
-    m = M;
+    combine(m, l, m2, l2);
   }
-  const float inv_l = 1.0f / l;
-  const int64_t z = min(T, ((q + 256) / 256) * 256);
-  for (int64_t j0 = lane * 8; j0 < z; j0 += 256) {
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (j0 <= q) {
-      float v[8];
-      load8_f32(srow + j0, v);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = (j0 + j <= q) ? exp2f((v[j] - m) * k) * inv_l : 0.0f;
-      w = pack8_bf16(v);
-    }
-    *reinterpret_cast<uint4*>(prow + j0) = w;
-  }
+  if (lane == 0) stats[row] = make_float2(m, 1.0f / l);
 }
 
-// One warp per row: D = sum_k dO[q, k] O[q, k] over the head's d columns, then
-// dS[q, j] = P[q, j] (dP[q, j] - D) / sqrt(d) for j <= q and zeros up to the same bound as P.
-__global__ void __launch_bounds__(kRowWarps * 32) attn_softmax_bwd_kernel(const __grid_constant__ AttnRows R,
-                                                                          int64_t rows, int64_t T, int64_t nql,
-                                                                          int d, float scale) {
+// One warp per (shard, head, query) row: D[q] = sum_k dO[q, k] O[q, k] over the head's d
+// columns (the rowsum term of the softmax backward).
+__global__ void __launch_bounds__(kRowWarps * 32) attn_rowdot_kernel(const __grid_constant__ AttnRows R,
+                                                                     float* __restrict__ D, int64_t rows,
+                                                                     int64_t T, int64_t nql, int d) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
@@ -133,33 +99,17 @@ __global__ void __launch_bounds__(kRowWarps * 32) attn_softmax_bwd_kernel(const 
   const int64_t c = r / T;
   const int64_t q = r - c * T;
   const int64_t hcol = q * nql * d + c * d;
-  float D = 0.0f;
+  float acc = 0.0f;
   for (int k0 = lane * 8; k0 < d; k0 += 256) {
     float a[8], b[8];
     unpack8_bf16(*reinterpret_cast<const uint4*>(R.dO[i] + hcol + k0), a);
     unpack8_bf16(*reinterpret_cast<const uint4*>(R.o[i] + hcol + k0), b);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) D = fmaf(a[j], b[j], D);
+    for (int j = 0; j < 8; ++j) acc = fmaf(a[j], b[j], acc);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) D += __shfl_xor_sync(0xffffffffu, D, off);
-
-  const float* dprow = R.s[i] + r * T;
-  const __nv_bfloat16* prow = R.p[i] + r * T;
-  __nv_bfloat16* dsrow = R.out[i] + r * T;
-  const int64_t z = min(T, ((q + 256) / 256) * 256);
-  for (int64_t j0 = lane * 8; j0 < z; j0 += 256) {
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (j0 <= q) {
-      float p[8], dp[8];
-      unpack8_bf16(*reinterpret_cast<const uint4*>(prow + j0), p);
-      load8_f32(dprow + j0, dp);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) p[j] = (j0 + j <= q) ? p[j] * (dp[j] - D) * scale : 0.0f;
-      w = pack8_bf16(p);
-    }
-    *reinterpret_cast<uint4*>(dsrow + j0) = w;
-  }
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) D[row] = acc;
 }
 
 struct Shape {
@@ -215,6 +165,24 @@ int head_block_map(GemmBatch& b, const __nv_bfloat16* base, const Shape& s, int6
 
 const __nv_bfloat16* bf(const ttl_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
 
+// (max, sum) partials per query row: one per half score tile (kGemmBN / 2 keys).
+int64_t key_tiles(const Shape& s) { return 2 * ((s.T + kGemmBN - 1) / kGemmBN); }
+
+// Forward workspace: the (max, sum) partials [t n_q/t T, key half tiles] and the row statistics
+// [t n_q/t T] (float2 each), rows ordered (shard, head, query).
+size_t fwd_part_bytes(const Shape& s) {
+  return round256(static_cast<size_t>(s.t * s.nql * s.T) * static_cast<size_t>(key_tiles(s)) * 8);
+}
+size_t fwd_ws_bytes(const Shape& s) { return fwd_part_bytes(s) + round256(static_cast<size_t>(s.t * s.nql * s.T) * 8); }
+
+// Backward workspace: D = rowsum(dO O) [t n_q/t T] fp32, then per shard dS (bf16 [n_q/t, T, T]),
+// dO, dQ ([T, n_q/t d]), dK, dV ([T, n_kv/t d]).
+size_t bwd_d_bytes(const Shape& s) { return round256(static_cast<size_t>(s.t * s.nql * s.T) * 4); }
+size_t bwd_shard_bytes(const Shape& s) {
+  const size_t tok = static_cast<size_t>(s.T) * 2;
+  return score_bytes(s, 2) + 2 * round256(tok * s.qc) + 2 * round256(tok * s.kc);
+}
+
 }  // namespace
 }  // namespace ttl
 
@@ -223,15 +191,13 @@ using namespace ttl;
 extern "C" size_t ttl_tp_attn_fwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d) {
   Shape s;
   if (check_shape(t, T, 8, n_q, n_kv, d, "ttl_tp_attn_fwd_workspace_size", &s)) return 0;
-  return score_bytes(s, 4) * static_cast<size_t>(t);
+  return fwd_ws_bytes(s);
 }
 
 extern "C" size_t ttl_tp_attn_bwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d) {
   Shape s;
   if (check_shape(t, T, 8, n_q, n_kv, d, "ttl_tp_attn_bwd_workspace_size", &s)) return 0;
-  const size_t tok = static_cast<size_t>(T) * 2;
-  const size_t per = score_bytes(s, 4) + score_bytes(s, 2) + 2 * round256(tok * s.qc) + 2 * round256(tok * s.kc);
-  return per * static_cast<size_t>(t);
+  return bwd_d_bytes(s) + bwd_shard_bytes(s) * static_cast<size_t>(t);
 }
 
 extern "C" int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const ttl_bf16* X,
@@ -261,8 +227,12 @@ extern "C" int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
   if (!aligned16(ws)) return set_error(TTL_ERR_ALIGN, "%s: workspace not 16-byte aligned", name);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t sb = score_bytes(s, 4);
-  auto S_of = [&](int i) { return reinterpret_cast<float*>(static_cast<char*>(ws) + sb * static_cast<size_t>(i)); };
+  const int64_t nt = key_tiles(s);
+  const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
+  float2* part = static_cast<float2*>(ws);
+  float2* stats = reinterpret_cast<float2*>(static_cast<char*>(ws) + fwd_part_bytes(s));
+  auto head_row0 = [&](int i, int64_t c) { return (static_cast<int64_t>(i) * s.nql + c) * T; };
+  const float k_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   GemmBatch batch;
 
   // Column-parallel projections: Q_i, K_i, V_i = X W{q,k,v}_i, one tile group over X.
@@ -283,36 +253,36 @@ extern "C" int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
   }
   if ((rc = batch.flush(st))) return rc;
 
-  // Scores S_c = Q_c K_g^T (fp32), tiles above the diagonal skipped.
-  for (int i = 0; i < t; ++i) {
-    for (int64_t c = 0; c < s.nql; ++c) {
-      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
-      const int mq = batch.add_map(Q_save[i], T, s.qc, s.qc, false);
-      const int mk = batch.add_map(K_save[i], T, s.kc, s.kc, false);
-      Problem* p = batch.add_problem(T, T, false, false, EPI_F32, false);
-      if (batch.error()) return batch.error();
-      p->causal = CAUSAL_SKIP_UPPER;
-      p->out0 = S_of(i) + c * T * T;
-      p->ld_out = T;
-      if ((rc = batch.add_seg(p, mq, c * d, mk, -1, (c / s.grp) * d, d))) return rc;
+  // Scores S_c = Q_c K_g^T twice (tiles above the diagonal skipped): first for the per-tile
+  // row statistics, then, with the combined statistics, for the probabilities themselves.
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+      TraceScope tr(st, TTL_K_SOFTMAX, 0.0, static_cast<double>(rows) * (nt / 2.0 + 1.0) * 8.0 + rows * 8.0);
+      attn_row_stats_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
+          part, stats, rows, T, static_cast<int>(nt));
+      if ((rc = cuda_check(cudaGetLastError(), "attn_row_stats_kernel launch"))) return rc;
     }
-  }
-  if ((rc = batch.flush(st))) return rc;
-
-  // Row softmax into the saved probabilities.
-  {
-    AttnRows R = {};
     for (int i = 0; i < t; ++i) {
-      R.s[i] = S_of(i);
-      R.out[i] = reinterpret_cast<__nv_bfloat16*>(P_save[i]);
+      for (int64_t c = 0; c < s.nql; ++c) {
+        if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+        const int mq = batch.add_map(Q_save[i], T, s.qc, s.qc, false);
+        const int mk = batch.add_map(K_save[i], T, s.kc, s.kc, false);
+        Problem* p = batch.add_problem(T, T, false, false, pass == 0 ? EPI_SMAX_STATS : EPI_SMAX_P, false);
+        if (batch.error()) return batch.error();
+        p->causal = CAUSAL_SKIP_UPPER;
+        p->fscale = k_log2;
+        if (pass == 0) {
+          p->out1 = part + head_row0(i, c) * nt;
+          p->ext1 = nt;
+        } else {
+          p->out0 = P_save[i] + c * T * T;
+          p->ld_out = T;
+          p->aux0 = stats + head_row0(i, c);
+        }
+        if ((rc = batch.add_seg(p, mq, c * d, mk, -1, (c / s.grp) * d, d))) return rc;
+      }
     }
-    const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
-    const double tri = static_cast<double>(rows) * (T + 1) / 2.0;
-    TraceScope tr(st, TTL_K_SOFTMAX, 0.0, tri * (4.0 + 2.0));
-    const float k = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-    attn_softmax_fwd_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
-        R, rows, T, s.nql, k);
-    if ((rc = cuda_check(cudaGetLastError(), "attn_softmax_fwd_kernel launch"))) return rc;
+    if ((rc = batch.flush(st))) return rc;
   }
 
   // O_c = P_c V_g into head c's columns of O_i; the K loop stops at the tile's last query.
@@ -397,17 +367,18 @@ extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
     return set_error(TTL_ERR_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
   if (!aligned16(ws)) return set_error(TTL_ERR_ALIGN, "%s: workspace not 16-byte aligned", name);
 
-  // Workspace, per shard: dP (fp32 scores), dS (bf16 scores), dO_i, dQ_i, dK_i, dV_i.
-  const size_t b_dp = score_bytes(s, 4), b_ds = score_bytes(s, 2);
+  // Workspace: D for every (shard, head, query) row, then per shard dS, dO_i, dQ_i, dK_i, dV_i.
+  const size_t b_ds = score_bytes(s, 2);
   const size_t b_q = round256(static_cast<size_t>(T) * 2 * s.qc), b_k = round256(static_cast<size_t>(T) * 2 * s.kc);
-  const size_t per = b_dp + b_ds + 2 * b_q + 2 * b_k;
-  auto base = [&](int i) { return static_cast<char*>(ws) + per * static_cast<size_t>(i); };
-  auto dP_of = [&](int i) { return reinterpret_cast<float*>(base(i)); };
-  auto dS_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp); };
-  auto dO_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds); };
-  auto dQ_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds + b_q); };
-  auto dK_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds + 2 * b_q); };
-  auto dV_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_dp + b_ds + 2 * b_q + b_k); };
+  float* Drow = static_cast<float*>(ws);
+  auto base = [&](int i) {
+    return static_cast<char*>(ws) + bwd_d_bytes(s) + bwd_shard_bytes(s) * static_cast<size_t>(i);
+  };
+  auto dS_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i)); };
+  auto dO_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds); };
+  auto dQ_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds + b_q); };
+  auto dK_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds + 2 * b_q); };
+  auto dV_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds + 2 * b_q + b_k); };
   GemmBatch batch;
 
   // g backward is the identity: dO_i = dY Wo_i^T (one tile group over dY) and dWo_i = O_i^T dY.
@@ -433,39 +404,40 @@ extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
   }
   if ((rc = batch.flush(st))) return rc;
 
-  // dP_c = dO_c V_g^T (fp32), tiles above the diagonal skipped.
+  // D = rowsum(dO_c O_c) for every (shard, head, query) row.
+  {
+    AttnRows R = {};
+    for (int i = 0; i < t; ++i) {
+      R.dO[i] = dO_of(i);
+      R.o[i] = bf(O_save[i]);
+    }
+    const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
+    TraceScope tr(st, TTL_K_SOFTMAX, 0.0, static_cast<double>(rows) * (4.0 * d + 4.0));
+    attn_rowdot_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
+        R, Drow, rows, T, s.nql, d);
+    if ((rc = cuda_check(cudaGetLastError(), "attn_rowdot_kernel launch"))) return rc;
+  }
+
+  // dP_c = dO_c V_g^T (tiles above the diagonal skipped); the epilogue turns it into
+  // dS = P (dP - D) / sqrt(d) with the saved probabilities.
   for (int i = 0; i < t; ++i) {
     for (int64_t c = 0; c < s.nql; ++c) {
       if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
       const int mdo = batch.add_map(dO_of(i), T, s.qc, s.qc, false);
       const int mv = batch.add_map(V_save[i], T, s.kc, s.kc, false);
-      Problem* p = batch.add_problem(T, T, false, false, EPI_F32, false);
+      Problem* p = batch.add_problem(T, T, false, false, EPI_SMAX_BWD, false);
       if (batch.error()) return batch.error();
       p->causal = CAUSAL_SKIP_UPPER;
-      p->out0 = dP_of(i) + c * T * T;
+      p->fscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+      p->out0 = dS_of(i) + c * T * T;
       p->ld_out = T;
+      p->aux0 = P_save[i] + c * T * T;
+      p->ld_aux = T;
+      p->aux1 = Drow + (static_cast<int64_t>(i) * s.nql + c) * T;
       if ((rc = batch.add_seg(p, mdo, c * d, mv, -1, (c / s.grp) * d, d))) return rc;
     }
   }
   if ((rc = batch.flush(st))) return rc;
-
-  // Softmax backward into dS.
-  {
-    AttnRows R = {};
-    for (int i = 0; i < t; ++i) {
-      R.s[i] = dP_of(i);
-      R.p[i] = bf(P_save[i]);
-      R.out[i] = dS_of(i);
-      R.dO[i] = dO_of(i);
-      R.o[i] = bf(O_save[i]);
-    }
-    const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
-    const double tri = static_cast<double>(rows) * (T + 1) / 2.0;
-    TraceScope tr(st, TTL_K_SOFTMAX, 0.0, tri * (4.0 + 2.0 + 2.0) + static_cast<double>(rows) * d * 4.0);
-    attn_softmax_bwd_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
-        R, rows, T, s.nql, d, static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))));
-    if ((rc = cuda_check(cudaGetLastError(), "attn_softmax_bwd_kernel launch"))) return rc;
-  }
 
   // dQ_c = dS_c K_g: the K loop stops at the tile's last query.
   for (int i = 0; i < t; ++i) {

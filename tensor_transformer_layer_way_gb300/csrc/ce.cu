@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const __grid_constant__ C
 }
 
 // Fused path, grid (T, t), one warp: shard i's statistics for token `tok` from the per-tile
-// partials the LM-head GEMM epilogue left (tps tiles per shard, ntot per token row), and the
+// partials the LM-head GEMM epilogue left (tps per shard, ntot per token row), and the
 // target logit the owning tile wrote.
 __global__ void __launch_bounds__(32) ce_stats_from_partials_kernel(const float2* part, const float* ztarget,
                                                                     const int64_t* target, int64_t T, int64_t Vs,
@@ -187,9 +187,9 @@ __global__ void __launch_bounds__(256) ce_dlogits_kernel(const __grid_constant__
 using namespace ttl;
 
 namespace {
-// Fused-statistics workspace: per token, one (max, sum exp) pair per GEMM n-tile of every
-// shard, then one target logit per token.
-int64_t ce_tiles_per_shard(int64_t Vs) { return (Vs + kGemmBN - 1) / kGemmBN; }
+// Fused-statistics workspace: per token, one (max, sum exp) pair per half GEMM n-tile
+// (kGemmBN / 2 vocabulary columns) of every shard, then one target logit per token.
+int64_t ce_tiles_per_shard(int64_t Vs) { return 2 * ((Vs + kGemmBN - 1) / kGemmBN); }
 size_t ce_part_bytes(int t, int64_t T, int64_t Vs) {
   return (static_cast<size_t>(T) * static_cast<size_t>(t * ce_tiles_per_shard(Vs)) * 8 + 255) & ~size_t(255);
 }

@@ -45,7 +45,7 @@ constexpr int BN = kGemmBN;        // accumulator columns per tile
 constexpr int BK = 64;             // K per stage
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int GROUP_M = 16;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;   // producer warp, MMA warp, 8 epilogue warps
 
 template <bool PAIR>
 struct Cfg {
@@ -69,8 +69,10 @@ struct TileCoord {
 // of GROUP_M m-tiles; within a band, n-tiles across all of the group's problems; within
 // an n-tile, the band's m-tiles.  Persistent workers taking consecutive indices therefore
 // share A rows (same band) and B columns (same n-tile) in L2.
-__device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile) {
-  int gi = 0;
+// `gi` is the caller's running group index: a worker visits increasing tile indices, so the
+// search for the tile's group resumes where the previous one ended (the parameter block
+// lives in constant memory, and a scan over dozens of groups per tile costs microseconds).
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile, int& gi) {
 #pragma unroll 1
   while (gi + 1 < P.ngroups && tile >= P.groups[gi + 1].tile_start) ++gi;
   const TileGroup& g = P.groups[gi];
@@ -81,9 +83,15 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile) 
   const int gm = min(GROUP_M, g.tiles_m - first_m);
   const int r = local - band * per_band;
   const int tn = r / gm;
-  int p = g.first;
+  // the problem holding n-tile tn: binary search over the group's first n-tiles
+  int lo = g.first, hi = g.first + g.count - 1;
 #pragma unroll 1
-  while (p + 1 < g.first + g.count && tn >= P.probs[p + 1].tn0) ++p;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.probs[mid].tn0 <= tn) lo = mid;
+    else hi = mid - 1;
+  }
+  const int p = lo;
   TileCoord c;
   c.p = p;
   c.tm = first_m + r % gm;
@@ -177,12 +185,13 @@ __device__ __forceinline__ void load_row32_bf16(const void* base, int64_t ld, in
 
 // Asks L2 to fetch this thread's row of the auxiliary inputs an epilogue will read (the
 // saved pre-activations of a backward epilogue), so those loads hit L2 when the tile's
-// accumulator is ready.  One 128-byte line per 64 bf16 columns.
+// accumulator is ready.  One 128-byte line per 64 bf16 columns, over the BN / 2 columns of
+// this warp's half of the tile.
 __device__ __forceinline__ void prefetch_aux_row(const Problem& pr, int row, int n_base) {
-  if (pr.epi != EPI_GELU_BWD && pr.epi != EPI_SWIGLU_BWD) return;
+  if (pr.epi != EPI_GELU_BWD && pr.epi != EPI_SWIGLU_BWD && pr.epi != EPI_SMAX_BWD) return;
   if (row >= pr.M) return;
 #pragma unroll
-  for (int c = 0; c < BN; c += 64) {
+  for (int c = 0; c < BN / 2; c += 64) {
     if (n_base + c >= pr.N) break;
     const int64_t off = static_cast<int64_t>(row) * pr.ld_aux + n_base + c;
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const __nv_bfloat16*>(pr.aux0) + off));
@@ -191,15 +200,146 @@ __device__ __forceinline__ void prefetch_aux_row(const Problem& pr, int row, int
   }
 }
 
+// Per-row state an epilogue carries across the chunks of one tile.
+struct EpiState {
+  float m = -INFINITY, s = 0.0f;   // EPI_F32_CE / EPI_SMAX_STATS: running max and sum
+  int64_t ce_tgt = -1;             // EPI_F32_CE: target column relative to the tile's first
+  float a = 0.0f, b = 0.0f;        // EPI_SMAX_P: row max and 1 / sum; EPI_SMAX_BWD: rowsum(dO O)
+};
+
+// The epilogue of one 32-column chunk (chunk `ch` of the tile starting at column n_base) of
+// this thread's row; r holds the fp32 accumulator bits.
+__device__ __forceinline__ void epilogue_chunk(const Problem& pr, int row, int n_base, int ch,
+                                               const uint32_t (&r)[32], EpiState& st) {
+  const int col0 = n_base + ch * 32;
+  if (col0 >= pr.N) return;
+  const int epi = pr.epi;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  if (epi == EPI_SMAX_STATS || epi == EPI_SMAX_P || epi == EPI_SMAX_BWD) {
+    // causal: column j is valid for j <= row; the chunk is "full" when all 32 are valid
+    const int nv = min(pr.N - col0, row - col0 + 1);
+    const bool full = nv >= 32;
+    const float k = pr.fscale;
+    if (epi == EPI_SMAX_STATS) {
+      if (nv <= 0) return;
+      float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
+      if (full) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          x0 = fmaxf(x0, v[j]);
+          x1 = fmaxf(x1, v[j + 1]);
+          x2 = fmaxf(x2, v[j + 2]);
+          x3 = fmaxf(x3, v[j + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x0 = fmaxf(x0, j < nv ? v[j] : -INFINITY);
+      }
+      const float mnew = fmaxf(st.m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * k);   // k > 0
+      const float nm = -mnew;
+      float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+      if (full) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          s0 += ex2_approx(fmaf(v[j], k, nm));
+          s1 += ex2_approx(fmaf(v[j + 1], k, nm));
+          s2 += ex2_approx(fmaf(v[j + 2], k, nm));
+          s3 += ex2_approx(fmaf(v[j + 3], k, nm));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s0 += j < nv ? ex2_approx(fmaf(v[j], k, nm)) : 0.0f;
+      }
+      st.s = st.s * ex2_approx(st.m - mnew) + ((s0 + s1) + (s2 + s3));   // 2^-inf = 0 on the first chunk
+      st.m = mnew;
+    } else if (epi == EPI_SMAX_P) {
+      const float nm = -st.a;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p = ex2_approx(fmaf(v[j], k, nm)) * st.b;
+        v[j] = (full || j < nv) ? p : 0.0f;
+      }
+      store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+    } else {
+      float p[32];
+      load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, p);
+      const float D = st.a;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float ds = (v[j] - D) * (p[j] * k);
+        v[j] = (full || j < nv) ? ds : 0.0f;
+      }
+      store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+    }
+    return;
+  }
+  if (epi == EPI_F32) {
+    store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
+  } else if (epi == EPI_F32_CE) {
+    store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
+    const int nv = min(32, pr.N - col0);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) mx = fmaxf(mx, v[j]);
+    if (mx > st.m) {
+      st.s *= __expf(st.m - mx);
+      st.m = mx;
+    }
+    float se = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nv) se += __expf(v[j] - st.m);
+      if (st.ce_tgt == ch * 32 + j && j < nv) reinterpret_cast<float*>(pr.out2)[row] = v[j];
+    }
+    st.s += se;
+  } else if (epi == EPI_BF16 || epi == EPI_GELU_FWD) {
+    if (pr.bias0) {
+      float b[32];
+      load_row32_bf16(pr.bias0, 0, 0, col0, pr.N, b);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += b[j];
+    }
+    store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+    if (epi == EPI_GELU_FWD) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j]);
+      store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
+    }
+  } else if (epi == EPI_GELU_BWD) {
+    float x[32];
+    load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, x);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(x[j]);
+    store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+  } else if (epi == EPI_SWIGLU_BWD) {
+    float gg[32], vv[32], dg[32];
+    load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, gg);
+    load_row32_bf16(pr.aux1, pr.ld_aux, row, col0, pr.N, vv);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float sg = sigmoid_f(gg[j]);
+      dg[j] = v[j] * vv[j] * sg * (1.0f + gg[j] * (1.0f - sg));
+      v[j] = v[j] * gg[j] * sg;
+    }
+    store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, dg);
+    store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
+  }
+}
+
 // Applies the problem's epilogue to one accumulator tile slice held in this CTA's TMEM
-// (128 rows; this thread owns one row) and stores it.
+// (128 rows; this thread owns one row) and stores it.  Two warps share each TMEM lane
+// quadrant: `half` selects the accumulator columns [half BN/2, (half + 1) BN/2) (a paired
+// tile: output columns [half BN/4, (half + 1) BN/4) of both halves).
 __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase, int row, int n_base_paired,
-                                              int n_base) {
+                                              int n_base, int half) {
   const bool row_ok = row < pr.M;
   const int epi = pr.epi;
   if (pr.paired) {
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 2 / 32; ++ch) {
+    for (int ch = half * (BN / 4 / 32); ch < (half + 1) * (BN / 4 / 32); ++ch) {
       uint32_t g[32], u[32];
       __syncwarp();
       tmem_ld_32x32b_x32(tbase + ch * 32, g);
@@ -221,80 +361,37 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
     }
     return;
   }
-  // EPI_F32_CE state: this row's running max and sum of exponentials over the tile, and the
-  // target's column relative to this tile's first column.
-  float ce_m = -INFINITY, ce_s = 0.0f;
-  int64_t ce_tgt = -1;
-  if (epi == EPI_F32_CE && row_ok) ce_tgt = reinterpret_cast<const int64_t*>(pr.aux0)[row] - pr.ext0 - n_base;
+  EpiState st;
+  if (epi == EPI_F32_CE && row_ok) st.ce_tgt = reinterpret_cast<const int64_t*>(pr.aux0)[row] - pr.ext0 - n_base;
+  if (row_ok && epi == EPI_SMAX_P) {
+    const float2 rs = reinterpret_cast<const float2*>(pr.aux0)[row];
+    st.a = rs.x;
+    st.b = rs.y;
+  } else if (row_ok && epi == EPI_SMAX_BWD) {
+    st.a = reinterpret_cast<const float*>(pr.aux1)[row];
+  }
+  // Two 32-column chunks per TMEM round trip: both loads are in flight before the one wait.
 #pragma unroll 1
-  for (int ch = 0; ch < BN / 32; ++ch) {
-    const int col0 = n_base + ch * 32;
-    if (col0 >= pr.N) break;   // the same for the whole warp: nothing left to store
-    uint32_t r[32];
+  for (int ch = half * (BN / 2 / 32); ch < (half + 1) * (BN / 2 / 32); ch += 2) {
+    if (n_base + ch * 32 >= pr.N) break;   // the same for the whole warp: nothing left to store
+    uint32_t r0[32], r1[32];
     __syncwarp();
-    tmem_ld_32x32b_x32(tbase + ch * 32, r);
+    tmem_ld_32x32b_x32(tbase + ch * 32, r0);
+    tmem_ld_32x32b_x32(tbase + ch * 32 + 32, r1);
     tmem_ld_wait();
-    if (row_ok && col0 < pr.N) {
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-      if (epi == EPI_F32) {
-        store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
-      } else if (epi == EPI_F32_CE) {
-        store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
-        const int nv = min(32, pr.N - col0);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nv) mx = fmaxf(mx, v[j]);
-        if (mx > ce_m) {
-          ce_s *= __expf(ce_m - mx);
-          ce_m = mx;
-        }
-        float se = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j < nv) se += __expf(v[j] - ce_m);
-          if (ce_tgt == ch * 32 + j && j < nv) reinterpret_cast<float*>(pr.out2)[row] = v[j];
-        }
-        ce_s += se;
-      } else if (epi == EPI_BF16 || epi == EPI_GELU_FWD) {
-        if (pr.bias0) {
-          float b[32];
-          load_row32_bf16(pr.bias0, 0, 0, col0, pr.N, b);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += b[j];
-        }
-        store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
-        if (epi == EPI_GELU_FWD) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j]);
-          store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
-        }
-      } else if (epi == EPI_GELU_BWD) {
-        float x[32];
-        load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, x);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(x[j]);
-        store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
-      } else if (epi == EPI_SWIGLU_BWD) {
-        float gg[32], vv[32], dg[32];
-        load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, gg);
-        load_row32_bf16(pr.aux1, pr.ld_aux, row, col0, pr.N, vv);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float s = sigmoid_f(gg[j]);
-          dg[j] = v[j] * vv[j] * s * (1.0f + gg[j] * (1.0f - s));
-          v[j] = v[j] * gg[j] * s;
-        }
-        store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, dg);
-        store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, v);
-      }
+    if (row_ok) {
+      epilogue_chunk(pr, row, n_base, ch, r0, st);
+      epilogue_chunk(pr, row, n_base, ch + 1, r1, st);
     }
   }
+  // One (max, sum) partial per row and half tile (BN / 2 columns): index 2 tile + half.
   if (epi == EPI_F32_CE && row_ok) {
     const int64_t gt = pr.tn0 + n_base / BN;   // this tile's index among the group's n-tiles
-    reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + gt] = make_float2(ce_m, ce_s);
+    reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + 2 * gt + half] = make_float2(st.m, st.s);
+  }
+  if (epi == EPI_SMAX_STATS && row_ok) {
+    reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + 2 * (n_base / BN) + half] =
+        make_float2(st.m, st.s);
   }
 }
 
@@ -329,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], PAIR ? 8 : 4);   // every epilogue warp of the pair arrives
+      mbar_init(&tempty_bar[a], PAIR ? 16 : 8);  // every epilogue warp of the pair arrives
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -363,8 +460,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
+      int gi = 0;
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
-        const TileCoord c = decode_tile(P, tile);
+        const TileCoord c = decode_tile(P, tile, gi);
         const Problem& pr = P.probs[c.p];
         if (tile_skipped<C::TILE_M>(pr, c)) continue;
         int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
@@ -470,8 +568,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       uint32_t acc_phase = 0;
       bool ok = true;
       const uint32_t sbase = smem_u32(smem);
+      int gi = 0;
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
-        const TileCoord c = decode_tile(P, tile);
+        const TileCoord c = decode_tile(P, tile, gi);
         const Problem& pr = P.probs[c.p];
         if (tile_skipped<C::TILE_M>(pr, c)) continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, status, tmo)) {
@@ -532,17 +631,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
   } else {
     // ---------------------------------------------------------------- epilogue warps
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;       // which half of the accumulator columns it stores
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint32_t tempty_leader0 = PAIR ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
     const int my_row0 = static_cast<int>(rank) * 128 + row_in_tile;
+    int gi = 0, gi_next = 0;
     if (unit < P.total_tiles) {
-      const TileCoord c0 = decode_tile(P, unit);
-      prefetch_aux_row(P.probs[c0.p], c0.tm * C::TILE_M + my_row0, c0.tn * BN);
+      const TileCoord c0 = decode_tile(P, unit, gi_next);
+      prefetch_aux_row(P.probs[c0.p], c0.tm * C::TILE_M + my_row0, c0.tn * BN + half * (BN / 2));
     }
     for (int tile = unit; tile < P.total_tiles; tile += nunits) {
-      const TileCoord c = decode_tile(P, tile);
+      const TileCoord c = decode_tile(P, tile, gi);
       const Problem& pr = P.probs[c.p];
       if (tile_skipped<C::TILE_M>(pr, c)) continue;
       const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
@@ -550,12 +651,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       tc_fence_after_sync();
       // The next tile's auxiliary rows travel to L2 while this tile's epilogue runs.
       if (tile + nunits < P.total_tiles) {
-        const TileCoord cn = decode_tile(P, tile + nunits);
-        prefetch_aux_row(P.probs[cn.p], cn.tm * C::TILE_M + my_row0, cn.tn * BN);
+        const TileCoord cn = decode_tile(P, tile + nunits, gi_next);
+        prefetch_aux_row(P.probs[cn.p], cn.tm * C::TILE_M + my_row0, cn.tn * BN + half * (BN / 2));
       }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const int row = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + row_in_tile;
-      epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN);
+      epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN, half);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -773,9 +874,10 @@ int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b
   bytes_ += 2.0 * (static_cast<double>(p->M) * K + ncols * K) * tri;
   if (p->nseg == 1) {
     const int nout = p->epi == EPI_SWIGLU_FWD ? 3 : (p->epi == EPI_GELU_FWD || p->epi == EPI_SWIGLU_BWD) ? 2 : 1;
-    const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : p->epi == EPI_GELU_BWD ? 1 : 0;
-    const double esz = (p->epi == EPI_F32 || p->epi == EPI_F32_CE) ? 4.0 : 2.0;
+    const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : (p->epi == EPI_GELU_BWD || p->epi == EPI_SMAX_BWD) ? 1 : 0;
+    const double esz = (p->epi == EPI_F32 || p->epi == EPI_F32_CE) ? 4.0 : p->epi == EPI_SMAX_STATS ? 0.0 : 2.0;
     bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux) * (p->causal == CAUSAL_SKIP_UPPER ? tri : 1.0);
+    if (p->epi == EPI_SMAX_STATS) bytes_ += 8.0 * p->M * ((p->N + BN - 1) / BN) * tri;   // the (max, sum) partials
   }
   return TTL_OK;
 }

@@ -64,6 +64,13 @@ enum Epilogue : int {
                        // partials: out1[row * ext1 + tn0 + tn] = (max, sum exp(z - max)) over
                        // the tile's columns; out2[row] = the logit at target aux0[row] - ext0
                        // when that column is in the tile
+  // Causal attention scores (rows = queries, columns = keys; column j valid for j <= row):
+  EPI_SMAX_STATS = 7,  // no store of the scores; out1[row * ext1 + tn] = (max, sum exp2(x - max)) of
+                       // x = acc * fscale over the tile's valid columns (fscale = log2(e) / sqrt(d))
+  EPI_SMAX_P = 8,      // out0 = bf16(exp2(acc * fscale - M) * R) with aux0[row] = float2 (M, R = 1 / sum),
+                       // zeros in the invalid columns
+  EPI_SMAX_BWD = 9,    // out0 = bf16(aux0 * (acc - aux1[row]) * fscale), aux0 = saved P (bf16, ld_aux),
+                       // aux1 = rowsum(dO O) (fp32), zeros in the invalid columns
 };
 
 // Causal structure of a problem whose rows or columns are token positions (attention).
@@ -107,7 +114,10 @@ struct Problem {
   const void* bias0;
   int64_t ld_out;         // row stride (elements) of out0/out1/out2
   int64_t ld_aux;         // row stride (elements) of aux0/aux1
-  int64_t ext0, ext1;     // epilogue-specific integers (EPI_F32_CE: vocab offset, row stride of out1)
+  int64_t ext0, ext1;     // epilogue-specific integers (EPI_F32_CE: vocab offset, row stride of out1;
+                          // EPI_SMAX_STATS: row stride of out1)
+  float fscale;           // epilogue-specific scale (EPI_SMAX_*)
+  int32_t pad2;
 };
 
 // Consecutive problems with the same M that read the same A rows form one tile group: its

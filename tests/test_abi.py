@@ -102,7 +102,7 @@ def test_gtp_and_ce_validation(lib):
                                      None, 0, 8, None) == 1
     # workspace too small for the fused statistics
     need = lib.ttl_vocab_parallel_ce_workspace_size(2, 8, 64, 32)
-    assert need == 256 + 8 * 4        # 8 tokens x 2 tiles x 8 bytes, rounded to 256, + 8 target logits
+    assert need == 256 + 8 * 4        # 8 tokens x 2 shards x 2 half tiles x 8 bytes, + 8 target logits
     assert lib.ttl_vocab_parallel_ce(2, 8, 64, 32, 0x90000, W, 0xA0000, L, L, 0xB0000, 0xC0000, 0xD0000,
                                      0xE0000, need - 1, 0, None) == 1
     # embedding: t does not divide V, misaligned ids
@@ -130,10 +130,12 @@ def test_attention_validation(lib):
     assert call(2, 64, 64, 8, 2, 128, arrs=[sh] * 9 + [None]) == 1   # Y missing
     assert call(2, 64, 64, 8, 2, 128, wb=16) == 1    # workspace too small
     assert call(2, 0, 64, 8, 2, 128) == 0            # no tokens: nothing to do
-    # fp32 scores, one [n_q/t, T, T] block per shard
-    assert lib.ttl_tp_attn_fwd_workspace_size(2, 64, 8, 2, 128) == 2 * 4 * 64 * 64 * 4
-    per = 4 * 64 * 64 * 4 + 4 * 64 * 64 * 2 + 2 * (64 * 512 * 2) + 2 * (64 * 128 * 2)
-    assert lib.ttl_tp_attn_bwd_workspace_size(2, 64, 8, 2, 128) == 2 * per
+    # (max, sum) partials per row and 128-key half tile, then (max, 1/sum) per row: 512 rows, 2 halves
+    assert lib.ttl_tp_attn_fwd_workspace_size(2, 64, 8, 2, 128) == 512 * 2 * 8 + 512 * 8
+    assert lib.ttl_tp_attn_fwd_workspace_size(1, 1000, 2, 1, 64) == 2000 * 8 * 8 + 16128   # 16000 rounded up to 256
+    # D per row (fp32), then per shard dS [4, 64, 64] bf16, dO, dQ [64, 512], dK, dV [64, 128]
+    per = 4 * 64 * 64 * 2 + 2 * (64 * 512 * 2) + 2 * (64 * 128 * 2)
+    assert lib.ttl_tp_attn_bwd_workspace_size(2, 64, 8, 2, 128) == 512 * 4 + 2 * per
     assert lib.ttl_tp_attn_bwd_workspace_size(3, 64, 8, 2, 128) == 0    # invalid shape
     bwd = lib.ttl_tp_attn_bwd
     assert bwd(2, 64, 64, 8, 2, 128, X, X, *([sh] * 9), sh, sh, sh, None, sh, ws, 1 << 40, None) == 1  # dWo missing
