@@ -659,9 +659,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN, half);
       tc_fence_before_sync();
       __syncwarp();
+      // This warp's accumulator reads are complete (tcgen05.wait::ld in the epilogue): the
+      // MMA may overwrite the buffer.  Relaxed: the tile's global stores need not drain first.
       if (lane == 0) {
-        if (PAIR) mbar_arrive_cluster(tempty_leader0 + acc * 8u);
-        else mbar_arrive(&tempty_bar[acc]);
+        if (PAIR) mbar_arrive_cluster_relaxed(tempty_leader0 + acc * 8u);
+        else mbar_arrive_relaxed(&tempty_bar[acc]);
       }
       if (++acc == 2) {
         acc = 0;

@@ -190,9 +190,17 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on an mbarrier given by its cluster-window address (possibly in the peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Relaxed arrives (the second on an mbarrier given by its cluster-window address, possibly in
+// the peer CTA): no ordering of this thread's earlier memory writes (which a release arrive
+// would first wait to complete).  For barriers that only say "my tcgen05.ld of the accumulator
+// has completed" (after tcgen05.wait::ld): the global stores of the tile need no ordering
+// against the MMA that next overwrites the accumulator.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is counted on an mbarrier that may
