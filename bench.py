@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--only", choices=["sp_mlp", "shard_reduce", "gtp_chain", "vocab_ce", "vocab_embedding",
                                        "tp_attention"],
                     help="run just one secondary component (for profiling); prints its JSON object")
+    ap.add_argument("--attn-small", action="store_true",
+                    help="tp_attention at the profiling size: T=4096, h=4096, 8 query / 2 KV heads of 128, t=2")
     return ap.parse_args()
 
 
@@ -574,8 +576,9 @@ def bench_embedding(ttl, torch, dev, pk, args):
 
 def bench_attention(ttl, torch, dev, pk, args):
     """Head-split TP attention block forward + backward at the Qwen3-8B shape: T=8192 tokens,
-    h=4096, 32 query / 8 KV heads of 128, t=8 (4 query heads + 1 KV head per shard)."""
-    t, T, h, n_q, n_kv, d = 8, 8192, 4096, 32, 8, 128
+    h=4096, 32 query / 8 KV heads of 128, t=8 (4 query heads + 1 KV head per shard); with
+    --attn-small the profiling case T=4096, 8 query / 2 KV heads, t=2."""
+    t, T, h, n_q, n_kv, d = (2, 4096, 4096, 8, 2, 128) if args.attn_small else (8, 8192, 4096, 32, 8, 128)
     qc, kc = n_q // t * d, n_kv // t * d
     g = torch.Generator(device=dev).manual_seed(7)
 
@@ -613,7 +616,8 @@ def bench_attention(ttl, torch, dev, pk, args):
     gm = [r for r in recs if r[0] == "gemm"]
     sm = [r for r in recs if r[0] == "softmax"]
     sm_gbs = sum(r[3] for r in sm) / (sum(r[1] for r in sm) * 1e-3) / 1e9
-    res = {"workload": "qwen3_8b_attention_t8_T8192_h4096_q32_kv8_d128_fwd_bwd", "ms_per_step": round(ms, 4),
+    name = f"attention_t{t}_T{T}_h{h}_q{n_q}_kv{n_kv}_d{d}_fwd_bwd"
+    res = {"workload": ("qwen3_8b_" if not args.attn_small else "") + name, "ms_per_step": round(ms, 4),
            "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "flops_per_step": flops,
            "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
            "frac_of_sustained_bf16": round(flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4),

@@ -49,7 +49,7 @@ struct TraceScope {
 // ------------------------------------------------------------------ GEMM problem block
 
 constexpr int kGemmBN = 256;   // accumulator columns per GEMM tile
-constexpr int kMaxMaps = 64;
+constexpr int kMaxMaps = 96;
 constexpr int kMaxProblems = 32;
 constexpr int kMaxSegs = kMaxShards;
 
@@ -60,13 +60,14 @@ enum Epilogue : int {
   EPI_SWIGLU_FWD = 3,  // paired tile: out0 = G, out1 = V, out2 = SiLU(G) * V
   EPI_GELU_BWD = 4,    // out0 = bf16(acc * GeLU'(aux0))                          (dU)
   EPI_SWIGLU_BWD = 5,  // out0 = bf16(acc * aux1 * SiLU'(aux0)), out1 = bf16(acc * SiLU(aux0))
-  EPI_F32_CE = 6,      // out0 = acc (fp32 logits) and, per row and tile, the cross-entropy
-                       // partials: out1[row * ext1 + tn0 + tn] = (max, sum exp(z - max)) over
-                       // the tile's columns; out2[row] = the logit at target aux0[row] - ext0
-                       // when that column is in the tile
+  EPI_F32_CE = 6,      // out0 = acc (fp32 logits) and, per row and half tile (BN / 2 columns),
+                       // the cross-entropy partials: out1[row * ext1 + 2 (tn0 + tn) + half] =
+                       // (max, sum exp(z - max)) over those columns; out2[row] = the logit at
+                       // target aux0[row] - ext0 when that column is in the tile
   // Causal attention scores (rows = queries, columns = keys; column j valid for j <= row):
-  EPI_SMAX_STATS = 7,  // no store of the scores; out1[row * ext1 + tn] = (max, sum exp2(x - max)) of
-                       // x = acc * fscale over the tile's valid columns (fscale = log2(e) / sqrt(d))
+  EPI_SMAX_STATS = 7,  // no store of the scores; out1[row * ext1 + 2 tn + half] = (max, sum exp2(x -
+                       // max)) of x = acc * fscale over the half tile's valid columns
+                       // (fscale = log2(e) / sqrt(d)); (-inf, 0) when none is valid
   EPI_SMAX_P = 8,      // out0 = bf16(exp2(acc * fscale - M) * R) with aux0[row] = float2 (M, R = 1 / sum),
                        // zeros in the invalid columns
   EPI_SMAX_BWD = 9,    // out0 = bf16(aux0 * (acc - aux1[row]) * fscale), aux0 = saved P (bf16, ld_aux),
