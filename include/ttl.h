@@ -327,11 +327,11 @@ int ttl_vocab_parallel_embedding_bwd(int t, int64_t T, int64_t h, int64_t V, con
  *   P_save[i] [n_q/t, T, T] out: the probabilities, head-major; row q is written for keys
  *             j < min(T, round_up(q+1, 256)) (zeros above the diagonal), the rest is untouched
  *   Y[i] [T,h] out: partial O_i Wo_i, then the all-reduced block output in every buffer
- *   ws   workspace of ttl_tp_attn_fwd_workspace_size() bytes: the softmax row statistics
- *        (a (max, sum) pair per query row and 256-key tile, then (max, 1/sum) per row); the
- *        scores themselves never reach memory (the score GEMM runs twice, its epilogues
- *        computing the statistics, then the probabilities)
- * t | n_q, t | n_kv, n_kv | n_q, d a multiple of 64, T and h multiples of 8.  Errors:
+ *   ws   unused: ttl_tp_attn_fwd_workspace_size() returns 0 and ws may be null.  The scores
+ *        and the softmax statistics stay on chip: one fused kernel per 128-query tile computes
+ *        the scores twice in tensor memory (exact row statistics, then the probabilities, which
+ *        feed P V straight from shared memory)
+ * t | n_q, t | n_kv, n_kv | n_q, d = 64 or 128, T and h multiples of 8.  Errors:
  * TTL_ERR_ARG (null or short arguments), TTL_ERR_SHAPE, TTL_ERR_ALIGN (pointers not 16-byte
  * aligned); nothing is launched when the call returns an error. */
 size_t ttl_tp_attn_fwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d);

@@ -8,25 +8,21 @@
 // shape.  The pages do not spell out the attention itself; this file computes causal scaled
 // dot-product attention with scale 1/sqrt(d), query head j reading KV head j / (n_q / n_kv).
 //
-// Every contraction runs in the tcgen05 GEMM; the causal structure is handled there (score
-// tiles above the diagonal are skipped, P V and dS K stop their K loop at the tile's last
-// query, dS^T Q and P^T dO start theirs at the tile's first key).  The softmax lives in the
-// score GEMMs' epilogues, so no fp32 score matrix reaches HBM:
-//   forward : QKV (3t problems) -> S = Q_c K_g^T, epilogue: per row and 256-key tile the max and
-//             sum of exp2 of the scaled scores -> combine per row into (max, 1 / sum)
-//             -> S again, epilogue: P = exp2(S log2(e) / sqrt(d) - max) / sum as bf16
-//             -> O_c = P_c V_g -> partial Y_i = O_i Wo_i -> all-reduce
+// The projections, W_O and every backward contraction run in the tcgen05 GEMM, whose causal
+// modes handle the triangle (score tiles above the diagonal are skipped, dS K stops its K loop
+// at the tile's last query, dS^T Q and P^T dO start theirs at the tile's first key).  The
+// forward core (scores, softmax, P V) is one fused kernel (attention_core.cu); the backward's
+// softmax lives in the dP GEMM's epilogue:
+//   forward : QKV (3t problems) -> fused core: S = Q_c K_g^T in TMEM, exact row statistics,
+//             P = softmax(S / sqrt(d)) (bf16, saved), O_c = P_c V_g -> Y_i = O_i Wo_i -> all-reduce
 //   backward: {dO_i = dY Wo_i^T, dWo_i = O_i^T dY} -> D = rowsum(dO_c O_c)
 //             -> dP = dO_c V_g^T, epilogue: dS = P (dP - D) / sqrt(d) as bf16
 //             -> {dQ_c = dS_c K_g, dK_g = sum_c dS_c^T Q_c, dV_g = sum_c P_c^T dO_c}
 //             -> {dW_i = X^T d{Q,K,V}_i, dX_i = dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T} -> all-reduce
-// The score GEMM runs twice in the forward (its K is only d): recomputing it costs less than
-// writing and re-reading T^2/2 fp32 scores per head.
 //
-// Zero fill: row q of P and of dS is written for every key j < min(T, round_up(q + 1, 256)),
-// the span of the score tiles that are not skipped with either tile height (128 or 256 rows);
+// Zero fill: row q of P and of dS is written for every key j < min(T, round_up(q + 1, 256));
 // the keys above the diagonal get exact zeros.  That covers every element the causal GEMMs
-// read, so no full-size mask pass is needed.
+// read with either tile height (128 or 256 rows), so no full-size mask pass is needed.
 
 #include <cmath>
 
@@ -49,40 +45,6 @@ struct AttnRows {
 __device__ __forceinline__ void unpack8_bf16(uint4 w, float* v) {
   v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
   v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-}
-
-// Combines (max, sum) pairs: sum of both sides rescaled to the larger max; an empty side
-// (m = -inf) weighs nothing.
-__device__ __forceinline__ void combine(float& m, float& l, float m2, float l2) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) return;
-  l = (m == -INFINITY ? 0.0f : l * exp2f(m - M)) + (m2 == -INFINITY ? 0.0f : l2 * exp2f(m2 - M));
-  m = M;
-}
-
-// One warp per (shard, head, query) row q: folds the (max, sum) partials of the score tiles
-// that hold keys 0..q (half tiles of 128 keys 0..2 (q/256) + 1; a half with no key <= q holds
-// (-inf, 0)) into (max, 1 / sum), the row statistics of the probabilities.
-__global__ void __launch_bounds__(kRowWarps * 32) attn_row_stats_kernel(const float2* __restrict__ part,
-                                                                        float2* __restrict__ stats, int64_t rows,
-                                                                        int64_t T, int ntiles) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t q = row % T;
-  const int n = 2 * (static_cast<int>(q / kGemmBN) + 1);
-  float m = -INFINITY, l = 0.0f;
-  for (int k = lane; k < n; k += 32) {
-    const float2 p = part[row * ntiles + k];
-    combine(m, l, p.x, p.y);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
-    combine(m, l, m2, l2);
-  }
-  if (lane == 0) stats[row] = make_float2(m, 1.0f / l);
 }
 
 // One warp per (shard, head, query) row: D[q] = sum_k dO[q, k] O[q, k] over the head's d
@@ -126,7 +88,7 @@ int check_shape(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const cha
   if (n_q % t || n_kv % t)
     return set_error(TTL_ERR_SHAPE, "%s: t=%d must divide the head counts %d and %d", name, t, n_q, n_kv);
   if (n_q % n_kv) return set_error(TTL_ERR_SHAPE, "%s: n_kv=%d must divide n_q=%d", name, n_kv, n_q);
-  if (d % 64) return set_error(TTL_ERR_SHAPE, "%s: head dimension %d must be a multiple of 64", name, d);
+  if (d != 64 && d != 128) return set_error(TTL_ERR_SHAPE, "%s: head dimension %d is not 64 or 128", name, d);
   if (T % 8 || h % 8 || h == 0)
     return set_error(TTL_ERR_SHAPE, "%s: T and h must be multiples of 8 (16-byte rows), h > 0", name);
   if (T >= (int64_t(1) << 28) || h >= (int64_t(1) << 31) || static_cast<int64_t>(n_q / t) * T >= (int64_t(1) << 31))
@@ -165,16 +127,6 @@ int head_block_map(GemmBatch& b, const __nv_bfloat16* base, const Shape& s, int6
 
 const __nv_bfloat16* bf(const ttl_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
 
-// (max, sum) partials per query row: one per half score tile (kGemmBN / 2 keys).
-int64_t key_tiles(const Shape& s) { return 2 * ((s.T + kGemmBN - 1) / kGemmBN); }
-
-// Forward workspace: the (max, sum) partials [t n_q/t T, key half tiles] and the row statistics
-// [t n_q/t T] (float2 each), rows ordered (shard, head, query).
-size_t fwd_part_bytes(const Shape& s) {
-  return round256(static_cast<size_t>(s.t * s.nql * s.T) * static_cast<size_t>(key_tiles(s)) * 8);
-}
-size_t fwd_ws_bytes(const Shape& s) { return fwd_part_bytes(s) + round256(static_cast<size_t>(s.t * s.nql * s.T) * 8); }
-
 // Backward workspace: D = rowsum(dO O) [t n_q/t T] fp32, then per shard dS (bf16 [n_q/t, T, T]),
 // dO, dQ ([T, n_q/t d]), dK, dV ([T, n_kv/t d]).
 size_t bwd_d_bytes(const Shape& s) { return round256(static_cast<size_t>(s.t * s.nql * s.T) * 4); }
@@ -191,7 +143,7 @@ using namespace ttl;
 extern "C" size_t ttl_tp_attn_fwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d) {
   Shape s;
   if (check_shape(t, T, 8, n_q, n_kv, d, "ttl_tp_attn_fwd_workspace_size", &s)) return 0;
-  return fwd_ws_bytes(s);
+  return 0;   // the fused forward core keeps its scores and statistics on chip
 }
 
 extern "C" size_t ttl_tp_attn_bwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d) {
@@ -221,18 +173,10 @@ extern "C" int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
       {reinterpret_cast<CP>(O_save), "O_save"}, {reinterpret_cast<CP>(Y), "Y"}};
   for (const auto& a : arrs)
     if ((rc = check_ptrs(a.p, t, a.n))) return rc;
-  const size_t need = ttl_tp_attn_fwd_workspace_size(t, T, n_q, n_kv, d);
-  if (!ws || ws_bytes < need)
-    return set_error(TTL_ERR_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
-  if (!aligned16(ws)) return set_error(TTL_ERR_ALIGN, "%s: workspace not 16-byte aligned", name);
+  (void)ws;
+  (void)ws_bytes;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t nt = key_tiles(s);
-  const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
-  float2* part = static_cast<float2*>(ws);
-  float2* stats = reinterpret_cast<float2*>(static_cast<char*>(ws) + fwd_part_bytes(s));
-  auto head_row0 = [&](int i, int64_t c) { return (static_cast<int64_t>(i) * s.nql + c) * T; };
-  const float k_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   GemmBatch batch;
 
   // Column-parallel projections: Q_i, K_i, V_i = X W{q,k,v}_i, one tile group over X.
@@ -253,55 +197,15 @@ extern "C" int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
   }
   if ((rc = batch.flush(st))) return rc;
 
-  // Scores S_c = Q_c K_g^T twice (tiles above the diagonal skipped): first for the per-tile
-  // row statistics, then, with the combined statistics, for the probabilities themselves.
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass == 1) {
-      TraceScope tr(st, TTL_K_SOFTMAX, 0.0, static_cast<double>(rows) * (nt / 2.0 + 1.0) * 8.0 + rows * 8.0);
-      attn_row_stats_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
-          part, stats, rows, T, static_cast<int>(nt));
-      if ((rc = cuda_check(cudaGetLastError(), "attn_row_stats_kernel launch"))) return rc;
-    }
-    for (int i = 0; i < t; ++i) {
-      for (int64_t c = 0; c < s.nql; ++c) {
-        if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
-        const int mq = batch.add_map(Q_save[i], T, s.qc, s.qc, false);
-        const int mk = batch.add_map(K_save[i], T, s.kc, s.kc, false);
-        Problem* p = batch.add_problem(T, T, false, false, pass == 0 ? EPI_SMAX_STATS : EPI_SMAX_P, false);
-        if (batch.error()) return batch.error();
-        p->causal = CAUSAL_SKIP_UPPER;
-        p->fscale = k_log2;
-        if (pass == 0) {
-          p->out1 = part + head_row0(i, c) * nt;
-          p->ext1 = nt;
-        } else {
-          p->out0 = P_save[i] + c * T * T;
-          p->ld_out = T;
-          p->aux0 = stats + head_row0(i, c);
-        }
-        if ((rc = batch.add_seg(p, mq, c * d, mk, -1, (c / s.grp) * d, d))) return rc;
-      }
-    }
-    if ((rc = batch.flush(st))) return rc;
+  // The fused core: scores, softmax and P V for every (shard, head, 128-query tile).
+  {
+    using CP = const void* const*;
+    using VP = void* const*;
+    if ((rc = attn_fwd_core(t, T, static_cast<int>(s.nql), static_cast<int>(s.grp), d, reinterpret_cast<CP>(Q_save),
+                            reinterpret_cast<CP>(K_save), reinterpret_cast<CP>(V_save), reinterpret_cast<VP>(P_save),
+                            reinterpret_cast<VP>(O_save), s.qc, s.kc, st)))
+      return rc;
   }
-
-  // O_c = P_c V_g into head c's columns of O_i; the K loop stops at the tile's last query.
-  for (int i = 0; i < t; ++i) {
-    for (int64_t c = 0; c < s.nql; ++c) {
-      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
-      const int mp = batch.add_map(P_save[i], s.nql * T, T, T, false);
-      const int mv = batch.add_map(V_save[i], T, s.kc, s.kc, true);
-      Problem* p = batch.add_problem(T, d, false, true, EPI_BF16, false);
-      if (batch.error()) return batch.error();
-      p->causal = CAUSAL_K_UPTO_ROW;
-      p->a_m0 = static_cast<int32_t>(c * T);
-      p->b_n0 = static_cast<int32_t>((c / s.grp) * d);
-      p->out0 = O_save[i] + c * d;
-      p->ld_out = s.qc;
-      if ((rc = batch.add_seg(p, mp, 0, mv, -1, 0, T))) return rc;
-    }
-  }
-  if ((rc = batch.flush(st))) return rc;
 
   // Row-parallel W_O: the full-shape partial Y_i = O_i Wo_i.
   for (int i = 0; i < t; ++i) {

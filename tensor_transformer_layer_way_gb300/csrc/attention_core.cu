@@ -1,0 +1,483 @@
+// The forward core of the head-split attention block in one kernel: for every (shard, query
+// head, 128-query tile) one CTA computes the causal softmax probabilities P of its rows and
+// O = P V, with the scores held in tensor memory and never written to HBM.
+//
+// Source: "v4:Tensor Parallel 与 Sequence Parallel", section "Attention:按 head 切" (each card
+// computes its heads' attention alone).  The attention itself is causal scaled dot-product
+// attention, scale 1/sqrt(d), query head j reading KV head j / (n_q / n_kv).
+//
+// Two passes over the key tiles 0..qt of query tile qt (128 keys each):
+//   pass 1: S = Q K^T (tcgen05, fp32 in TMEM); per row the max and the sum of 2^(s log2e/sqrt(d) - max)
+//           over the keys <= the query -- exact row statistics, so P needs no later rescaling;
+//   pass 2: S again; P = 2^(s log2e/sqrt(d) - M) / sum as bf16, written to shared memory (the A
+//           operand of the next MMA) and to HBM (saved for the backward); O += P V in TMEM.
+// The probabilities the backward reads are therefore written once; nothing re-reads them here.
+//
+// Roles (320 threads): warp 0 issues TMA loads (Q once; then K_0..K_n-1 for pass 1 and K_0, V_0,
+// K_1, V_1, ... for pass 2 through a 3-slot ring), warp 1 issues the MMAs, warps 2..9 run the
+// softmax: two warps per TMEM lane quadrant, each on 64 of a tile's 128 keys (and, at the end,
+// half of O's d columns).  The MMA warp issues S_j before P_(j-1) V_(j-1), so the softmax of
+// tile j overlaps the previous tile's P V.  Every wait is bounded (TTL_ERR_TIMEOUT on expiry).
+//
+// Layouts: Q, K tiles K-major (d contiguous, 64-column 128-byte-swizzled boxes of 128 rows);
+// V tiles MN-major (64 d x 64 keys boxes); P tiles K-major like Q; TMEM columns [0,128) and
+// [128,256) are the two score buffers, [256, 256 + d) the O accumulator.
+
+#include <cmath>
+#include <cstring>
+
+#include "ttl_device.cuh"
+#include "ttl_internal.h"
+
+namespace ttl {
+namespace {
+
+constexpr int kBQ = 128;            // queries per CTA
+constexpr int kBKV = 128;           // keys per tile
+constexpr int kRing = 3;            // K / V slots
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+
+struct CoreParams {
+  CUtensorMap q[kMaxShards];   // Q_i [T, n_q/t d], box 64 x 128
+  CUtensorMap k[kMaxShards];   // K_i [T, n_kv/t d], box 64 x 128
+  CUtensorMap v[kMaxShards];   // V_i [T, n_kv/t d], box 64 x 64 (MN-major B operand)
+  __nv_bfloat16* P[kMaxShards];   // [n_q/t, T, T]
+  __nv_bfloat16* O[kMaxShards];   // [T, n_q/t d]
+  int t, nql, grp, T, ntq;         // ntq = query tiles per head
+  float k_log2;                    // log2(e) / sqrt(d)
+  int* status;
+  uint64_t timeout_ns;
+};
+
+template <int D>
+struct CoreCfg {
+  static constexpr int KB = D / 64;                       // 64-wide d blocks
+  static constexpr int Q_BYTES = KB * kBQ * 128;          // 16 KiB per d block
+  static constexpr int SLOT = KB * kBKV * 128;            // a K tile or a V tile
+  static constexpr int P_BYTES = kBQ * kBKV * 2;          // 32 KiB
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_RING + kRing * SLOT;
+  static constexpr int OFF_XCH = OFF_P + 2 * P_BYTES;     // float2 [2][128] row-statistics exchange
+  static constexpr int OFF_BAR = OFF_XCH + 2 * kBQ * 8;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;       // barriers + alignment slack
+  static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid_constant__ CoreParams P) {
+  using C = CoreCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sRing = smem + C::OFF_RING;
+  uint8_t* sP = smem + C::OFF_P;
+  float2* xch = reinterpret_cast<float2*>(smem + C::OFF_XCH);
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* ring_full = q_full + 1;
+  uint64_t* ring_empty = ring_full + kRing;
+  uint64_t* s_full = ring_empty + kRing;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* p_empty = p_full + 2;
+  uint64_t* o_full = p_empty + 2;
+  uint64_t* done_bar = o_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // Heaviest query tiles first: block b takes tile ntq - 1 - b / (t n_q/t) of head b % (t n_q/t).
+  const int heads = P.t * P.nql;
+  const int qt = P.ntq - 1 - static_cast<int>(blockIdx.x) / heads;
+  const int hh = static_cast<int>(blockIdx.x) % heads;
+  const int shard = hh / P.nql;
+  const int c = hh % P.nql;                 // query head within the shard
+  const int g = c / P.grp;                  // its KV head within the shard
+  const int q0 = qt * kBQ;
+  const int ntiles = min(qt + 1, (P.T + kBKV - 1) / kBKV);   // key tiles 0..qt
+  int* status = P.status;
+  const uint64_t tmo = P.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], 8);   // every softmax warp
+      mbar_init(&p_full[b], 8);
+      mbar_init(&p_empty[b], 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&P.q[shard]);
+    tma_prefetch_map(&P.k[shard]);
+    tma_prefetch_map(&P.v[shard]);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(sQ + kb * 16384, &P.q[shard], q_full, c * D + kb * 64, q0);
+      // ring sequence: pass 1 K_0..K_{n-1}, pass 2 K_0, V_0, K_1, V_1, ...
+      const int nseq = 3 * ntiles;
+      int issued = 0;
+      for (int seq = 0; ok && seq < nseq; ++seq) {
+        const int slot = seq % kRing;
+        const uint32_t ph = static_cast<uint32_t>(seq / kRing) & 1u;
+        if (!mbar_wait(&ring_empty[slot], ph ^ 1u, abort_flag, status, tmo)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = sRing + slot * C::SLOT;
+        const bool is_v = seq >= ntiles && ((seq - ntiles) & 1);
+        const int j = seq < ntiles ? seq : (seq - ntiles) >> 1;
+        mbar_arrive_expect_tx(&ring_full[slot], C::SLOT);
+        if (!is_v) {
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(dst + kb * 16384, &P.k[shard], &ring_full[slot], g * D + kb * 64, j * kBKV);
+        } else {
+          // two 64-key blocks, each KB boxes of 64 d x 64 keys
+          for (int kk = 0; kk < 2; ++kk)
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(dst + (kk * C::KB + kb) * 8192, &P.v[shard], &ring_full[slot], g * D + kb * 64,
+                          j * kBKV + kk * 64);
+        }
+        ++issued;
+      }
+      // No copy may still be landing when the CTA leaves: wait (bounded) for the last loads.
+      int dummy_abort = 0;
+      mbar_wait(q_full, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+      const int pending = issued < kRing ? issued : kRing;
+      for (int i = issued - pending; i < issued; ++i)
+        mbar_wait(&ring_full[i % kRing], static_cast<uint32_t>(i / kRing) & 1u,
+                  reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, abort_flag, status, tmo);
+      tc_fence_after_sync();
+      const uint32_t qaddr = smem_u32(sQ);
+      const uint32_t ring0 = smem_u32(sRing);
+      const uint32_t paddr = smem_u32(sP);
+      const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKV, false, false);
+      const uint32_t idesc_o = idesc_bf16_f32(kBQ, D, false, true);
+      int seq = 0;           // ring position consumed next
+      int sj = 0;            // S tiles issued (both passes), selects the score buffer
+      auto issue_s = [&](int slot) {
+        const int b = sj & 1;
+        const uint32_t sph = static_cast<uint32_t>(sj >> 1) & 1u;
+        if (!mbar_wait(&s_empty[b], sph ^ 1u, abort_flag, status, tmo)) return false;
+        tc_fence_after_sync();
+        const uint32_t kaddr = ring0 + slot * C::SLOT;
+        for (int kb = 0; kb < C::KB; ++kb) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc_sw128(qaddr + kb * 16384 + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kaddr + kb * 16384 + kk * 32, 16, 1024);
+            umma_bf16(tmem_base + b * kBKV, ad, bd, idesc_s, (kb | kk) ? 1u : 0u);
+          }
+        }
+        umma_commit(&ring_empty[slot]);
+        umma_commit(&s_full[b]);
+        ++sj;
+        return true;
+      };
+      auto wait_slot = [&](int& slot) {
+        slot = seq % kRing;
+        const uint32_t ph = static_cast<uint32_t>(seq / kRing) & 1u;
+        ++seq;
+        if (!mbar_wait(&ring_full[slot], ph, abort_flag, status, tmo)) return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      // pass 1: scores only
+      for (int j = 0; ok && j < ntiles; ++j) {
+        int slot;
+        ok = wait_slot(slot) && issue_s(slot);
+      }
+      // pass 2: S_j, then P_{j-1} V_{j-1}
+      int vslot_prev = -1;
+      for (int j = 0; ok && j <= ntiles; ++j) {
+        int kslot = -1, vslot = -1;
+        if (j < ntiles) {
+          ok = wait_slot(kslot) && issue_s(kslot);
+          if (ok) ok = wait_slot(vslot);   // V_j arrives right after K_j in the ring
+        }
+        if (ok && j > 0) {
+          const int jp = j - 1;
+          const int b = jp & 1;
+          if (!mbar_wait(&p_full[b], static_cast<uint32_t>(jp >> 1) & 1u, abort_flag, status, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t vaddr = ring0 + vslot_prev * C::SLOT;
+          for (int kk2 = 0; kk2 < 2; ++kk2) {          // 64-key blocks
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kk2 * 16384 + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(vaddr + kk2 * C::KB * 8192 + kk * 2048, 8192, 1024);
+              umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_o, (jp | kk2 | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(&ring_empty[vslot_prev]);
+          umma_commit(&p_empty[b]);
+        }
+        vslot_prev = vslot;
+      }
+      if (ok) umma_commit(o_full);
+      // Every MMA issued here must finish before TMEM is released.
+      umma_commit(done_bar);
+      int dummy_abort = 0;
+      mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warps
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;          // keys [half 64, half 64 + 64) of each tile
+    const int r = quad * 32 + lane;            // row within the query tile
+    const int q = q0 + r;                      // query index
+    const bool row_ok = q < P.T;
+    const float k = P.k_log2;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    bool ok = true;
+    int sj = 0;
+    // pass 1: running max and sum over the keys <= q
+    float m = -INFINITY, l = 0.0f;
+    for (int j = 0; j < ntiles; ++j, ++sj) {
+      const int b = sj & 1;
+      ok = ok && mbar_wait(&s_full[b], static_cast<uint32_t>(sj >> 1) & 1u, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64, r0);
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64 + 32, r1);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[b]);
+      const int key0 = j * kBKV + half * 64;
+      const int nv = min(64, q - key0 + 1);    // valid keys of this row among the 64
+      if (nv > 0) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          mx = fmaxf(mx, e < nv ? __uint_as_float(r0[e]) : -INFINITY);
+          mx = fmaxf(mx, e + 32 < nv ? __uint_as_float(r1[e]) : -INFINITY);
+        }
+        const float mnew = fmaxf(m, mx * k);
+        const float nm = -mnew;
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          s0 += e < nv ? ex2_approx(fmaf(__uint_as_float(r0[e]), k, nm)) : 0.0f;
+          s1 += e + 32 < nv ? ex2_approx(fmaf(__uint_as_float(r1[e]), k, nm)) : 0.0f;
+        }
+        l = l * ex2_approx(m - mnew) + (s0 + s1);
+        m = mnew;
+      }
+    }
+    // combine the two halves of each row (every softmax warp reaches this barrier)
+    xch[half * kBQ + r] = make_float2(m, l);
+    named_bar_sync(1, 256);
+    {
+      const float2 o = xch[(1 - half) * kBQ + r];
+      const float M = fmaxf(m, o.x);
+      const float L = (m == -INFINITY ? 0.0f : l * ex2_approx(m - M)) + (o.x == -INFINITY ? 0.0f : o.y * ex2_approx(o.x - M));
+      m = M;
+      l = L;
+    }
+    const float nm = -m;
+    const float inv_l = 1.0f / l;
+    // pass 2: probabilities
+    __nv_bfloat16* Prow = P.P[shard] + (static_cast<int64_t>(c) * P.T + (row_ok ? q : 0)) * P.T;
+    for (int j = 0; ok && j < ntiles; ++j, ++sj) {
+      const int b = sj & 1;
+      ok = mbar_wait(&s_full[b], static_cast<uint32_t>(sj >> 1) & 1u, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64, r0);
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64 + 32, r1);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[b]);
+      const int key0 = j * kBKV + half * 64;
+      const int nv = q - key0 + 1;
+      uint4 w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float e8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int col = u * 8 + e;
+          const float s = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
+          e8[e] = col < nv ? ex2_approx(fmaf(s, k, nm)) * inv_l : 0.0f;
+        }
+        w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
+                          pack_bf16x2(e8[6], e8[7]));
+      }
+      // the P buffer is free once the P V that read it two tiles ago has completed
+      const int pb = j & 1;
+      ok = mbar_wait(&p_empty[pb], static_cast<uint32_t>((j >> 1) & 1) ^ 1u, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      uint8_t* box = sP + pb * C::P_BYTES + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(box + ((u ^ (r & 7)) << 4)) = w[u];
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[pb]);
+      if (row_ok) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (key0 + u * 8 < P.T) *reinterpret_cast<uint4*>(Prow + key0 + u * 8) = w[u];
+      }
+    }
+    // Keys up to the next multiple of 256 are written as zeros too (the backward's causal K
+    // loops read that far): for an even query tile, the key tile after the diagonal.
+    if (ok && row_ok && (qt & 1) == 0) {
+      const int key0 = (qt + 1) * kBKV + half * 64;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (key0 + u * 8 < P.T) *reinterpret_cast<uint4*>(Prow + key0 + u * 8) = make_uint4(0, 0, 0, 0);
+    }
+    // O = (sum_j P_j V_j): this warp stores its half of the d columns
+    if (ok) ok = mbar_wait(o_full, 0, abort_flag, status, tmo);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after_sync();
+      __nv_bfloat16* Orow = P.O[shard] + static_cast<int64_t>(row_ok ? q : 0) * (P.nql * D) + c * D + half * (D / 2);
+#pragma unroll
+      for (int cc = 0; cc < D / 2; cc += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(lane_base + 2 * kBKV + half * (D / 2) + cc, o);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(Orow + cc + u * 8) = make_uint4(
+                pack_bf16x2(__uint_as_float(o[u * 8 + 0]), __uint_as_float(o[u * 8 + 1])),
+                pack_bf16x2(__uint_as_float(o[u * 8 + 2]), __uint_as_float(o[u * 8 + 3])),
+                pack_bf16x2(__uint_as_float(o[u * 8 + 4]), __uint_as_float(o[u * 8 + 5])),
+                pack_bf16x2(__uint_as_float(o[u * 8 + 6]), __uint_as_float(o[u * 8 + 7])));
+        }
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* Q, const void* const* K,
+                  const void* const* V, void* const* Pout, void* const* Oout, int64_t qc, int64_t kc,
+                  cudaStream_t stream) {
+  if (d != 64 && d != 128) return set_error(TTL_ERR_SHAPE, "attention core: head dimension %d is not 64 or 128", d);
+  int rc = require_sm103();
+  if (rc) return rc;
+  CoreParams* p = new CoreParams;
+  std::memset(static_cast<void*>(p), 0, sizeof(CoreParams));
+  for (int i = 0; i < t && !rc; ++i) {
+    rc = encode_map_bf16(&p->q[i], Q[i], T, qc, qc, 64, 128);
+    if (!rc) rc = encode_map_bf16(&p->k[i], K[i], T, kc, kc, 64, 128);
+    if (!rc) rc = encode_map_bf16(&p->v[i], V[i], T, kc, kc, 64, 64);
+    p->P[i] = static_cast<__nv_bfloat16*>(Pout[i]);
+    p->O[i] = static_cast<__nv_bfloat16*>(Oout[i]);
+  }
+  if (rc) {
+    delete p;
+    return rc;
+  }
+  p->t = t;
+  p->nql = nql;
+  p->grp = grp;
+  p->T = static_cast<int>(T);
+  p->ntq = static_cast<int>((T + kBQ - 1) / kBQ);
+  p->k_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  p->status = device_status_ptr();
+  p->timeout_ns = 2000000000ull;
+  if (!p->status) {
+    delete p;
+    return TTL_ERR_CUDA;
+  }
+  const unsigned blocks = static_cast<unsigned>(t) * nql * p->ntq;
+  const double tri = static_cast<double>(T) * (T + 1) / 2.0;
+  // Algorithmic work: S = Q K^T and P V over the causal triangle (the second score pass is a
+  // recomputation and is not counted); bytes: Q, K, V read once, P and O written once.
+  TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
+                2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
+  if (d == 128) {
+    static bool attr = false;
+    if (!attr) {
+      if ((rc = cuda_check(cudaFuncSetAttribute(attn_fwd_core_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                CoreCfg<128>::SMEM),
+                           "cudaFuncSetAttribute(attn core)"))) {
+        delete p;
+        return rc;
+      }
+      attr = true;
+    }
+    attn_fwd_core_kernel<128><<<blocks, kThreads, CoreCfg<128>::SMEM, stream>>>(*p);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      if ((rc = cuda_check(cudaFuncSetAttribute(attn_fwd_core_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                CoreCfg<64>::SMEM),
+                           "cudaFuncSetAttribute(attn core)"))) {
+        delete p;
+        return rc;
+      }
+      attr = true;
+    }
+    attn_fwd_core_kernel<64><<<blocks, kThreads, CoreCfg<64>::SMEM, stream>>>(*p);
+  }
+  delete p;
+  return cuda_check(cudaGetLastError(), "attn_fwd_core_kernel launch");
+}
+
+}  // namespace ttl

@@ -202,9 +202,9 @@ __device__ __forceinline__ void prefetch_aux_row(const Problem& pr, int row, int
 
 // Per-row state an epilogue carries across the chunks of one tile.
 struct EpiState {
-  float m = -INFINITY, s = 0.0f;   // EPI_F32_CE / EPI_SMAX_STATS: running max and sum
+  float m = -INFINITY, s = 0.0f;   // EPI_F32_CE: running max and sum
   int64_t ce_tgt = -1;             // EPI_F32_CE: target column relative to the tile's first
-  float a = 0.0f, b = 0.0f;        // EPI_SMAX_P: row max and 1 / sum; EPI_SMAX_BWD: rowsum(dO O)
+  float a = 0.0f;                  // EPI_SMAX_BWD: rowsum(dO O)
 };
 
 // The epilogue of one 32-column chunk (chunk `ch` of the tile starting at column n_base) of
@@ -217,62 +217,20 @@ __device__ __forceinline__ void epilogue_chunk(const Problem& pr, int row, int n
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  if (epi == EPI_SMAX_STATS || epi == EPI_SMAX_P || epi == EPI_SMAX_BWD) {
+  if (epi == EPI_SMAX_BWD) {
     // causal: column j is valid for j <= row; the chunk is "full" when all 32 are valid
     const int nv = min(pr.N - col0, row - col0 + 1);
     const bool full = nv >= 32;
     const float k = pr.fscale;
-    if (epi == EPI_SMAX_STATS) {
-      if (nv <= 0) return;
-      float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
-      if (full) {
+    float p[32];
+    load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, p);
+    const float D = st.a;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          x0 = fmaxf(x0, v[j]);
-          x1 = fmaxf(x1, v[j + 1]);
-          x2 = fmaxf(x2, v[j + 2]);
-          x3 = fmaxf(x3, v[j + 3]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x0 = fmaxf(x0, j < nv ? v[j] : -INFINITY);
-      }
-      const float mnew = fmaxf(st.m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * k);   // k > 0
-      const float nm = -mnew;
-      float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-      if (full) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          s0 += ex2_approx(fmaf(v[j], k, nm));
-          s1 += ex2_approx(fmaf(v[j + 1], k, nm));
-          s2 += ex2_approx(fmaf(v[j + 2], k, nm));
-          s3 += ex2_approx(fmaf(v[j + 3], k, nm));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) s0 += j < nv ? ex2_approx(fmaf(v[j], k, nm)) : 0.0f;
-      }
-      st.s = st.s * ex2_approx(st.m - mnew) + ((s0 + s1) + (s2 + s3));   // 2^-inf = 0 on the first chunk
-      st.m = mnew;
-    } else if (epi == EPI_SMAX_P) {
-      const float nm = -st.a;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p = ex2_approx(fmaf(v[j], k, nm)) * st.b;
-        v[j] = (full || j < nv) ? p : 0.0f;
-      }
-      store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
-    } else {
-      float p[32];
-      load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, p);
-      const float D = st.a;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float ds = (v[j] - D) * (p[j] * k);
-        v[j] = (full || j < nv) ? ds : 0.0f;
-      }
-      store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
+    for (int j = 0; j < 32; ++j) {
+      const float ds = (v[j] - D) * (p[j] * k);
+      v[j] = (full || j < nv) ? ds : 0.0f;
     }
+    store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
     return;
   }
   if (epi == EPI_F32) {
@@ -363,13 +321,7 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
   }
   EpiState st;
   if (epi == EPI_F32_CE && row_ok) st.ce_tgt = reinterpret_cast<const int64_t*>(pr.aux0)[row] - pr.ext0 - n_base;
-  if (row_ok && epi == EPI_SMAX_P) {
-    const float2 rs = reinterpret_cast<const float2*>(pr.aux0)[row];
-    st.a = rs.x;
-    st.b = rs.y;
-  } else if (row_ok && epi == EPI_SMAX_BWD) {
-    st.a = reinterpret_cast<const float*>(pr.aux1)[row];
-  }
+  if (row_ok && epi == EPI_SMAX_BWD) st.a = reinterpret_cast<const float*>(pr.aux1)[row];
   // Two 32-column chunks per TMEM round trip: both loads are in flight before the one wait.
 #pragma unroll 1
   for (int ch = half * (BN / 2 / 32); ch < (half + 1) * (BN / 2 / 32); ch += 2) {
@@ -388,10 +340,6 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
   if (epi == EPI_F32_CE && row_ok) {
     const int64_t gt = pr.tn0 + n_base / BN;   // this tile's index among the group's n-tiles
     reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + 2 * gt + half] = make_float2(st.m, st.s);
-  }
-  if (epi == EPI_SMAX_STATS && row_ok) {
-    reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + 2 * (n_base / BN) + half] =
-        make_float2(st.m, st.s);
   }
 }
 
@@ -762,6 +710,23 @@ bool pair_allowed() {
 
 }  // namespace
 
+int encode_map_bf16(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                    int box_rows) {
+  if (!aligned16(ptr) || (ld * 2) % 16 != 0 || cols % 8 != 0 || rows <= 0 || cols <= 0)
+    return set_error(TTL_ERR_ALIGN, "tensor map %p: pointer, row stride (%lld) and width (%lld) must be 16-byte aligned",
+                     ptr, (long long)ld, (long long)cols);
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return set_error(TTL_ERR_CUDA, "cuTensorMapEncodeTiled not available from the CUDA driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return cu_check(enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                  "cuTensorMapEncodeTiled");
+}
+
 GemmBatch::GemmBatch() : p_(new GemmParams), nmaps_(0), err_(TTL_OK), flops_(0.0), bytes_(0.0) {
   std::memset(static_cast<void*>(p_), 0, sizeof(GemmParams));
 }
@@ -877,9 +842,8 @@ int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b
   if (p->nseg == 1) {
     const int nout = p->epi == EPI_SWIGLU_FWD ? 3 : (p->epi == EPI_GELU_FWD || p->epi == EPI_SWIGLU_BWD) ? 2 : 1;
     const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : (p->epi == EPI_GELU_BWD || p->epi == EPI_SMAX_BWD) ? 1 : 0;
-    const double esz = (p->epi == EPI_F32 || p->epi == EPI_F32_CE) ? 4.0 : p->epi == EPI_SMAX_STATS ? 0.0 : 2.0;
+    const double esz = (p->epi == EPI_F32 || p->epi == EPI_F32_CE) ? 4.0 : 2.0;
     bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux) * (p->causal == CAUSAL_SKIP_UPPER ? tri : 1.0);
-    if (p->epi == EPI_SMAX_STATS) bytes_ += 8.0 * p->M * ((p->N + BN - 1) / BN) * tri;   // the (max, sum) partials
   }
   return TTL_OK;
 }

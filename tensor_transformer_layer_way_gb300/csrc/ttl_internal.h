@@ -64,13 +64,8 @@ enum Epilogue : int {
                        // the cross-entropy partials: out1[row * ext1 + 2 (tn0 + tn) + half] =
                        // (max, sum exp(z - max)) over those columns; out2[row] = the logit at
                        // target aux0[row] - ext0 when that column is in the tile
-  // Causal attention scores (rows = queries, columns = keys; column j valid for j <= row):
-  EPI_SMAX_STATS = 7,  // no store of the scores; out1[row * ext1 + 2 tn + half] = (max, sum exp2(x -
-                       // max)) of x = acc * fscale over the half tile's valid columns
-                       // (fscale = log2(e) / sqrt(d)); (-inf, 0) when none is valid
-  EPI_SMAX_P = 8,      // out0 = bf16(exp2(acc * fscale - M) * R) with aux0[row] = float2 (M, R = 1 / sum),
-                       // zeros in the invalid columns
-  EPI_SMAX_BWD = 9,    // out0 = bf16(aux0 * (acc - aux1[row]) * fscale), aux0 = saved P (bf16, ld_aux),
+  // Causal attention score gradients (rows = queries, columns = keys; column j valid for j <= row):
+  EPI_SMAX_BWD = 7,    // out0 = bf16(aux0 * (acc - aux1[row]) * fscale), aux0 = saved P (bf16, ld_aux),
                        // aux1 = rowsum(dO O) (fp32), zeros in the invalid columns
 };
 
@@ -115,9 +110,8 @@ struct Problem {
   const void* bias0;
   int64_t ld_out;         // row stride (elements) of out0/out1/out2
   int64_t ld_aux;         // row stride (elements) of aux0/aux1
-  int64_t ext0, ext1;     // epilogue-specific integers (EPI_F32_CE: vocab offset, row stride of out1;
-                          // EPI_SMAX_STATS: row stride of out1)
-  float fscale;           // epilogue-specific scale (EPI_SMAX_*)
+  int64_t ext0, ext1;     // epilogue-specific integers (EPI_F32_CE: vocab offset, row stride of out1)
+  float fscale;           // epilogue-specific scale (EPI_SMAX_BWD: 1 / sqrt(d))
   int32_t pad2;
 };
 
@@ -188,6 +182,19 @@ class GemmBatch {
   double flops_;   // algorithmic FLOPs of the collected problems (2 M N K each)
   double bytes_;   // operand bytes read once + output bytes written once
 };
+
+// Encodes a 2-D tensor map of a row-major bf16 matrix [rows, cols] (row stride ld elements)
+// with a box of box_cols x box_rows elements and 128-byte swizzle.  TTL_OK or an error code.
+int encode_map_bf16(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                    int box_rows);
+
+// Forward core of the head-split attention block for t shards (one kernel launch): from Q_i
+// [T, qc], K_i and V_i [T, kc] (qc = nql d, kc = nql d / grp) writes the probabilities P_i
+// [nql, T, T] (rows up to key min(T, round_up(q + 1, 256)), zeros above the diagonal) and
+// O_i [T, qc].  d is 64 or 128.
+int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* Q, const void* const* K,
+                  const void* const* V, void* const* Pout, void* const* Oout, int64_t qc, int64_t kc,
+                  cudaStream_t stream);
 
 // Zero-fill helper (used where a contraction is empty).
 int fill_zero(void* ptr, size_t bytes, cudaStream_t stream);

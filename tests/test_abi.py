@@ -124,15 +124,14 @@ def test_attention_validation(lib):
     assert call(3, 64, 64, 32, 8, 128) == 2          # t does not divide the head counts
     assert call(2, 64, 64, 8, 3, 128) == 2           # t does not divide n_kv
     assert call(2, 64, 64, 6, 4, 128) == 2           # n_kv does not divide n_q
-    assert call(2, 64, 64, 8, 2, 96) == 2            # head dimension not a multiple of 64
+    assert call(2, 64, 64, 8, 2, 96) == 2            # head dimension not 64 or 128
+    assert call(2, 64, 64, 8, 2, 256) == 2
     assert call(2, 60, 64, 8, 2, 128) == 2           # T not a multiple of 8
     assert call(2, 64, 64, 8, 2, 128, x=X + 2) == 3  # misaligned X
     assert call(2, 64, 64, 8, 2, 128, arrs=[sh] * 9 + [None]) == 1   # Y missing
-    assert call(2, 64, 64, 8, 2, 128, wb=16) == 1    # workspace too small
     assert call(2, 0, 64, 8, 2, 128) == 0            # no tokens: nothing to do
-    # (max, sum) partials per row and 128-key half tile, then (max, 1/sum) per row: 512 rows, 2 halves
-    assert lib.ttl_tp_attn_fwd_workspace_size(2, 64, 8, 2, 128) == 512 * 2 * 8 + 512 * 8
-    assert lib.ttl_tp_attn_fwd_workspace_size(1, 1000, 2, 1, 64) == 2000 * 8 * 8 + 16128   # 16000 rounded up to 256
+    # the fused forward keeps scores and statistics on chip
+    assert lib.ttl_tp_attn_fwd_workspace_size(2, 64, 8, 2, 128) == 0
     # D per row (fp32), then per shard dS [4, 64, 64] bf16, dO, dQ [64, 512], dK, dV [64, 128]
     per = 4 * 64 * 64 * 2 + 2 * (64 * 512 * 2) + 2 * (64 * 128 * 2)
     assert lib.ttl_tp_attn_bwd_workspace_size(2, 64, 8, 2, 128) == 512 * 4 + 2 * per
