@@ -14,7 +14,7 @@
 // The probabilities the backward reads are therefore written once; nothing re-reads them here.
 //
 // Roles (320 threads): warp 0 issues TMA loads (Q once; then K_0..K_n-1 for pass 1 and K_0, V_0,
-// K_1, V_1, ... for pass 2 through a 3-slot ring), warp 1 issues the MMAs, warps 2..9 run the
+// K_1, V_1, ... for pass 2 through a 4-slot ring), warp 1 issues the MMAs, warps 2..9 run the
 // softmax: two warps per TMEM lane quadrant, each on 64 of a tile's 128 keys (and, at the end,
 // half of O's d columns).  The MMA warp issues S_j before P_(j-1) V_(j-1), so the softmax of
 // tile j overlaps the previous tile's P V.  Every wait is bounded (TTL_ERR_TIMEOUT on expiry).
@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kBQ = 128;            // queries per CTA
 constexpr int kBKV = 128;           // keys per tile
-constexpr int kRing = 3;            // K / V slots
+constexpr int kRing = 4;            // K / V slots
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 
@@ -42,7 +42,7 @@ struct CoreParams {
   CUtensorMap q[kMaxShards];   // Q_i [T, n_q/t d], box 64 x 128
   CUtensorMap k[kMaxShards];   // K_i [T, n_kv/t d], box 64 x 128
   CUtensorMap v[kMaxShards];   // V_i [T, n_kv/t d], box 64 x 64 (MN-major B operand)
-  __nv_bfloat16* P[kMaxShards];   // [n_q/t, T, T]
+  CUtensorMap pm[kMaxShards];  // P_i as [n_q/t][T][T], box 64 x 128 x 1 (TMA stores of P tiles)
   __nv_bfloat16* O[kMaxShards];   // [T, n_q/t d]
   int t, nql, grp, T, ntq;         // ntq = query tiles per head
   float k_log2;                    // log2(e) / sqrt(d)
@@ -59,8 +59,10 @@ struct CoreCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
   static constexpr int OFF_P = OFF_RING + kRing * SLOT;
-  static constexpr int OFF_XCH = OFF_P + 2 * P_BYTES;     // float2 [2][128] row-statistics exchange
-  static constexpr int OFF_BAR = OFF_XCH + 2 * kBQ * 8;
+  // float2 [2][128] row-statistics exchange between the two passes, in the P buffers (which
+  // pass 2 only writes after every softmax warp has read it)
+  static constexpr int OFF_XCH = OFF_P;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;       // barriers + alignment slack
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
 };
@@ -72,6 +74,25 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+
+// Bulk tensor store shared -> global of one box; completion tracked by bulk async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// All but the newest N committed store groups have finished reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// All committed store groups have completed.
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid_constant__ CoreParams P) {
@@ -104,7 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
   const int c = hh % P.nql;                 // query head within the shard
   const int g = c / P.grp;                  // its KV head within the shard
   const int q0 = qt * kBQ;
-  const int ntiles = min(qt + 1, (P.T + kBKV - 1) / kBKV);   // key tiles 0..qt
+  const int ntiles = qt + 1;   // key tiles 0..qt (qt * 128 < T)
+  // The keys up to the next multiple of 256 are written as zeros (the backward's causal K loops
+  // read that far): for an even query tile, one all-zero P tile after the diagonal.
+  const bool zero_tile = (qt & 1) == 0 && (qt + 1) * kBKV < P.T;
   int* status = P.status;
   const uint64_t tmo = P.timeout_ns;
 
@@ -118,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], 8);   // every softmax warp
       mbar_init(&p_full[b], 8);
-      mbar_init(&p_empty[b], 1);
+      mbar_init(&p_empty[b], 2);   // the P V MMAs and the TMA store of the tile have both read it
     }
     mbar_init(o_full, 1);
     mbar_init(done_bar, 1);
@@ -129,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
     tma_prefetch_map(&P.q[shard]);
     tma_prefetch_map(&P.k[shard]);
     tma_prefetch_map(&P.v[shard]);
+    tma_prefetch_map(&P.pm[shard]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -190,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       const uint32_t paddr = smem_u32(sP);
       const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKV, false, false);
       const uint32_t idesc_o = idesc_bf16_f32(kBQ, D, false, true);
-      int seq = 0;           // ring position consumed next
       int sj = 0;            // S tiles issued (both passes), selects the score buffer
       auto issue_s = [&](int slot) {
         const int b = sj & 1;
@@ -211,36 +235,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
         ++sj;
         return true;
       };
-      auto wait_slot = [&](int& slot) {
-        slot = seq % kRing;
-        const uint32_t ph = static_cast<uint32_t>(seq / kRing) & 1u;
-        ++seq;
-        if (!mbar_wait(&ring_full[slot], ph, abort_flag, status, tmo)) return false;
+      // Ring position pos (the producer's load order) lives in slot pos % kRing.
+      auto wait_pos = [&](int pos) {
+        const int slot = pos % kRing;
+        if (!mbar_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u, abort_flag, status, tmo))
+          return -1;
         tc_fence_after_sync();
-        return true;
+        return slot;
       };
-      // pass 1: scores only
+      // pass 1: scores only (K_j at position j)
       for (int j = 0; ok && j < ntiles; ++j) {
-        int slot;
-        ok = wait_slot(slot) && issue_s(slot);
+        const int slot = wait_pos(j);
+        ok = slot >= 0 && issue_s(slot);
       }
-      // pass 2: S_j, then P_{j-1} V_{j-1}
-      int vslot_prev = -1;
+      // pass 2: S_j (K_j at position n + 2j), then P_(j-1) V_(j-1) (V_(j-1) at n + 2j - 1): each V
+      // is waited for just before its own P V, two iterations after its load could start
       for (int j = 0; ok && j <= ntiles; ++j) {
-        int kslot = -1, vslot = -1;
         if (j < ntiles) {
-          ok = wait_slot(kslot) && issue_s(kslot);
-          if (ok) ok = wait_slot(vslot);   // V_j arrives right after K_j in the ring
+          const int kslot = wait_pos(ntiles + 2 * j);
+          ok = kslot >= 0 && issue_s(kslot);
         }
         if (ok && j > 0) {
           const int jp = j - 1;
           const int b = jp & 1;
-          if (!mbar_wait(&p_full[b], static_cast<uint32_t>(jp >> 1) & 1u, abort_flag, status, tmo)) {
+          const int vslot = wait_pos(ntiles + 2 * jp + 1);
+          if (vslot < 0 || !mbar_wait(&p_full[b], static_cast<uint32_t>(jp >> 1) & 1u, abort_flag, status, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t vaddr = ring0 + vslot_prev * C::SLOT;
+          // P_jp -> HBM: two 64-key boxes straight from the MMA's A operand tile
+          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, jp * kBKV, q0, c);
+          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, jp * kBKV + 64, q0, c);
+          bulk_commit_group();
+          const uint32_t vaddr = ring0 + vslot * C::SLOT;
           for (int kk2 = 0; kk2 < 2; ++kk2) {          // 64-key blocks
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -249,16 +277,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
               umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_o, (jp | kk2 | kk) ? 1u : 0u);
             }
           }
-          umma_commit(&ring_empty[vslot_prev]);
-          umma_commit(&p_empty[b]);
+          umma_commit(&ring_empty[vslot]);
+          umma_commit(&p_empty[b]);                  // first arrival: the MMAs have read P_jp
+          bulk_wait_group_read<1>();                 // the store of P_(jp-1) has read its buffer
+          if (jp > 0) mbar_arrive(&p_empty[(jp - 1) & 1]);
         }
-        vslot_prev = vslot;
+      }
+      bulk_wait_group_read<0>();
+      if (ntiles > 0) mbar_arrive(&p_empty[(ntiles - 1) & 1]);
+      if (ok && zero_tile) {
+        const int b = ntiles & 1;
+        if (mbar_wait(&p_full[b], static_cast<uint32_t>(ntiles >> 1) & 1u, abort_flag, status, tmo)) {
+          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, ntiles * kBKV, q0, c);
+          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, ntiles * kBKV + 64, q0, c);
+          bulk_commit_group();
+        }
       }
       if (ok) umma_commit(o_full);
-      // Every MMA issued here must finish before TMEM is released.
+      // Every MMA issued here must finish before TMEM is released, and every store before the
+      // CTA's shared memory goes away.
       umma_commit(done_bar);
       int dummy_abort = 0;
       mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+      bulk_wait_group_all();
     }
     __syncwarp();
   } else {
@@ -291,7 +332,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       if (lane == 0) mbar_arrive(&s_empty[b]);
       const int key0 = j * kBKV + half * 64;
       const int nv = min(64, q - key0 + 1);    // valid keys of this row among the 64
-      if (nv > 0) {
+      if (nv >= 64) {                          // below the diagonal: no mask
+        float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          x0 = fmaxf(x0, __uint_as_float(r0[e]));
+          x1 = fmaxf(x1, __uint_as_float(r0[e + 1]));
+          x2 = fmaxf(x2, __uint_as_float(r1[e]));
+          x3 = fmaxf(x3, __uint_as_float(r1[e + 1]));
+        }
+        const float mnew = fmaxf(m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * k);
+        const float nm = -mnew;
+        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          s0 += ex2_approx(fmaf(__uint_as_float(r0[e]), k, nm));
+          s1 += ex2_approx(fmaf(__uint_as_float(r0[e + 1]), k, nm));
+          s2 += ex2_approx(fmaf(__uint_as_float(r1[e]), k, nm));
+          s3 += ex2_approx(fmaf(__uint_as_float(r1[e + 1]), k, nm));
+        }
+        l = l * ex2_approx(m - mnew) + ((s0 + s1) + (s2 + s3));
+        m = mnew;
+      } else if (nv > 0) {
         float mx = -INFINITY;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -320,10 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       m = M;
       l = L;
     }
+    named_bar_sync(1, 256);   // every half has read the exchange before P overwrites it
     const float nm = -m;
     const float inv_l = 1.0f / l;
-    // pass 2: probabilities
-    __nv_bfloat16* Prow = P.P[shard] + (static_cast<int64_t>(c) * P.T + (row_ok ? q : 0)) * P.T;
+    // pass 2: probabilities, into the P buffer the MMA warp feeds to P V and stores to HBM
+    uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
     for (int j = 0; ok && j < ntiles; ++j, ++sj) {
       const int b = sj & 1;
       ok = mbar_wait(&s_full[b], static_cast<uint32_t>(sj >> 1) & 1u, abort_flag, status, tmo);
@@ -339,47 +402,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);
-      const int key0 = j * kBKV + half * 64;
-      const int nv = q - key0 + 1;
+      const int nv = q - (j * kBKV + half * 64) + 1;
       uint4 w[8];
+      if (nv >= 64) {   // below the diagonal: no mask
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float e8[8];
+        for (int u = 0; u < 8; ++u) {
+          float e8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int col = u * 8 + e;
-          const float s = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
-          e8[e] = col < nv ? ex2_approx(fmaf(s, k, nm)) * inv_l : 0.0f;
+          for (int e = 0; e < 8; ++e) {
+            const int col = u * 8 + e;
+            e8[e] = ex2_approx(fmaf(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]), k, nm)) * inv_l;
+          }
+          w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
+                            pack_bf16x2(e8[6], e8[7]));
         }
-        w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
-                          pack_bf16x2(e8[6], e8[7]));
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float e8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int col = u * 8 + e;
+            const float s = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
+            e8[e] = col < nv ? ex2_approx(fmaf(s, k, nm)) * inv_l : 0.0f;
+          }
+          w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
+                            pack_bf16x2(e8[6], e8[7]));
+        }
       }
-      // the P buffer is free once the P V that read it two tiles ago has completed
+      // the P buffer is free once the P V and the store that read it two tiles ago are done
       const int pb = j & 1;
       ok = mbar_wait(&p_empty[pb], static_cast<uint32_t>((j >> 1) & 1) ^ 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      uint8_t* box = sP + pb * C::P_BYTES + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(box + ((u ^ (r & 7)) << 4)) = w[u];
+      for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(my_row + pb * C::P_BYTES + ((u ^ (r & 7)) << 4)) = w[u];
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
-      if (row_ok) {
+    }
+    if (ok && zero_tile) {
+      const int pb = ntiles & 1;
+      ok = mbar_wait(&p_empty[pb], static_cast<uint32_t>((ntiles >> 1) & 1) ^ 1u, abort_flag, status, tmo);
+      if (__all_sync(0xffffffffu, ok)) {
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          if (key0 + u * 8 < P.T) *reinterpret_cast<uint4*>(Prow + key0 + u * 8) = w[u];
+          *reinterpret_cast<uint4*>(my_row + pb * C::P_BYTES + (u << 4)) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[pb]);
+      } else {
+        ok = false;
       }
-    }
-    // Keys up to the next multiple of 256 are written as zeros too (the backward's causal K
-    // loops read that far): for an even query tile, the key tile after the diagonal.
-    if (ok && row_ok && (qt & 1) == 0) {
-      const int key0 = (qt + 1) * kBKV + half * 64;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (key0 + u * 8 < P.T) *reinterpret_cast<uint4*>(Prow + key0 + u * 8) = make_uint4(0, 0, 0, 0);
     }
     // O = (sum_j P_j V_j): this warp stores its half of the d columns
     if (ok) ok = mbar_wait(o_full, 0, abort_flag, status, tmo);
@@ -426,7 +502,7 @@ int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
     rc = encode_map_bf16(&p->q[i], Q[i], T, qc, qc, 64, 128);
     if (!rc) rc = encode_map_bf16(&p->k[i], K[i], T, kc, kc, 64, 128);
     if (!rc) rc = encode_map_bf16(&p->v[i], V[i], T, kc, kc, 64, 64);
-    p->P[i] = static_cast<__nv_bfloat16*>(Pout[i]);
+    if (!rc) rc = encode_map_bf16_3d(&p->pm[i], Pout[i], T, T, nql, T, T * T, 64, 128);
     p->O[i] = static_cast<__nv_bfloat16*>(Oout[i]);
   }
   if (rc) {

@@ -727,6 +727,22 @@ int encode_map_bf16(CUtensorMap* out, const void* ptr, int64_t rows, int64_t col
                   "cuTensorMapEncodeTiled");
 }
 
+int encode_map_bf16_3d(CUtensorMap* out, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int64_t ld1,
+                       int64_t ld2, int box0, int box1) {
+  if (!aligned16(ptr) || (ld1 * 2) % 16 != 0 || (ld2 * 2) % 16 != 0 || d0 % 8 != 0 || d0 <= 0 || d1 <= 0 || d2 <= 0)
+    return set_error(TTL_ERR_ALIGN, "tensor map %p: pointer, strides and width must be 16-byte aligned", ptr);
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return set_error(TTL_ERR_CUDA, "cuTensorMapEncodeTiled not available from the CUDA driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1), static_cast<cuuint64_t>(d2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld1) * 2, static_cast<cuuint64_t>(ld2) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return cu_check(enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                  "cuTensorMapEncodeTiled(3d)");
+}
+
 GemmBatch::GemmBatch() : p_(new GemmParams), nmaps_(0), err_(TTL_OK), flops_(0.0), bytes_(0.0) {
   std::memset(static_cast<void*>(p_), 0, sizeof(GemmParams));
 }

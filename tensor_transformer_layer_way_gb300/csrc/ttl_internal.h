@@ -188,6 +188,11 @@ class GemmBatch {
 int encode_map_bf16(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
                     int box_rows);
 
+// The same for a 3-D bf16 tensor [d2][d1][d0] (d0 contiguous; ld1, ld2 the strides of dims 1
+// and 2 in elements) with a box of box0 x box1 x 1.
+int encode_map_bf16_3d(CUtensorMap* out, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int64_t ld1,
+                       int64_t ld2, int box0, int box1);
+
 // Forward core of the head-split attention block for t shards (one kernel launch): from Q_i
 // [T, qc], K_i and V_i [T, kc] (qc = nql d, kc = nql d / grp) writes the probabilities P_i
 // [nql, T, T] (rows up to key min(T, round_up(q + 1, 256)), zeros above the diagonal) and
