@@ -8,16 +8,15 @@
 // shape.  The pages do not spell out the attention itself; this file computes causal scaled
 // dot-product attention with scale 1/sqrt(d), query head j reading KV head j / (n_q / n_kv).
 //
-// The projections, W_O and every backward contraction run in the tcgen05 GEMM, whose causal
-// modes handle the triangle (score tiles above the diagonal are skipped, dS K stops its K loop
-// at the tile's last query, dS^T Q and P^T dO start theirs at the tile's first key).  The
-// forward core (scores, softmax, P V) is one fused kernel (attention_core.cu); the backward's
-// softmax lives in the dP GEMM's epilogue:
-//   forward : QKV (3t problems) -> fused core: S = Q_c K_g^T in TMEM, exact row statistics,
-//             P = softmax(S / sqrt(d)) (bf16, saved), O_c = P_c V_g -> Y_i = O_i Wo_i -> all-reduce
+// The projections, W_O, dK / dV and the projection gradients run in the tcgen05 GEMM, whose
+// causal mode starts the K loops of dS^T Q and P^T dO at the tile's first key.  The two cores
+// are fused kernels (attention_core.cu) with the scores in tensor memory:
+//   forward : QKV (3t problems) -> core: S = Q_c K_g^T, exact row statistics, P = softmax(S /
+//             sqrt(d)) (bf16, saved), O_c = P_c V_g -> Y_i = O_i Wo_i -> all-reduce
 //   backward: {dO_i = dY Wo_i^T, dWo_i = O_i^T dY} -> D = rowsum(dO_c O_c)
-//             -> dP = dO_c V_g^T, epilogue: dS = P (dP - D) / sqrt(d) as bf16
-//             -> {dQ_c = dS_c K_g, dK_g = sum_c dS_c^T Q_c, dV_g = sum_c P_c^T dO_c}
+//             -> core: dP = dO_c V_g^T, dS = P (dP - D) / sqrt(d) (bf16, to the workspace),
+//                dQ_c = dS_c K_g
+//             -> {dK_g = sum_c dS_c^T Q_c, dV_g = sum_c P_c^T dO_c}
 //             -> {dW_i = X^T d{Q,K,V}_i, dX_i = dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T} -> all-reduce
 //
 // Zero fill: row q of P and of dS is written for every key j < min(T, round_up(q + 1, 256));
@@ -322,43 +321,24 @@ extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
     if ((rc = cuda_check(cudaGetLastError(), "attn_rowdot_kernel launch"))) return rc;
   }
 
-  // dP_c = dO_c V_g^T (tiles above the diagonal skipped); the epilogue turns it into
-  // dS = P (dP - D) / sqrt(d) with the saved probabilities.
-  for (int i = 0; i < t; ++i) {
-    for (int64_t c = 0; c < s.nql; ++c) {
-      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
-      const int mdo = batch.add_map(dO_of(i), T, s.qc, s.qc, false);
-      const int mv = batch.add_map(V_save[i], T, s.kc, s.kc, false);
-      Problem* p = batch.add_problem(T, T, false, false, EPI_SMAX_BWD, false);
-      if (batch.error()) return batch.error();
-      p->causal = CAUSAL_SKIP_UPPER;
-      p->fscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
-      p->out0 = dS_of(i) + c * T * T;
-      p->ld_out = T;
-      p->aux0 = P_save[i] + c * T * T;
-      p->ld_aux = T;
-      p->aux1 = Drow + (static_cast<int64_t>(i) * s.nql + c) * T;
-      if ((rc = batch.add_seg(p, mdo, c * d, mv, -1, (c / s.grp) * d, d))) return rc;
+  // The fused backward core: dP = dO_c V_g^T in TMEM, dS = P (dP - D) / sqrt(d) written to the
+  // workspace, dQ_c = dS_c K_g, for every (shard, head, 128-query tile).
+  {
+    using CP = const void* const*;
+    const void* dOs[kMaxShards];
+    void* dSs[kMaxShards];
+    void* dQs[kMaxShards];
+    for (int i = 0; i < t; ++i) {
+      dOs[i] = dO_of(i);
+      dSs[i] = dS_of(i);
+      dQs[i] = dQ_of(i);
     }
+    if ((rc = attn_bwd_core(t, T, static_cast<int>(s.nql), static_cast<int>(s.grp), d, dOs,
+                            reinterpret_cast<CP>(V_save), reinterpret_cast<CP>(K_save), reinterpret_cast<CP>(P_save),
+                            dSs, dQs, Drow, s.qc, s.kc, st)))
+      return rc;
   }
-  if ((rc = batch.flush(st))) return rc;
 
-  // dQ_c = dS_c K_g: the K loop stops at the tile's last query.
-  for (int i = 0; i < t; ++i) {
-    for (int64_t c = 0; c < s.nql; ++c) {
-      if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
-      const int ms = batch.add_map(dS_of(i), s.nql * T, T, T, false);
-      const int mk = batch.add_map(K_save[i], T, s.kc, s.kc, true);
-      Problem* p = batch.add_problem(T, d, false, true, EPI_BF16, false);
-      if (batch.error()) return batch.error();
-      p->causal = CAUSAL_K_UPTO_ROW;
-      p->a_m0 = static_cast<int32_t>(c * T);
-      p->b_n0 = static_cast<int32_t>((c / s.grp) * d);
-      p->out0 = dQ_of(i) + c * d;
-      p->ld_out = s.qc;
-      if ((rc = batch.add_seg(p, ms, 0, mk, -1, 0, T))) return rc;
-    }
-  }
   // dK_g = sum_c dS_c^T Q_c and dV_g = sum_c P_c^T dO_c over the group's query heads, one K
   // segment per head; the K loop (queries) starts at the tile's first key.
   for (int i = 0; i < t; ++i) {

@@ -488,6 +488,369 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
   }
 }
 
+// ------------------------------------------------------------------ backward core
+
+struct BwdParams {
+  CUtensorMap dO[kMaxShards];    // dO_i [T, n_q/t d], box 64 x 128 (A of dP)
+  CUtensorMap v[kMaxShards];     // V_i [T, n_kv/t d], box 64 x 128 (K-major B of dP = dO V^T)
+  CUtensorMap kmn[kMaxShards];   // K_i [T, n_kv/t d], box 64 x 64 (MN-major B of dQ = dS K)
+  CUtensorMap p[kMaxShards];     // P_i as [n_q/t][T][T], box 64 x 128 x 1 (loads)
+  CUtensorMap ds[kMaxShards];    // dS_i as [n_q/t][T][T], box 64 x 128 x 1 (stores)
+  __nv_bfloat16* dQ[kMaxShards];  // [T, n_q/t d]
+  const float* D;                 // rowsum(dO O), [t][n_q/t][T]
+  int t, nql, grp, T, ntq;
+  float scale;                    // 1 / sqrt(d)
+  int* status;
+  uint64_t timeout_ns;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KB = D / 64;
+  static constexpr int A_BYTES = KB * kBQ * 128;          // the dO tile
+  static constexpr int SLOT = KB * kBKV * 128;            // a V tile or a K tile
+  static constexpr int P_BYTES = kBQ * kBKV * 2;          // a P tile, overwritten in place by dS
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_RING = OFF_A + A_BYTES;
+  static constexpr int OFF_P = OFF_RING + kRing * SLOT;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+};
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// For every (shard, query head, 128-query tile) over the key tiles 0..qt (128 keys each):
+//   dP_j = dO_c V_j^T (tcgen05, TMEM); the P_j tile arrives by TMA into a shared buffer; the
+//   softmax warps overwrite it in place (each thread its own row) with
+//   dS_j = P_j (dP_j - D) / sqrt(d), zeros above the diagonal; dS_j goes to HBM by TMA store
+//   (dK and dV read it) and dQ += dS_j K_j accumulates in TMEM.  dQ is stored at the end.
+// Roles as in the forward core: warp 0 lane 0 loads dO, then V_j / K_j through the 4-slot ring;
+// warp 0 lane 1 loads the P tiles into the two P buffers; warp 1 issues the MMAs (dP_j, then
+// dQ_(j-1)); warps 2..9 compute dS, two per TMEM lane quadrant.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid_constant__ BwdParams P) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sRing = smem + C::OFF_RING;
+  uint8_t* sP = smem + C::OFF_P;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* ring_full = a_full + 1;
+  uint64_t* ring_empty = ring_full + kRing;
+  uint64_t* dp_full = ring_empty + kRing;
+  uint64_t* dp_empty = dp_full + 2;
+  uint64_t* pb_full = dp_empty + 2;
+  uint64_t* pb_empty = pb_full + 2;
+  uint64_t* ds_full = pb_empty + 2;
+  uint64_t* dq_full = ds_full + 2;
+  uint64_t* done_bar = dq_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int heads = P.t * P.nql;
+  const int qt = P.ntq - 1 - static_cast<int>(blockIdx.x) / heads;
+  const int hh = static_cast<int>(blockIdx.x) % heads;
+  const int shard = hh / P.nql;
+  const int c = hh % P.nql;
+  const int g = c / P.grp;
+  const int q0 = qt * kBQ;
+  const int ntiles = qt + 1;
+  const bool zero_tile = (qt & 1) == 0 && (qt + 1) * kBKV < P.T;
+  const int npt = ntiles + (zero_tile ? 1 : 0);   // P buffers used (the zero tile takes one)
+  int* status = P.status;
+  const uint64_t tmo = P.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&dp_full[b], 1);
+      mbar_init(&dp_empty[b], 8);
+      mbar_init(&pb_full[b], 1);
+      mbar_init(&pb_empty[b], 2);   // the dQ MMAs and the TMA store of dS have both read it
+      mbar_init(&ds_full[b], 8);
+    }
+    mbar_init(dq_full, 1);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&P.dO[shard]);
+    tma_prefetch_map(&P.v[shard]);
+    tma_prefetch_map(&P.kmn[shard]);
+    tma_prefetch_map(&P.p[shard]);
+    tma_prefetch_map(&P.ds[shard]);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- dO, then V_j / K_j
+      bool ok = true;
+      mbar_arrive_expect_tx(a_full, C::A_BYTES);
+      for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(sA + kb * 16384, &P.dO[shard], a_full, c * D + kb * 64, q0);
+      int issued = 0;
+      for (int pos = 0; ok && pos < 2 * ntiles; ++pos) {
+        const int slot = pos % kRing;
+        if (!mbar_wait(&ring_empty[slot], (static_cast<uint32_t>(pos / kRing) & 1u) ^ 1u, abort_flag, status, tmo)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = sRing + slot * C::SLOT;
+        const int j = pos >> 1;
+        mbar_arrive_expect_tx(&ring_full[slot], C::SLOT);
+        if ((pos & 1) == 0) {   // V_j, K-major
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(dst + kb * 16384, &P.v[shard], &ring_full[slot], g * D + kb * 64, j * kBKV);
+        } else {                // K_j, MN-major: two 64-key blocks of KB boxes
+          for (int kk = 0; kk < 2; ++kk)
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(dst + (kk * C::KB + kb) * 8192, &P.kmn[shard], &ring_full[slot], g * D + kb * 64,
+                          j * kBKV + kk * 64);
+        }
+        ++issued;
+      }
+      int dummy_abort = 0;
+      mbar_wait(a_full, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+      const int pending = issued < kRing ? issued : kRing;
+      for (int i = issued - pending; i < issued; ++i)
+        mbar_wait(&ring_full[i % kRing], static_cast<uint32_t>(i / kRing) & 1u,
+                  reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+    } else if (lane == 1) {
+      // ---------------------------------------------------------------- P tiles
+      bool ok = true;
+      int started = 0;   // tiles whose buffer phase was started (a load, or the zero tile's arrive)
+      for (int j = 0; ok && j < npt; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
+          ok = false;
+          break;
+        }
+        if (j < ntiles) {
+          mbar_arrive_expect_tx(&pb_full[b], C::P_BYTES);
+          tma_load_3d(sP + b * C::P_BYTES, &P.p[shard], &pb_full[b], j * kBKV, q0, c);
+          tma_load_3d(sP + b * C::P_BYTES + 16384, &P.p[shard], &pb_full[b], j * kBKV + 64, q0, c);
+        } else {
+          mbar_arrive(&pb_full[b]);   // the zero tile: the buffer is free, nothing to load
+        }
+        ++started;
+      }
+      // No copy may still be landing when the CTA leaves: wait (bounded) for the latest phase of
+      // each buffer.  Only the latest: a parity wait on a phase the barrier has since passed
+      // twice would never see it complete.  An earlier load on a buffer completed before the
+      // buffer could be reused.
+      int dummy_abort = 0;
+      for (int b = 0; b < 2; ++b) {
+        const int jl = started - 1 - ((started - 1 - b) & 1);   // last started tile on buffer b
+        if (jl >= 0)
+          mbar_wait(&pb_full[b], static_cast<uint32_t>(jl >> 1) & 1u, reinterpret_cast<volatile int*>(&dummy_abort),
+                    status, tmo);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(a_full, 0, abort_flag, status, tmo);
+      tc_fence_after_sync();
+      const uint32_t aaddr = smem_u32(sA);
+      const uint32_t ring0 = smem_u32(sRing);
+      const uint32_t paddr = smem_u32(sP);
+      const uint32_t idesc_dp = idesc_bf16_f32(kBQ, kBKV, false, false);
+      const uint32_t idesc_dq = idesc_bf16_f32(kBQ, D, false, true);
+      auto wait_pos = [&](int pos) {
+        const int slot = pos % kRing;
+        if (!mbar_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u, abort_flag, status, tmo))
+          return -1;
+        tc_fence_after_sync();
+        return slot;
+      };
+      for (int j = 0; ok && j <= ntiles; ++j) {
+        if (j < ntiles) {   // dP_j = dO V_j^T into score buffer j & 1
+          const int b = j & 1;
+          const int vslot = wait_pos(2 * j);
+          if (vslot < 0 ||
+              !mbar_wait(&dp_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t vaddr = ring0 + vslot * C::SLOT;
+          for (int kb = 0; kb < C::KB; ++kb) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc_sw128(aaddr + kb * 16384 + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(vaddr + kb * 16384 + kk * 32, 16, 1024);
+              umma_bf16(tmem_base + b * kBKV, ad, bd, idesc_dp, (kb | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(&ring_empty[vslot]);
+          umma_commit(&dp_full[b]);
+        }
+        if (j > 0) {        // dS_(j-1) -> HBM, dQ += dS_(j-1) K_(j-1)
+          const int jp = j - 1;
+          const int b = jp & 1;
+          const int kslot = wait_pos(2 * jp + 1);
+          if (kslot < 0 || !mbar_wait(&ds_full[b], static_cast<uint32_t>(jp >> 1) & 1u, abort_flag, status, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES, jp * kBKV, q0, c);
+          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES + 16384, jp * kBKV + 64, q0, c);
+          bulk_commit_group();
+          const uint32_t kaddr = ring0 + kslot * C::SLOT;
+          for (int kk2 = 0; kk2 < 2; ++kk2) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kk2 * 16384 + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(kaddr + kk2 * C::KB * 8192 + kk * 2048, 8192, 1024);
+              umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_dq, (jp | kk2 | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(&ring_empty[kslot]);
+          umma_commit(&pb_empty[b]);                 // first arrival: the MMAs have read dS
+          bulk_wait_group_read<1>();                 // the store of dS_(jp-1) has read its buffer
+          if (jp > 0) mbar_arrive(&pb_empty[(jp - 1) & 1]);
+        }
+      }
+      bulk_wait_group_read<0>();
+      if (ntiles > 0) mbar_arrive(&pb_empty[(ntiles - 1) & 1]);
+      if (ok && zero_tile) {
+        const int b = ntiles & 1;
+        if (mbar_wait(&ds_full[b], static_cast<uint32_t>(ntiles >> 1) & 1u, abort_flag, status, tmo)) {
+          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES, ntiles * kBKV, q0, c);
+          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES + 16384, ntiles * kBKV + 64, q0, c);
+          bulk_commit_group();
+        }
+      }
+      if (ok) umma_commit(dq_full);
+      umma_commit(done_bar);
+      int dummy_abort = 0;
+      mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+      bulk_wait_group_all();
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ dS warps
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quad * 32 + lane;
+    const int q = q0 + r;
+    const bool row_ok = q < P.T;
+    const float Dq = row_ok ? P.D[(static_cast<int64_t>(shard) * P.nql + c) * P.T + q] : 0.0f;
+    const float scale = P.scale;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+    bool ok = true;
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int b = j & 1;
+      ok = mbar_wait(&dp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64, r0);
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64 + 32, r1);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dp_empty[b]);
+      ok = mbar_wait(&pb_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      uint8_t* row = my_row + b * C::P_BYTES;
+      const int nv = q - (j * kBKV + half * 64) + 1;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
+        const uint4 pw = *unit;
+        const uint32_t pv[4] = {pw.x, pw.y, pw.z, pw.w};
+        float e8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int col = u * 8 + e;
+          const float dp = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
+          const float p = (e & 1) ? bf16_hi(pv[e >> 1]) : bf16_lo(pv[e >> 1]);
+          const float ds = (dp - Dq) * (p * scale);
+          e8[e] = (nv >= 64 || col < nv) ? ds : 0.0f;
+        }
+        *unit = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
+                           pack_bf16x2(e8[6], e8[7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ds_full[b]);
+    }
+    if (ok && zero_tile) {
+      const int b = ntiles & 1;
+      ok = mbar_wait(&pb_full[b], static_cast<uint32_t>(ntiles >> 1) & 1u, abort_flag, status, tmo);
+      if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(my_row + b * C::P_BYTES + (u << 4)) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_full[b]);
+      } else {
+        ok = false;
+      }
+    }
+    if (ok) ok = mbar_wait(dq_full, 0, abort_flag, status, tmo);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after_sync();
+      __nv_bfloat16* out = P.dQ[shard] + static_cast<int64_t>(row_ok ? q : 0) * (P.nql * D) + c * D + half * (D / 2);
+#pragma unroll
+      for (int cc = 0; cc < D / 2; cc += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(lane_base + 2 * kBKV + half * (D / 2) + cc, o);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(out + cc + u * 8) = make_uint4(
+                pack_bf16x2(__uint_as_float(o[u * 8 + 0]), __uint_as_float(o[u * 8 + 1])),
+                pack_bf16x2(__uint_as_float(o[u * 8 + 2]), __uint_as_float(o[u * 8 + 3])),
+                pack_bf16x2(__uint_as_float(o[u * 8 + 4]), __uint_as_float(o[u * 8 + 5])),
+                pack_bf16x2(__uint_as_float(o[u * 8 + 6]), __uint_as_float(o[u * 8 + 7])));
+        }
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 }  // namespace
 
 int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* Q, const void* const* K,
@@ -554,6 +917,75 @@ int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
   }
   delete p;
   return cuda_check(cudaGetLastError(), "attn_fwd_core_kernel launch");
+}
+
+
+int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* dO, const void* const* V,
+                  const void* const* K, const void* const* Pin, void* const* dS, void* const* dQ, const float* Drow,
+                  int64_t qc, int64_t kc, cudaStream_t stream) {
+  if (d != 64 && d != 128) return set_error(TTL_ERR_SHAPE, "attention core: head dimension %d is not 64 or 128", d);
+  int rc = require_sm103();
+  if (rc) return rc;
+  BwdParams* p = new BwdParams;
+  std::memset(static_cast<void*>(p), 0, sizeof(BwdParams));
+  for (int i = 0; i < t && !rc; ++i) {
+    rc = encode_map_bf16(&p->dO[i], dO[i], T, qc, qc, 64, 128);
+    if (!rc) rc = encode_map_bf16(&p->v[i], V[i], T, kc, kc, 64, 128);
+    if (!rc) rc = encode_map_bf16(&p->kmn[i], K[i], T, kc, kc, 64, 64);
+    if (!rc) rc = encode_map_bf16_3d(&p->p[i], Pin[i], T, T, nql, T, T * T, 64, 128);
+    if (!rc) rc = encode_map_bf16_3d(&p->ds[i], dS[i], T, T, nql, T, T * T, 64, 128);
+    p->dQ[i] = static_cast<__nv_bfloat16*>(dQ[i]);
+  }
+  if (rc) {
+    delete p;
+    return rc;
+  }
+  p->D = Drow;
+  p->t = t;
+  p->nql = nql;
+  p->grp = grp;
+  p->T = static_cast<int>(T);
+  p->ntq = static_cast<int>((T + kBQ - 1) / kBQ);
+  p->scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  p->status = device_status_ptr();
+  p->timeout_ns = 2000000000ull;
+  if (!p->status) {
+    delete p;
+    return TTL_ERR_CUDA;
+  }
+  const unsigned blocks = static_cast<unsigned>(t) * nql * p->ntq;
+  const double tri = static_cast<double>(T) * (T + 1) / 2.0;
+  // Algorithmic work: dP = dO V^T and dQ = dS K over the causal triangle; bytes: P read, dS
+  // written, dO, V, K read and dQ written once.
+  TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
+                4.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
+  if (d == 128) {
+    static bool attr = false;
+    if (!attr) {
+      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_core_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                BwdCfg<128>::SMEM),
+                           "cudaFuncSetAttribute(attn bwd core)"))) {
+        delete p;
+        return rc;
+      }
+      attr = true;
+    }
+    attn_bwd_core_kernel<128><<<blocks, kThreads, BwdCfg<128>::SMEM, stream>>>(*p);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_core_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                BwdCfg<64>::SMEM),
+                           "cudaFuncSetAttribute(attn bwd core)"))) {
+        delete p;
+        return rc;
+      }
+      attr = true;
+    }
+    attn_bwd_core_kernel<64><<<blocks, kThreads, BwdCfg<64>::SMEM, stream>>>(*p);
+  }
+  delete p;
+  return cuda_check(cudaGetLastError(), "attn_bwd_core_kernel launch");
 }
 
 }  // namespace ttl

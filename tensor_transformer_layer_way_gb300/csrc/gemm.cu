@@ -99,22 +99,14 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile, 
   return c;
 }
 
-// Causal structure: whether a tile has any work, and the k-block range of one segment.
-template <int TILE_M>
-__device__ __forceinline__ bool tile_skipped(const Problem& pr, const TileCoord& c) {
-  return pr.causal == CAUSAL_SKIP_UPPER && c.tn * BN >= (c.tm + 1) * TILE_M;
-}
-
+// Causal structure: the k-block range of one segment (K = queries, rows = keys: the queries
+// before the tile's first key contribute nothing).
 template <int TILE_M>
 __device__ __forceinline__ void seg_kblocks(const Problem& pr, const Seg& sg, const TileCoord& c, int& kb0,
                                             int& kb1) {
   kb0 = 0;
   kb1 = sg.kblocks;
-  if (pr.causal == CAUSAL_K_UPTO_ROW) {
-    kb1 = min(kb1, ((c.tm + 1) * TILE_M + BK - 1) / BK);
-  } else if (pr.causal == CAUSAL_K_FROM_ROW) {
-    kb0 = min(kb1, (c.tm * TILE_M) / BK);
-  }
+  if (pr.causal == CAUSAL_K_FROM_ROW) kb0 = min(kb1, (c.tm * TILE_M) / BK);
 }
 
 // ------------------------------------------------------------------ epilogue math
@@ -188,7 +180,7 @@ __device__ __forceinline__ void load_row32_bf16(const void* base, int64_t ld, in
 // accumulator is ready.  One 128-byte line per 64 bf16 columns, over the BN / 2 columns of
 // this warp's half of the tile.
 __device__ __forceinline__ void prefetch_aux_row(const Problem& pr, int row, int n_base) {
-  if (pr.epi != EPI_GELU_BWD && pr.epi != EPI_SWIGLU_BWD && pr.epi != EPI_SMAX_BWD) return;
+  if (pr.epi != EPI_GELU_BWD && pr.epi != EPI_SWIGLU_BWD) return;
   if (row >= pr.M) return;
 #pragma unroll
   for (int c = 0; c < BN / 2; c += 64) {
@@ -204,7 +196,6 @@ __device__ __forceinline__ void prefetch_aux_row(const Problem& pr, int row, int
 struct EpiState {
   float m = -INFINITY, s = 0.0f;   // EPI_F32_CE: running max and sum
   int64_t ce_tgt = -1;             // EPI_F32_CE: target column relative to the tile's first
-  float a = 0.0f;                  // EPI_SMAX_BWD: rowsum(dO O)
 };
 
 // The epilogue of one 32-column chunk (chunk `ch` of the tile starting at column n_base) of
@@ -217,22 +208,6 @@ __device__ __forceinline__ void epilogue_chunk(const Problem& pr, int row, int n
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  if (epi == EPI_SMAX_BWD) {
-    // causal: column j is valid for j <= row; the chunk is "full" when all 32 are valid
-    const int nv = min(pr.N - col0, row - col0 + 1);
-    const bool full = nv >= 32;
-    const float k = pr.fscale;
-    float p[32];
-    load_row32_bf16(pr.aux0, pr.ld_aux, row, col0, pr.N, p);
-    const float D = st.a;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float ds = (v[j] - D) * (p[j] * k);
-      v[j] = (full || j < nv) ? ds : 0.0f;
-    }
-    store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, v);
-    return;
-  }
   if (epi == EPI_F32) {
     store_row32_f32(pr.out0, pr.ld_out, row, col0, pr.N, v);
   } else if (epi == EPI_F32_CE) {
@@ -321,7 +296,6 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
   }
   EpiState st;
   if (epi == EPI_F32_CE && row_ok) st.ce_tgt = reinterpret_cast<const int64_t*>(pr.aux0)[row] - pr.ext0 - n_base;
-  if (row_ok && epi == EPI_SMAX_BWD) st.a = reinterpret_cast<const float*>(pr.aux1)[row];
   // Two 32-column chunks per TMEM round trip: both loads are in flight before the one wait.
 #pragma unroll 1
   for (int ch = half * (BN / 2 / 32); ch < (half + 1) * (BN / 2 / 32); ch += 2) {
@@ -412,7 +386,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
         const TileCoord c = decode_tile(P, tile, gi);
         const Problem& pr = P.probs[c.p];
-        if (tile_skipped<C::TILE_M>(pr, c)) continue;
         int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
         int slab = 0;
         if (pr.a_slab_rows > 0) {   // rows of token slab `slab` come from its own map
@@ -520,7 +493,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
         const TileCoord c = decode_tile(P, tile, gi);
         const Problem& pr = P.probs[c.p];
-        if (tile_skipped<C::TILE_M>(pr, c)) continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
@@ -593,7 +565,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     for (int tile = unit; tile < P.total_tiles; tile += nunits) {
       const TileCoord c = decode_tile(P, tile, gi);
       const Problem& pr = P.probs[c.p];
-      if (tile_skipped<C::TILE_M>(pr, c)) continue;
       const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
@@ -857,9 +828,9 @@ int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b
   bytes_ += 2.0 * (static_cast<double>(p->M) * K + ncols * K) * tri;
   if (p->nseg == 1) {
     const int nout = p->epi == EPI_SWIGLU_FWD ? 3 : (p->epi == EPI_GELU_FWD || p->epi == EPI_SWIGLU_BWD) ? 2 : 1;
-    const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : (p->epi == EPI_GELU_BWD || p->epi == EPI_SMAX_BWD) ? 1 : 0;
+    const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : p->epi == EPI_GELU_BWD ? 1 : 0;
     const double esz = (p->epi == EPI_F32 || p->epi == EPI_F32_CE) ? 4.0 : 2.0;
-    bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux) * (p->causal == CAUSAL_SKIP_UPPER ? tri : 1.0);
+    bytes_ += static_cast<double>(p->M) * p->N * (esz * nout + 2.0 * naux);
   }
   return TTL_OK;
 }

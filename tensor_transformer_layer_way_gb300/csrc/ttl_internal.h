@@ -64,17 +64,12 @@ enum Epilogue : int {
                        // the cross-entropy partials: out1[row * ext1 + 2 (tn0 + tn) + half] =
                        // (max, sum exp(z - max)) over those columns; out2[row] = the logit at
                        // target aux0[row] - ext0 when that column is in the tile
-  // Causal attention score gradients (rows = queries, columns = keys; column j valid for j <= row):
-  EPI_SMAX_BWD = 7,    // out0 = bf16(aux0 * (acc - aux1[row]) * fscale), aux0 = saved P (bf16, ld_aux),
-                       // aux1 = rowsum(dO O) (fp32), zeros in the invalid columns
 };
 
 // Causal structure of a problem whose rows or columns are token positions (attention).
 enum Causal : int {
   CAUSAL_NONE = 0,
-  CAUSAL_SKIP_UPPER = 1,   // rows = queries, cols = keys: tiles wholly above the diagonal are skipped
-  CAUSAL_K_UPTO_ROW = 2,   // rows = queries, K = keys: each segment's K loop stops after the tile's last row
-  CAUSAL_K_FROM_ROW = 3,   // rows = keys, K = queries: each segment's K loop starts at the tile's first row
+  CAUSAL_K_FROM_ROW = 1,   // rows = keys, K = queries: each segment's K loop starts at the tile's first row
 };
 
 // One K-range of a problem: k-blocks of 64 read from map_a at K offset a_k0 and from
@@ -111,8 +106,6 @@ struct Problem {
   int64_t ld_out;         // row stride (elements) of out0/out1/out2
   int64_t ld_aux;         // row stride (elements) of aux0/aux1
   int64_t ext0, ext1;     // epilogue-specific integers (EPI_F32_CE: vocab offset, row stride of out1)
-  float fscale;           // epilogue-specific scale (EPI_SMAX_BWD: 1 / sqrt(d))
-  int32_t pad2;
 };
 
 // Consecutive problems with the same M that read the same A rows form one tile group: its
@@ -200,6 +193,14 @@ int encode_map_bf16_3d(CUtensorMap* out, const void* ptr, int64_t d0, int64_t d1
 int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* Q, const void* const* K,
                   const void* const* V, void* const* Pout, void* const* Oout, int64_t qc, int64_t kc,
                   cudaStream_t stream);
+
+// Backward core of the head-split attention block (one launch): from dO_i [T, qc], V_i, K_i
+// [T, kc], the saved P_i [nql, T, T] and D = rowsum(dO O) [t][nql][T] (fp32) writes
+// dS_i = P (dO V^T - D) / sqrt(d) [nql, T, T] (same written span and zeros as P) and
+// dQ_i = dS K [T, qc].  d is 64 or 128.
+int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* dO, const void* const* V,
+                  const void* const* K, const void* const* Pin, void* const* dS, void* const* dQ, const float* Drow,
+                  int64_t qc, int64_t kc, cudaStream_t stream);
 
 // Zero-fill helper (used where a contraction is empty).
 int fill_zero(void* ptr, size_t bytes, cudaStream_t stream);
