@@ -325,7 +325,7 @@ int ttl_vocab_parallel_embedding_bwd(int t, int64_t T, int64_t h, int64_t V, con
  *   X [T,h]; Wq[i] [h, n_q/t d]; Wk[i], Wv[i] [h, n_kv/t d]; Wo[i] [n_q/t d, h]
  *   Q_save[i] [T, n_q/t d], K_save[i], V_save[i] [T, n_kv/t d], O_save[i] [T, n_q/t d]  out
  *   P_save[i] [n_q/t, T, T] out: the probabilities, head-major; row q is written for keys
- *             j < min(T, round_up(q+1, 256)) (zeros above the diagonal), the rest is untouched
+ *             j < min(T, round_up(q+1, 128)) (zeros above the diagonal), the rest is untouched
  *   Y[i] [T,h] out: partial O_i Wo_i, then the all-reduced block output in every buffer
  *   ws   unused: ttl_tp_attn_fwd_workspace_size() returns 0 and ws may be null.  The scores
  *        and the softmax statistics stay on chip: one fused kernel per 128-query tile computes
@@ -347,8 +347,10 @@ int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const
  *   dY [T,h]; X, W*, *_save as given to / written by ttl_tp_attn_fwd
  *   dWq[i], dWk[i], dWv[i], dWo[i] out, shaped like the weights
  *   dX[i] [T,h] out: partial, then the all-reduced dX in every buffer
- *   ws   workspace of ttl_tp_attn_bwd_workspace_size() bytes: rowsum(dO O) per query row,
- *        then per shard dS [n_q/t, T, T] bf16 (written by the dP GEMM's epilogue), dO, dQ, dK, dV
+ *   ws   workspace of ttl_tp_attn_bwd_workspace_size() bytes: rowsum(dO O) per query row, then
+ *        per shard dO, dQ, dK, dV.  The score gradients dS never reach memory: a kernel per
+ *        query tile (dQ) and one per key tile (dK, dV) each recompute dP = dO V^T in tensor
+ *        memory and dS from the saved P
  * T = 0 writes zero weight gradients (token-sized pointers may then be null). */
 size_t ttl_tp_attn_bwd_workspace_size(int t, int64_t T, int n_q, int n_kv, int d);
 int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, int d, const ttl_bf16* X,

@@ -8,20 +8,17 @@
 // shape.  The pages do not spell out the attention itself; this file computes causal scaled
 // dot-product attention with scale 1/sqrt(d), query head j reading KV head j / (n_q / n_kv).
 //
-// The projections, W_O, dK / dV and the projection gradients run in the tcgen05 GEMM, whose
-// causal mode starts the K loops of dS^T Q and P^T dO at the tile's first key.  The two cores
-// are fused kernels (attention_core.cu) with the scores in tensor memory:
+// The projections, W_O and the projection gradients run in the tcgen05 GEMM; the attention
+// itself runs in three fused kernels (attention_core.cu) with every score tile in tensor memory:
 //   forward : QKV (3t problems) -> core: S = Q_c K_g^T, exact row statistics, P = softmax(S /
 //             sqrt(d)) (bf16, saved), O_c = P_c V_g -> Y_i = O_i Wo_i -> all-reduce
 //   backward: {dO_i = dY Wo_i^T, dWo_i = O_i^T dY} -> D = rowsum(dO_c O_c)
-//             -> core: dP = dO_c V_g^T, dS = P (dP - D) / sqrt(d) (bf16, to the workspace),
-//                dQ_c = dS_c K_g
-//             -> {dK_g = sum_c dS_c^T Q_c, dV_g = sum_c P_c^T dO_c}
+//             -> query-tile core: dP = dO_c V_g^T, dS = P (dP - D) / sqrt(d), dQ_c = dS_c K_g
+//             -> key-tile core: the same dP and dS, dK_g = sum_c dS_c^T Q_c, dV_g = sum_c P_c^T dO_c
 //             -> {dW_i = X^T d{Q,K,V}_i, dX_i = dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T} -> all-reduce
-//
-// Zero fill: row q of P and of dS is written for every key j < min(T, round_up(q + 1, 256));
-// the keys above the diagonal get exact zeros.  That covers every element the causal GEMMs
-// read with either tile height (128 or 256 rows), so no full-size mask pass is needed.
+// Only P goes through HBM (written once, read by both backward cores); dS never does.
+// Row q of P is written for every key j < min(T, round_up(q + 1, 128)) (its query tile's
+// diagonal tile), with exact zeros above the diagonal.
 
 #include <cmath>
 
@@ -108,30 +105,14 @@ int check_ptrs(const void* const* arr, int t, const char* what) {
   return TTL_OK;
 }
 
-size_t score_bytes(const Shape& s, size_t esz) {   // one shard's [n_q/t, T, T] block
-  return round256(static_cast<size_t>(s.nql) * static_cast<size_t>(s.T) * static_cast<size_t>(s.T) * esz);
-}
-
-// MN-major operand rows [T queries, T keys] of head c in a shard's head-major [n_q/t, T, T]
-// block.  When T is a multiple of 64 no k-block crosses into the next head, so one map with a
-// K offset serves every head; otherwise each head gets its own map, whose edge reads as zeros.
-int head_block_map(GemmBatch& b, const __nv_bfloat16* base, const Shape& s, int64_t c, int64_t* k0) {
-  if (s.T % 64 == 0) {
-    *k0 = c * s.T;
-    return b.add_map(base, s.nql * s.T, s.T, s.T, true);
-  }
-  *k0 = 0;
-  return b.add_map(base + c * s.T * s.T, s.T, s.T, s.T, true);
-}
-
 const __nv_bfloat16* bf(const ttl_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
 
-// Backward workspace: D = rowsum(dO O) [t n_q/t T] fp32, then per shard dS (bf16 [n_q/t, T, T]),
-// dO, dQ ([T, n_q/t d]), dK, dV ([T, n_kv/t d]).
+// Backward workspace: D = rowsum(dO O) [t n_q/t T] fp32, then per shard dO, dQ ([T, n_q/t d]),
+// dK, dV ([T, n_kv/t d]).
 size_t bwd_d_bytes(const Shape& s) { return round256(static_cast<size_t>(s.t * s.nql * s.T) * 4); }
 size_t bwd_shard_bytes(const Shape& s) {
   const size_t tok = static_cast<size_t>(s.T) * 2;
-  return score_bytes(s, 2) + 2 * round256(tok * s.qc) + 2 * round256(tok * s.kc);
+  return 2 * round256(tok * s.qc) + 2 * round256(tok * s.kc);
 }
 
 }  // namespace
@@ -270,18 +251,16 @@ extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
     return set_error(TTL_ERR_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
   if (!aligned16(ws)) return set_error(TTL_ERR_ALIGN, "%s: workspace not 16-byte aligned", name);
 
-  // Workspace: D for every (shard, head, query) row, then per shard dS, dO_i, dQ_i, dK_i, dV_i.
-  const size_t b_ds = score_bytes(s, 2);
+  // Workspace: D for every (shard, head, query) row, then per shard dO_i, dQ_i, dK_i, dV_i.
   const size_t b_q = round256(static_cast<size_t>(T) * 2 * s.qc), b_k = round256(static_cast<size_t>(T) * 2 * s.kc);
   float* Drow = static_cast<float*>(ws);
   auto base = [&](int i) {
     return static_cast<char*>(ws) + bwd_d_bytes(s) + bwd_shard_bytes(s) * static_cast<size_t>(i);
   };
-  auto dS_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i)); };
-  auto dO_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds); };
-  auto dQ_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds + b_q); };
-  auto dK_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds + 2 * b_q); };
-  auto dV_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_ds + 2 * b_q + b_k); };
+  auto dO_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i)); };
+  auto dQ_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + b_q); };
+  auto dK_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + 2 * b_q); };
+  auto dV_of = [&](int i) { return reinterpret_cast<__nv_bfloat16*>(base(i) + 2 * b_q + b_k); };
   GemmBatch batch;
 
   // g backward is the identity: dO_i = dY Wo_i^T (one tile group over dY) and dWo_i = O_i^T dY.
@@ -321,48 +300,30 @@ extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
     if ((rc = cuda_check(cudaGetLastError(), "attn_rowdot_kernel launch"))) return rc;
   }
 
-  // The fused backward core: dP = dO_c V_g^T in TMEM, dS = P (dP - D) / sqrt(d) written to the
-  // workspace, dQ_c = dS_c K_g, for every (shard, head, 128-query tile).
+  // The backward cores: dQ per (shard, query head, 128-query tile) and dK, dV per (shard, KV
+  // head, 128-key tile), each recomputing dP = dO V^T in TMEM and dS = P (dP - D) / sqrt(d) on
+  // chip from the saved P.
   {
     using CP = const void* const*;
     const void* dOs[kMaxShards];
-    void* dSs[kMaxShards];
     void* dQs[kMaxShards];
+    void* dKs[kMaxShards];
+    void* dVs[kMaxShards];
     for (int i = 0; i < t; ++i) {
       dOs[i] = dO_of(i);
-      dSs[i] = dS_of(i);
       dQs[i] = dQ_of(i);
+      dKs[i] = dK_of(i);
+      dVs[i] = dV_of(i);
     }
     if ((rc = attn_bwd_core(t, T, static_cast<int>(s.nql), static_cast<int>(s.grp), d, dOs,
                             reinterpret_cast<CP>(V_save), reinterpret_cast<CP>(K_save), reinterpret_cast<CP>(P_save),
-                            dSs, dQs, Drow, s.qc, s.kc, st)))
+                            dQs, Drow, s.qc, s.kc, st)))
+      return rc;
+    if ((rc = attn_bwd_kv(t, T, static_cast<int>(s.nql), static_cast<int>(s.nkvl), static_cast<int>(s.grp), d,
+                          reinterpret_cast<CP>(Q_save), dOs, reinterpret_cast<CP>(V_save), reinterpret_cast<CP>(P_save),
+                          dKs, dVs, Drow, s.qc, s.kc, st)))
       return rc;
   }
-
-  // dK_g = sum_c dS_c^T Q_c and dV_g = sum_c P_c^T dO_c over the group's query heads, one K
-  // segment per head; the K loop (queries) starts at the tile's first key.
-  for (int i = 0; i < t; ++i) {
-    for (int64_t g = 0; g < s.nkvl; ++g) {
-      for (int w = 0; w < 2; ++w) {
-        if (!batch.has_room(static_cast<int>(2 * s.grp), 1) && (rc = batch.flush(st))) return rc;
-        const __nv_bfloat16* a_base = w == 0 ? dS_of(i) : bf(P_save[i]);
-        const void* b_base = w == 0 ? static_cast<const void*>(Q_save[i]) : static_cast<const void*>(dO_of(i));
-        const int mb = batch.add_map(b_base, T, s.qc, s.qc, true);
-        Problem* p = batch.add_problem(T, d, true, true, EPI_BF16, false);
-        if (batch.error()) return batch.error();
-        p->causal = CAUSAL_K_FROM_ROW;
-        p->out0 = (w == 0 ? dK_of(i) : dV_of(i)) + g * d;
-        p->ld_out = s.kc;
-        for (int64_t c = g * s.grp; c < (g + 1) * s.grp; ++c) {
-          int64_t k0 = 0;
-          const int ma = head_block_map(batch, a_base, s, c, &k0);
-          if (batch.error()) return batch.error();
-          if ((rc = batch.add_seg(p, ma, k0, mb, -1, 0, T, c * d))) return rc;
-        }
-      }
-    }
-  }
-  if ((rc = batch.flush(st))) return rc;
 
   // Column-parallel projections backward: dW{q,k,v}_i = X^T d{Q,K,V}_i (one tile group over
   // X^T) and the dX partials dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T (three K segments).

@@ -126,9 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
   const int g = c / P.grp;                  // its KV head within the shard
   const int q0 = qt * kBQ;
   const int ntiles = qt + 1;   // key tiles 0..qt (qt * 128 < T)
-  // The keys up to the next multiple of 256 are written as zeros (the backward's causal K loops
-  // read that far): for an even query tile, one all-zero P tile after the diagonal.
-  const bool zero_tile = (qt & 1) == 0 && (qt + 1) * kBKV < P.T;
   int* status = P.status;
   const uint64_t tmo = P.timeout_ns;
 
@@ -285,14 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       }
       bulk_wait_group_read<0>();
       if (ntiles > 0) mbar_arrive(&p_empty[(ntiles - 1) & 1]);
-      if (ok && zero_tile) {
-        const int b = ntiles & 1;
-        if (mbar_wait(&p_full[b], static_cast<uint32_t>(ntiles >> 1) & 1u, abort_flag, status, tmo)) {
-          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, ntiles * kBKV, q0, c);
-          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, ntiles * kBKV + 64, q0, c);
-          bulk_commit_group();
-        }
-      }
       if (ok) umma_commit(o_full);
       // Every MMA issued here must finish before TMEM is released, and every store before the
       // CTA's shared memory goes away.
@@ -443,20 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
     }
-    if (ok && zero_tile) {
-      const int pb = ntiles & 1;
-      ok = mbar_wait(&p_empty[pb], static_cast<uint32_t>((ntiles >> 1) & 1) ^ 1u, abort_flag, status, tmo);
-      if (__all_sync(0xffffffffu, ok)) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(my_row + pb * C::P_BYTES + (u << 4)) = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[pb]);
-      } else {
-        ok = false;
-      }
-    }
     // O = (sum_j P_j V_j): this warp stores its half of the d columns
     if (ok) ok = mbar_wait(o_full, 0, abort_flag, status, tmo);
     if (__all_sync(0xffffffffu, ok)) {
@@ -495,7 +470,6 @@ struct BwdParams {
   CUtensorMap v[kMaxShards];     // V_i [T, n_kv/t d], box 64 x 128 (K-major B of dP = dO V^T)
   CUtensorMap kmn[kMaxShards];   // K_i [T, n_kv/t d], box 64 x 64 (MN-major B of dQ = dS K)
   CUtensorMap p[kMaxShards];     // P_i as [n_q/t][T][T], box 64 x 128 x 1 (loads)
-  CUtensorMap ds[kMaxShards];    // dS_i as [n_q/t][T][T], box 64 x 128 x 1 (stores)
   __nv_bfloat16* dQ[kMaxShards];  // [T, n_q/t d]
   const float* D;                 // rowsum(dO O), [t][n_q/t][T]
   int t, nql, grp, T, ntq;
@@ -527,11 +501,11 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// For every (shard, query head, 128-query tile) over the key tiles 0..qt (128 keys each):
+// dQ: for every (shard, query head, 128-query tile) over the key tiles 0..qt (128 keys each):
 //   dP_j = dO_c V_j^T (tcgen05, TMEM); the P_j tile arrives by TMA into a shared buffer; the
 //   softmax warps overwrite it in place (each thread its own row) with
-//   dS_j = P_j (dP_j - D) / sqrt(d), zeros above the diagonal; dS_j goes to HBM by TMA store
-//   (dK and dV read it) and dQ += dS_j K_j accumulates in TMEM.  dQ is stored at the end.
+//   dS_j = P_j (dP_j - D) / sqrt(d) (P is zero above the diagonal, so is dS), and
+//   dQ += dS_j K_j accumulates in TMEM.  dQ is stored at the end.
 // Roles as in the forward core: warp 0 lane 0 loads dO, then V_j / K_j through the 4-slot ring;
 // warp 0 lane 1 loads the P tiles into the two P buffers; warp 1 issues the MMAs (dP_j, then
 // dQ_(j-1)); warps 2..9 compute dS, two per TMEM lane quadrant.
@@ -566,8 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
   const int g = c / P.grp;
   const int q0 = qt * kBQ;
   const int ntiles = qt + 1;
-  const bool zero_tile = (qt & 1) == 0 && (qt + 1) * kBKV < P.T;
-  const int npt = ntiles + (zero_tile ? 1 : 0);   // P buffers used (the zero tile takes one)
   int* status = P.status;
   const uint64_t tmo = P.timeout_ns;
 
@@ -581,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
       mbar_init(&dp_full[b], 1);
       mbar_init(&dp_empty[b], 8);
       mbar_init(&pb_full[b], 1);
-      mbar_init(&pb_empty[b], 2);   // the dQ MMAs and the TMA store of dS have both read it
+      mbar_init(&pb_empty[b], 1);   // the dQ MMAs have read dS
       mbar_init(&ds_full[b], 8);
     }
     mbar_init(dq_full, 1);
@@ -594,7 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
     tma_prefetch_map(&P.v[shard]);
     tma_prefetch_map(&P.kmn[shard]);
     tma_prefetch_map(&P.p[shard]);
-    tma_prefetch_map(&P.ds[shard]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -641,20 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
     } else if (lane == 1) {
       // ---------------------------------------------------------------- P tiles
       bool ok = true;
-      int started = 0;   // tiles whose buffer phase was started (a load, or the zero tile's arrive)
-      for (int j = 0; ok && j < npt; ++j) {
+      int started = 0;   // P tiles whose load was issued
+      for (int j = 0; ok && j < ntiles; ++j) {
         const int b = j & 1;
         if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
-        if (j < ntiles) {
-          mbar_arrive_expect_tx(&pb_full[b], C::P_BYTES);
-          tma_load_3d(sP + b * C::P_BYTES, &P.p[shard], &pb_full[b], j * kBKV, q0, c);
-          tma_load_3d(sP + b * C::P_BYTES + 16384, &P.p[shard], &pb_full[b], j * kBKV + 64, q0, c);
-        } else {
-          mbar_arrive(&pb_full[b]);   // the zero tile: the buffer is free, nothing to load
-        }
+        mbar_arrive_expect_tx(&pb_full[b], C::P_BYTES);
+        tma_load_3d(sP + b * C::P_BYTES, &P.p[shard], &pb_full[b], j * kBKV, q0, c);
+        tma_load_3d(sP + b * C::P_BYTES + 16384, &P.p[shard], &pb_full[b], j * kBKV + 64, q0, c);
         ++started;
       }
       // No copy may still be landing when the CTA leaves: wait (bounded) for the latest phase of
@@ -709,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
           umma_commit(&ring_empty[vslot]);
           umma_commit(&dp_full[b]);
         }
-        if (j > 0) {        // dS_(j-1) -> HBM, dQ += dS_(j-1) K_(j-1)
+        if (j > 0) {        // dQ += dS_(j-1) K_(j-1)
           const int jp = j - 1;
           const int b = jp & 1;
           const int kslot = wait_pos(2 * jp + 1);
@@ -718,9 +685,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
             break;
           }
           tc_fence_after_sync();
-          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES, jp * kBKV, q0, c);
-          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES + 16384, jp * kBKV + 64, q0, c);
-          bulk_commit_group();
           const uint32_t kaddr = ring0 + kslot * C::SLOT;
           for (int kk2 = 0; kk2 < 2; ++kk2) {
 #pragma unroll
@@ -731,26 +695,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
             }
           }
           umma_commit(&ring_empty[kslot]);
-          umma_commit(&pb_empty[b]);                 // first arrival: the MMAs have read dS
-          bulk_wait_group_read<1>();                 // the store of dS_(jp-1) has read its buffer
-          if (jp > 0) mbar_arrive(&pb_empty[(jp - 1) & 1]);
-        }
-      }
-      bulk_wait_group_read<0>();
-      if (ntiles > 0) mbar_arrive(&pb_empty[(ntiles - 1) & 1]);
-      if (ok && zero_tile) {
-        const int b = ntiles & 1;
-        if (mbar_wait(&ds_full[b], static_cast<uint32_t>(ntiles >> 1) & 1u, abort_flag, status, tmo)) {
-          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES, ntiles * kBKV, q0, c);
-          tma_store_3d(&P.ds[shard], sP + b * C::P_BYTES + 16384, ntiles * kBKV + 64, q0, c);
-          bulk_commit_group();
+          umma_commit(&pb_empty[b]);                 // the MMAs have read dS: the buffer is free
         }
       }
       if (ok) umma_commit(dq_full);
       umma_commit(done_bar);
       int dummy_abort = 0;
       mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
-      bulk_wait_group_all();
     }
     __syncwarp();
   } else {
@@ -786,7 +737,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
         break;
       }
       uint8_t* row = my_row + b * C::P_BYTES;
-      const int nv = q - (j * kBKV + half * 64) + 1;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
@@ -798,8 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
           const int col = u * 8 + e;
           const float dp = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
           const float p = (e & 1) ? bf16_hi(pv[e >> 1]) : bf16_lo(pv[e >> 1]);
-          const float ds = (dp - Dq) * (p * scale);
-          e8[e] = (nv >= 64 || col < nv) ? ds : 0.0f;
+          e8[e] = (dp - Dq) * (p * scale);   // P is zero above the diagonal
         }
         *unit = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
                            pack_bf16x2(e8[6], e8[7]));
@@ -807,19 +756,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[b]);
-    }
-    if (ok && zero_tile) {
-      const int b = ntiles & 1;
-      ok = mbar_wait(&pb_full[b], static_cast<uint32_t>(ntiles >> 1) & 1u, abort_flag, status, tmo);
-      if (__all_sync(0xffffffffu, ok)) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(my_row + b * C::P_BYTES + (u << 4)) = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ds_full[b]);
-      } else {
-        ok = false;
-      }
     }
     if (ok) ok = mbar_wait(dq_full, 0, abort_flag, status, tmo);
     if (__all_sync(0xffffffffu, ok)) {
@@ -838,6 +774,349 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
                 pack_bf16x2(__uint_as_float(o[u * 8 + 2]), __uint_as_float(o[u * 8 + 3])),
                 pack_bf16x2(__uint_as_float(o[u * 8 + 4]), __uint_as_float(o[u * 8 + 5])),
                 pack_bf16x2(__uint_as_float(o[u * 8 + 6]), __uint_as_float(o[u * 8 + 7])));
+        }
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ dK and dV
+
+struct KvParams {
+  CUtensorMap q[kMaxShards];    // Q_i [T, n_q/t d], box 64 x 128 (MN-major B of dK)
+  CUtensorMap dO[kMaxShards];   // dO_i [T, n_q/t d], box 64 x 128 (A of dP, MN-major B of dV)
+  CUtensorMap v[kMaxShards];    // V_i [T, n_kv/t d], box 64 x 128 (K-major B of dP)
+  CUtensorMap p[kMaxShards];    // P_i as [n_q/t][T][T], box 64 x 128 x 1
+  __nv_bfloat16* dK[kMaxShards];  // [T, n_kv/t d]
+  __nv_bfloat16* dV[kMaxShards];
+  const float* D;                 // rowsum(dO O), [t][n_q/t][T]
+  int t, nql, nkvl, grp, T, ntq;
+  float scale;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+template <int D>
+struct KvCfg {
+  static constexpr int KB = D / 64;
+  static constexpr int V_BYTES = KB * kBKV * 128;         // the CTA's V tile
+  static constexpr int SLOT = KB * kBQ * 128;             // a Q tile or a dO tile
+  static constexpr int P_BYTES = kBQ * kBKV * 2;          // a P tile, overwritten in place by dS
+  static constexpr int OFF_V = 0;
+  static constexpr int OFF_RING = OFF_V + V_BYTES;
+  static constexpr int OFF_P = OFF_RING + kRing * SLOT;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+};
+
+// dK and dV: for every (shard, KV head g, 128-key tile kt), over the pairs (query head c of the
+// group, query tile qt >= kt), with the queries as rows of every score tile:
+//   dP = dO_c V^T (TMEM); the saved P tile arrives by TMA; dV += P^T dO_c reads it as an
+//   MN-major operand; the softmax warps then overwrite it in place with
+//   dS = P (dP - D) / sqrt(d) (zero above the diagonal, where P is zero); dK += dS^T Q_c.
+// Neither P^T nor dS^T is ever formed: the MMAs read the [queries x keys] tiles as MN-major A
+// operands, and the [queries x d] Q and dO tiles loaded K-major double as MN-major B operands.
+// Roles: warp 0 lane 0 loads V once, then dO_j, Q_j through the 4-slot ring; warp 0 lane 1 loads
+// P_j into the two P buffers; warp 1 issues dP_j, dV_j, then dK_(j-1); warps 2..9 compute dS
+// (two per TMEM lane quadrant) and at the end store dK and dV.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kv_kernel(const __grid_constant__ KvParams P) {
+  using C = KvCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sRing = smem + C::OFF_RING;
+  uint8_t* sP = smem + C::OFF_P;
+  uint64_t* v_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* ring_full = v_full + 1;
+  uint64_t* ring_empty = ring_full + kRing;
+  uint64_t* dp_full = ring_empty + kRing;
+  uint64_t* dp_empty = dp_full + 2;
+  uint64_t* pb_full = dp_empty + 2;
+  uint64_t* pb_empty = pb_full + 2;
+  uint64_t* pv_done = pb_empty + 2;
+  uint64_t* ds_full = pv_done + 2;
+  uint64_t* acc_full = ds_full + 2;
+  uint64_t* done_bar = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // Heaviest key tiles first: block b takes key tile b / (t n_kv/t) of KV head b % (t n_kv/t).
+  const int kvheads = P.t * P.nkvl;
+  const int kt = static_cast<int>(blockIdx.x) / kvheads;
+  const int hh = static_cast<int>(blockIdx.x) % kvheads;
+  const int shard = hh / P.nkvl;
+  const int g = hh % P.nkvl;
+  const int k0 = kt * kBKV;
+  const int nqt = P.ntq - kt;               // query tiles kt .. ntq-1
+  const int npairs = nqt * P.grp;           // pair j: query tile kt + j / grp, head g grp + j % grp
+  int* status = P.status;
+  const uint64_t tmo = P.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(v_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 2);   // a dO tile: the dP and the dV MMAs; a Q tile: two commits after dK
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&dp_full[b], 1);
+      mbar_init(&dp_empty[b], 8);
+      mbar_init(&pb_full[b], 1);
+      mbar_init(&pb_empty[b], 1);
+      mbar_init(&pv_done[b], 1);
+      mbar_init(&ds_full[b], 8);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&P.q[shard]);
+    tma_prefetch_map(&P.dO[shard]);
+    tma_prefetch_map(&P.v[shard]);
+    tma_prefetch_map(&P.p[shard]);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- V, then dO_j / Q_j
+      bool ok = true;
+      mbar_arrive_expect_tx(v_full, C::V_BYTES);
+      for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(sV + kb * 16384, &P.v[shard], v_full, g * D + kb * 64, k0);
+      int issued = 0;
+      for (int pos = 0; ok && pos < 2 * npairs; ++pos) {
+        const int slot = pos % kRing;
+        if (!mbar_wait(&ring_empty[slot], (static_cast<uint32_t>(pos / kRing) & 1u) ^ 1u, abort_flag, status, tmo)) {
+          ok = false;
+          break;
+        }
+        const int j = pos >> 1;
+        const int qrow = (kt + j / P.grp) * kBQ;
+        const int c = g * P.grp + j % P.grp;
+        const CUtensorMap* map = (pos & 1) ? &P.q[shard] : &P.dO[shard];   // dO_j at 2j, Q_j at 2j + 1
+        uint8_t* dst = sRing + slot * C::SLOT;
+        mbar_arrive_expect_tx(&ring_full[slot], C::SLOT);
+        for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(dst + kb * 16384, map, &ring_full[slot], c * D + kb * 64, qrow);
+        ++issued;
+      }
+      int dummy_abort = 0;
+      mbar_wait(v_full, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+      const int pending = issued < kRing ? issued : kRing;
+      for (int i = issued - pending; i < issued; ++i)
+        mbar_wait(&ring_full[i % kRing], static_cast<uint32_t>(i / kRing) & 1u,
+                  reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+    } else if (lane == 1) {
+      // ---------------------------------------------------------------- P tiles
+      bool ok = true;
+      int started = 0;
+      for (int j = 0; ok && j < npairs; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
+          ok = false;
+          break;
+        }
+        const int qrow = (kt + j / P.grp) * kBQ;
+        const int c = g * P.grp + j % P.grp;
+        mbar_arrive_expect_tx(&pb_full[b], C::P_BYTES);
+        tma_load_3d(sP + b * C::P_BYTES, &P.p[shard], &pb_full[b], k0, qrow, c);
+        tma_load_3d(sP + b * C::P_BYTES + 16384, &P.p[shard], &pb_full[b], k0 + 64, qrow, c);
+        ++started;
+      }
+      int dummy_abort = 0;
+      for (int b = 0; b < 2; ++b) {
+        const int jl = started - 1 - ((started - 1 - b) & 1);   // last started tile on buffer b
+        if (jl >= 0)
+          mbar_wait(&pb_full[b], static_cast<uint32_t>(jl >> 1) & 1u, reinterpret_cast<volatile int*>(&dummy_abort),
+                    status, tmo);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(v_full, 0, abort_flag, status, tmo);
+      tc_fence_after_sync();
+      const uint32_t vaddr = smem_u32(sV);
+      const uint32_t ring0 = smem_u32(sRing);
+      const uint32_t paddr = smem_u32(sP);
+      const uint32_t idesc_dp = idesc_bf16_f32(kBQ, kBKV, false, false);   // [queries x keys]
+      const uint32_t idesc_acc = idesc_bf16_f32(kBKV, D, true, true);      // [keys x d], A and B MN-major
+      const uint32_t t_dk = tmem_base + 2 * kBKV;
+      const uint32_t t_dv = tmem_base + 2 * kBKV + D;
+      auto wait_pos = [&](int pos) {
+        const int slot = pos % kRing;
+        if (!mbar_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u, abort_flag, status, tmo))
+          return -1;
+        tc_fence_after_sync();
+        return slot;
+      };
+      int qslot_prev = -1;
+      for (int j = 0; ok && j <= npairs; ++j) {
+        if (j < npairs) {
+          const int b = j & 1;
+          // dP_j = dO_j V^T  [queries x keys]
+          const int dslot = wait_pos(2 * j);
+          if (dslot < 0 ||
+              !mbar_wait(&dp_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t daddr = ring0 + dslot * C::SLOT;
+          for (int kb = 0; kb < C::KB; ++kb) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc_sw128(daddr + kb * 16384 + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(vaddr + kb * 16384 + kk * 32, 16, 1024);
+              umma_bf16(tmem_base + b * kBKV, ad, bd, idesc_dp, (kb | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(&dp_full[b]);
+          umma_commit(&ring_empty[dslot]);          // first of the dO tile's two releases
+          // dV += P_j^T dO_j: A = P tile read MN-major (keys contiguous), B = dO tile read MN-major
+          if (!mbar_wait(&pb_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kq = 0; kq < kBQ / 16; ++kq) {   // K = the 128 queries, 16 per MMA
+            const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kq * 2048, 16384, 1024);
+            const uint64_t bd = smem_desc_sw128(daddr + kq * 2048, 16384, 1024);
+            umma_bf16(t_dv, ad, bd, idesc_acc, (j | kq) ? 1u : 0u);
+          }
+          umma_commit(&pv_done[b]);
+          umma_commit(&ring_empty[dslot]);          // second release of the dO tile
+        }
+        if (ok && j > 0) {
+          // dK += dS_(j-1)^T Q_(j-1): A = dS (in the P buffer) MN-major, B = Q tile MN-major
+          const int jp = j - 1;
+          const int b = jp & 1;
+          const int qslot = wait_pos(2 * jp + 1);
+          if (qslot < 0 || !mbar_wait(&ds_full[b], static_cast<uint32_t>(jp >> 1) & 1u, abort_flag, status, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t qaddr = ring0 + qslot * C::SLOT;
+#pragma unroll
+          for (int kq = 0; kq < kBQ / 16; ++kq) {
+            const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kq * 2048, 16384, 1024);
+            const uint64_t bd = smem_desc_sw128(qaddr + kq * 2048, 16384, 1024);
+            umma_bf16(t_dk, ad, bd, idesc_acc, (jp | kq) ? 1u : 0u);
+          }
+          umma_commit(&pb_empty[b]);
+          umma_commit(&ring_empty[qslot]);          // a Q tile is released by two commits
+          umma_commit(&ring_empty[qslot]);
+          qslot_prev = qslot;
+        }
+      }
+      (void)qslot_prev;
+      if (ok) umma_commit(acc_full);
+      umma_commit(done_bar);
+      int dummy_abort = 0;
+      mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ dS warps
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quad * 32 + lane;            // query row within the pair's query tile
+    const float scale = P.scale;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+    bool ok = true;
+    for (int j = 0; ok && j < npairs; ++j) {
+      const int b = j & 1;
+      const int q = (kt + j / P.grp) * kBQ + r;
+      const int c = g * P.grp + j % P.grp;
+      const float Dq = q < P.T ? P.D[(static_cast<int64_t>(shard) * P.nql + c) * P.T + q] : 0.0f;
+      ok = mbar_wait(&dp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64, r0);
+      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64 + 32, r1);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dp_empty[b]);
+      // dV's MMA has read P_j: it may now be overwritten by dS_j
+      ok = mbar_wait(&pv_done[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint8_t* row = my_row + b * C::P_BYTES;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
+        const uint4 pw = *unit;
+        const uint32_t pv[4] = {pw.x, pw.y, pw.z, pw.w};
+        float e8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int col = u * 8 + e;
+          const float dp = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
+          const float p = (e & 1) ? bf16_hi(pv[e >> 1]) : bf16_lo(pv[e >> 1]);
+          e8[e] = (dp - Dq) * (p * scale);   // P is zero above the diagonal
+        }
+        *unit = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
+                           pack_bf16x2(e8[6], e8[7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ds_full[b]);
+    }
+    // dK and dV rows (keys): this warp stores half of the d columns of each
+    if (ok) ok = mbar_wait(acc_full, 0, abort_flag, status, tmo);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after_sync();
+      const int key = k0 + r;
+      const bool key_ok = key < P.T;
+      const int64_t off = static_cast<int64_t>(key_ok ? key : 0) * (P.nkvl * D) + g * D + half * (D / 2);
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        __nv_bfloat16* out = (w == 0 ? P.dK[shard] : P.dV[shard]) + off;
+#pragma unroll
+        for (int cc = 0; cc < D / 2; cc += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(lane_base + 2 * kBKV + w * D + half * (D / 2) + cc, o);
+          tmem_ld_wait();
+          if (key_ok) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(out + cc + u * 8) = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[u * 8 + 0]), __uint_as_float(o[u * 8 + 1])),
+                  pack_bf16x2(__uint_as_float(o[u * 8 + 2]), __uint_as_float(o[u * 8 + 3])),
+                  pack_bf16x2(__uint_as_float(o[u * 8 + 4]), __uint_as_float(o[u * 8 + 5])),
+                  pack_bf16x2(__uint_as_float(o[u * 8 + 6]), __uint_as_float(o[u * 8 + 7])));
+          }
         }
       }
     }
@@ -921,8 +1200,8 @@ int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
 
 
 int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* dO, const void* const* V,
-                  const void* const* K, const void* const* Pin, void* const* dS, void* const* dQ, const float* Drow,
-                  int64_t qc, int64_t kc, cudaStream_t stream) {
+                  const void* const* K, const void* const* Pin, void* const* dQ, const float* Drow, int64_t qc,
+                  int64_t kc, cudaStream_t stream) {
   if (d != 64 && d != 128) return set_error(TTL_ERR_SHAPE, "attention core: head dimension %d is not 64 or 128", d);
   int rc = require_sm103();
   if (rc) return rc;
@@ -933,7 +1212,6 @@ int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
     if (!rc) rc = encode_map_bf16(&p->v[i], V[i], T, kc, kc, 64, 128);
     if (!rc) rc = encode_map_bf16(&p->kmn[i], K[i], T, kc, kc, 64, 64);
     if (!rc) rc = encode_map_bf16_3d(&p->p[i], Pin[i], T, T, nql, T, T * T, 64, 128);
-    if (!rc) rc = encode_map_bf16_3d(&p->ds[i], dS[i], T, T, nql, T, T * T, 64, 128);
     p->dQ[i] = static_cast<__nv_bfloat16*>(dQ[i]);
   }
   if (rc) {
@@ -955,10 +1233,10 @@ int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
   }
   const unsigned blocks = static_cast<unsigned>(t) * nql * p->ntq;
   const double tri = static_cast<double>(T) * (T + 1) / 2.0;
-  // Algorithmic work: dP = dO V^T and dQ = dS K over the causal triangle; bytes: P read, dS
-  // written, dO, V, K read and dQ written once.
+  // Algorithmic work: dP = dO V^T and dQ = dS K over the causal triangle; bytes: P read, dO, V,
+  // K read and dQ written once.
   TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
-                4.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
+                2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
   if (d == 128) {
     static bool attr = false;
     if (!attr) {
@@ -986,6 +1264,76 @@ int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
   }
   delete p;
   return cuda_check(cudaGetLastError(), "attn_bwd_core_kernel launch");
+}
+
+
+int attn_bwd_kv(int t, int64_t T, int nql, int nkvl, int grp, int d, const void* const* Q, const void* const* dO,
+                const void* const* V, const void* const* Pin, void* const* dK, void* const* dV, const float* Drow,
+                int64_t qc, int64_t kc, cudaStream_t stream) {
+  if (d != 64 && d != 128) return set_error(TTL_ERR_SHAPE, "attention core: head dimension %d is not 64 or 128", d);
+  int rc = require_sm103();
+  if (rc) return rc;
+  KvParams* p = new KvParams;
+  std::memset(static_cast<void*>(p), 0, sizeof(KvParams));
+  for (int i = 0; i < t && !rc; ++i) {
+    rc = encode_map_bf16(&p->q[i], Q[i], T, qc, qc, 64, 128);
+    if (!rc) rc = encode_map_bf16(&p->dO[i], dO[i], T, qc, qc, 64, 128);
+    if (!rc) rc = encode_map_bf16(&p->v[i], V[i], T, kc, kc, 64, 128);
+    if (!rc) rc = encode_map_bf16_3d(&p->p[i], Pin[i], T, T, nql, T, T * T, 64, 128);
+    p->dK[i] = static_cast<__nv_bfloat16*>(dK[i]);
+    p->dV[i] = static_cast<__nv_bfloat16*>(dV[i]);
+  }
+  if (rc) {
+    delete p;
+    return rc;
+  }
+  p->D = Drow;
+  p->t = t;
+  p->nql = nql;
+  p->nkvl = nkvl;
+  p->grp = grp;
+  p->T = static_cast<int>(T);
+  p->ntq = static_cast<int>((T + kBQ - 1) / kBQ);
+  p->scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  p->status = device_status_ptr();
+  p->timeout_ns = 2000000000ull;
+  if (!p->status) {
+    delete p;
+    return TTL_ERR_CUDA;
+  }
+  const unsigned blocks = static_cast<unsigned>(t) * nkvl * p->ntq;
+  const double tri = static_cast<double>(T) * (T + 1) / 2.0;
+  // Algorithmic work: dV = P^T dO and dK = dS^T Q over the causal triangle (the dP it recomputes
+  // is not counted); bytes: P read once, Q, dO, V read once, dK and dV written once.
+  TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
+                2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 3.0 * kc) * t);
+  if (d == 128) {
+    static bool attr = false;
+    if (!attr) {
+      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_kv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                KvCfg<128>::SMEM),
+                           "cudaFuncSetAttribute(attn kv core)"))) {
+        delete p;
+        return rc;
+      }
+      attr = true;
+    }
+    attn_bwd_kv_kernel<128><<<blocks, kThreads, KvCfg<128>::SMEM, stream>>>(*p);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_kv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                KvCfg<64>::SMEM),
+                           "cudaFuncSetAttribute(attn kv core)"))) {
+        delete p;
+        return rc;
+      }
+      attr = true;
+    }
+    attn_bwd_kv_kernel<64><<<blocks, kThreads, KvCfg<64>::SMEM, stream>>>(*p);
+  }
+  delete p;
+  return cuda_check(cudaGetLastError(), "attn_bwd_kv_kernel launch");
 }
 
 }  // namespace ttl

@@ -99,16 +99,6 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile, 
   return c;
 }
 
-// Causal structure: the k-block range of one segment (K = queries, rows = keys: the queries
-// before the tile's first key contribute nothing).
-template <int TILE_M>
-__device__ __forceinline__ void seg_kblocks(const Problem& pr, const Seg& sg, const TileCoord& c, int& kb0,
-                                            int& kb1) {
-  kb0 = 0;
-  kb1 = sg.kblocks;
-  if (pr.causal == CAUSAL_K_FROM_ROW) kb0 = min(kb1, (c.tm * TILE_M) / BK);
-}
-
 // ------------------------------------------------------------------ epilogue math
 
 // The epilogue math uses the fast exponential intrinsic: its results are rounded to bf16
@@ -403,9 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
           // [N/2, N) of the MMA (64 of a 128-column one); paired tiles share coordinates.
           const int bn1 = pr.paired ? bn0 : bn0 + (pr.half_n ? BN / 4 : BN / 2);
           const bool b_half = !PAIR && pr.half_n;   // one CTA, 128 columns: no second B box
-          int kb0, kb1;
-          seg_kblocks<C::TILE_M>(pr, sg, c, kb0, kb1);
-          for (int kb = kb0; kb < kb1; ++kb) {
+          for (int kb = 0; kb < sg.kblocks; ++kb) {
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, status, tmo)) {
               ok = false;
               break;
@@ -506,9 +494,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
         const uint32_t b_lbo = pr.b_mn ? 8192u : 16u;
         uint32_t accumulate = 0;
         for (int s = 0; ok && s < pr.nseg; ++s) {
-          int kb0, kb1;
-          seg_kblocks<C::TILE_M>(pr, pr.seg[s], c, kb0, kb1);
-          for (int kb = kb0; kb < kb1; ++kb) {
+          for (int kb = 0; kb < pr.seg[s].kblocks; ++kb) {
             if (!mbar_wait(&full_bar[stage], phase, abort_flag, status, tmo)) {
               ok = false;
               break;
@@ -821,11 +807,8 @@ int GemmBatch::add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b
   s.kblocks = static_cast<int32_t>((K + BK - 1) / BK);
   s.b_n1 = static_cast<int32_t>(b_n1);
   const double ncols = p->paired ? 2.0 * p->N : static_cast<double>(p->N);
-  // A causal problem is square in its token dimension (M = T queries or keys): only the
-  // (T + 1) / (2 T) of it on or below the diagonal is work.
-  const double tri = p->causal != CAUSAL_NONE ? (p->M + 1.0) / (2.0 * p->M) : 1.0;
-  flops_ += 2.0 * p->M * ncols * static_cast<double>(K) * tri;
-  bytes_ += 2.0 * (static_cast<double>(p->M) * K + ncols * K) * tri;
+  flops_ += 2.0 * p->M * ncols * static_cast<double>(K);
+  bytes_ += 2.0 * (static_cast<double>(p->M) * K + ncols * K);
   if (p->nseg == 1) {
     const int nout = p->epi == EPI_SWIGLU_FWD ? 3 : (p->epi == EPI_GELU_FWD || p->epi == EPI_SWIGLU_BWD) ? 2 : 1;
     const int naux = p->epi == EPI_SWIGLU_BWD ? 2 : p->epi == EPI_GELU_BWD ? 1 : 0;

@@ -66,12 +66,6 @@ enum Epilogue : int {
                        // target aux0[row] - ext0 when that column is in the tile
 };
 
-// Causal structure of a problem whose rows or columns are token positions (attention).
-enum Causal : int {
-  CAUSAL_NONE = 0,
-  CAUSAL_K_FROM_ROW = 1,   // rows = keys, K = queries: each segment's K loop starts at the tile's first row
-};
-
 // One K-range of a problem: k-blocks of 64 read from map_a at K offset a_k0 and from
 // map_b (and, for a paired tile, map_b2) at K offset b_k0; b_n1 is added to B's N
 // coordinate for this segment only (e.g. one head's columns of a head-major operand).
@@ -94,7 +88,7 @@ struct Problem {
   uint8_t epi, nseg;
   uint8_t paired;
   uint8_t join;           // 1 = same tile group as the previous problem (shares its A rows)
-  uint8_t causal;         // CAUSAL_*: work a lower-triangular (query x key) structure skips
+  uint8_t pad0;
   uint8_t half_n;         // set by launch() when N <= 128 (unpaired): the MMAs are 128 columns wide
   Seg seg[kMaxSegs];
   void* out0;
@@ -150,7 +144,6 @@ class GemmBatch {
   // join = true puts the problem in the previous problem's tile group; use it when both
   // read the same A rows (same A tensor, same a_m0, same M).
   Problem* add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired, bool join = false);
-  // Set p->causal before adding its segments: the FLOP and byte counts of the trace follow it.
   int add_seg(Problem* p, int map_a, int64_t a_k0, int map_b, int map_b2, int64_t b_k0, int64_t K,
               int64_t b_n1 = 0);
   int launch(cudaStream_t stream);
@@ -188,19 +181,23 @@ int encode_map_bf16_3d(CUtensorMap* out, const void* ptr, int64_t d0, int64_t d1
 
 // Forward core of the head-split attention block for t shards (one kernel launch): from Q_i
 // [T, qc], K_i and V_i [T, kc] (qc = nql d, kc = nql d / grp) writes the probabilities P_i
-// [nql, T, T] (rows up to key min(T, round_up(q + 1, 256)), zeros above the diagonal) and
+// [nql, T, T] (row q up to key min(T, round_up(q + 1, 128)), zeros above the diagonal) and
 // O_i [T, qc].  d is 64 or 128.
 int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* Q, const void* const* K,
                   const void* const* V, void* const* Pout, void* const* Oout, int64_t qc, int64_t kc,
                   cudaStream_t stream);
 
-// Backward core of the head-split attention block (one launch): from dO_i [T, qc], V_i, K_i
-// [T, kc], the saved P_i [nql, T, T] and D = rowsum(dO O) [t][nql][T] (fp32) writes
-// dS_i = P (dO V^T - D) / sqrt(d) [nql, T, T] (same written span and zeros as P) and
-// dQ_i = dS K [T, qc].  d is 64 or 128.
+// Backward cores of the head-split attention block (one launch each), from dO_i [T, qc],
+// V_i, K_i [T, kc], Q_i [T, qc], the saved P_i [nql, T, T] and D = rowsum(dO O) [t][nql][T]
+// (fp32): attn_bwd_core writes dQ_i = dS K [T, qc] with dS = P (dO V^T - D) / sqrt(d);
+// attn_bwd_kv writes dK_i = sum over the group's heads of dS^T Q and dV_i = sum of P^T dO
+// ([T, kc]).  Neither writes dS.  d is 64 or 128.
 int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* dO, const void* const* V,
-                  const void* const* K, const void* const* Pin, void* const* dS, void* const* dQ, const float* Drow,
-                  int64_t qc, int64_t kc, cudaStream_t stream);
+                  const void* const* K, const void* const* Pin, void* const* dQ, const float* Drow, int64_t qc,
+                  int64_t kc, cudaStream_t stream);
+int attn_bwd_kv(int t, int64_t T, int nql, int nkvl, int grp, int d, const void* const* Q, const void* const* dO,
+                const void* const* V, const void* const* Pin, void* const* dK, void* const* dV, const float* Drow,
+                int64_t qc, int64_t kc, cudaStream_t stream);
 
 // Zero-fill helper (used where a contraction is empty).
 int fill_zero(void* ptr, size_t bytes, cudaStream_t stream);

@@ -132,8 +132,8 @@ def test_attention_validation(lib):
     assert call(2, 0, 64, 8, 2, 128) == 0            # no tokens: nothing to do
     # the fused forward keeps scores and statistics on chip
     assert lib.ttl_tp_attn_fwd_workspace_size(2, 64, 8, 2, 128) == 0
-    # D per row (fp32), then per shard dS [4, 64, 64] bf16, dO, dQ [64, 512], dK, dV [64, 128]
-    per = 4 * 64 * 64 * 2 + 2 * (64 * 512 * 2) + 2 * (64 * 128 * 2)
+    # D per row (fp32), then per shard dO, dQ [64, 512], dK, dV [64, 128]
+    per = 2 * (64 * 512 * 2) + 2 * (64 * 128 * 2)
     assert lib.ttl_tp_attn_bwd_workspace_size(2, 64, 8, 2, 128) == 512 * 4 + 2 * per
     assert lib.ttl_tp_attn_bwd_workspace_size(3, 64, 8, 2, 128) == 0    # invalid shape
     bwd = lib.ttl_tp_attn_bwd

@@ -66,10 +66,11 @@ def _W64(inp):
 
 
 def _check_p_band(P, T):
-    """Row q of every head's P is zero for q < j < min(T, round_up(q + 1, 256))."""
+    """Row q of every head's P is zero for q < j < min(T, round_up(q + 1, 128)) (the rest of
+    its query tile's diagonal tile)."""
     j = torch.arange(T, device=P.device)
     q = j[:, None]
-    band = (j[None, :] > q) & (j[None, :] < torch.clamp((q // 256 + 1) * 256, max=T))
+    band = (j[None, :] > q) & (j[None, :] < torch.clamp((q // 128 + 1) * 128, max=T))
     assert torch.all(P[:, band] == 0)
 
 
@@ -184,7 +185,7 @@ def test_qwen3_forward_sampled_rows(qwen3):
     for i in (0, s.t - 1):
         Ps = fwd["P"][i][:, rows, :].float()
         for r, q in enumerate(rows):
-            z = min(s.T, (q // 256 + 1) * 256)
+            z = min(s.T, (q // 128 + 1) * 128)
             assert torch.all((Ps[:, r, :q + 1].sum(-1) - 1).abs() < 1e-2)
             assert torch.all(Ps[:, r, q + 1:z] == 0)
     del fwd
