@@ -492,6 +492,14 @@ struct BwdCfg {
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
 };
 
+// Asks L2 to fetch one box ahead of its load (HBM latency hidden without shared memory).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                             int z) {
   asm volatile(
@@ -613,8 +621,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
       // ---------------------------------------------------------------- P tiles
       bool ok = true;
       int started = 0;   // P tiles whose load was issued
+      for (int j = 0; j < 2 && j < ntiles; ++j) {
+        tma_prefetch_3d(&P.p[shard], j * kBKV, q0, c);
+        tma_prefetch_3d(&P.p[shard], j * kBKV + 64, q0, c);
+      }
       for (int j = 0; ok && j < ntiles; ++j) {
         const int b = j & 1;
+        if (j + 2 < ntiles) {   // two tiles ahead into L2
+          tma_prefetch_3d(&P.p[shard], (j + 2) * kBKV, q0, c);
+          tma_prefetch_3d(&P.p[shard], (j + 2) * kBKV + 64, q0, c);
+        }
         if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
@@ -929,8 +945,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kv_kernel(const __grid_c
       // ---------------------------------------------------------------- P tiles
       bool ok = true;
       int started = 0;
+      auto prefetch_pair = [&](int j) {
+        const int qrow = (kt + j / P.grp) * kBQ;
+        const int c = g * P.grp + j % P.grp;
+        tma_prefetch_3d(&P.p[shard], k0, qrow, c);
+        tma_prefetch_3d(&P.p[shard], k0 + 64, qrow, c);
+      };
+      for (int j = 0; j < 2 && j < npairs; ++j) prefetch_pair(j);
       for (int j = 0; ok && j < npairs; ++j) {
         const int b = j & 1;
+        if (j + 2 < npairs) prefetch_pair(j + 2);   // two pairs ahead into L2
         if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
