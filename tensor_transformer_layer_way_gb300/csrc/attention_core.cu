@@ -245,39 +245,61 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
         const int slot = wait_pos(j);
         ok = slot >= 0 && issue_s(slot);
       }
-      // pass 2: S_j (K_j at position n + 2j), then P_(j-1) V_(j-1) (V_(j-1) at n + 2j - 1): each V
-      // is waited for just before its own P V, two iterations after its load could start
-      for (int j = 0; ok && j <= ntiles; ++j) {
-        if (j < ntiles) {
-          const int kslot = wait_pos(ntiles + 2 * j);
-          ok = kslot >= 0 && issue_s(kslot);
+      // pass 2: issue whichever is ready first -- the next score tile S_ns (K_ns at ring position
+      // n + 2 ns, a free score buffer) or the next P_np V_np (V_np at n + 2 np + 1, P_np written)
+      // -- so that a P V never waits behind a late K tile, nor an S behind a late softmax.
+      int ns = 0, np = 0;
+      uint64_t t_idle = globaltimer_ns();
+      while (ok && np < ntiles) {
+        bool progress = false;
+        if (ns < ntiles) {
+          const int pos = ntiles + 2 * ns;
+          const int slot = pos % kRing;
+          const int b = sj & 1;
+          if (mbar_test_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u) &&
+              mbar_test_wait(&s_empty[b], (static_cast<uint32_t>(sj >> 1) & 1u) ^ 1u)) {
+            tc_fence_after_sync();
+            ok = issue_s(slot);   // both conditions hold: no wait inside
+            ++ns;
+            progress = true;
+          }
         }
-        if (ok && j > 0) {
-          const int jp = j - 1;
-          const int b = jp & 1;
-          const int vslot = wait_pos(ntiles + 2 * jp + 1);
-          if (vslot < 0 || !mbar_wait(&p_full[b], static_cast<uint32_t>(jp >> 1) & 1u, abort_flag, status, tmo)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          // P_jp -> HBM: two 64-key boxes straight from the MMA's A operand tile
-          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, jp * kBKV, q0, c);
-          tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, jp * kBKV + 64, q0, c);
-          bulk_commit_group();
-          const uint32_t vaddr = ring0 + vslot * C::SLOT;
-          for (int kk2 = 0; kk2 < 2; ++kk2) {          // 64-key blocks
+        if (ok && np < ns) {
+          const int pos = ntiles + 2 * np + 1;
+          const int vslot = pos % kRing;
+          const int b = np & 1;
+          if (mbar_test_wait(&ring_full[vslot], static_cast<uint32_t>(pos / kRing) & 1u) &&
+              mbar_test_wait(&p_full[b], static_cast<uint32_t>(np >> 1) & 1u)) {
+            tc_fence_after_sync();
+            // P_np -> HBM: two 64-key boxes straight from the MMA's A operand tile
+            tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, np * kBKV, q0, c);
+            tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, np * kBKV + 64, q0, c);
+            bulk_commit_group();
+            const uint32_t vaddr = ring0 + vslot * C::SLOT;
+            for (int kk2 = 0; kk2 < 2; ++kk2) {          // 64-key blocks
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kk2 * 16384 + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(vaddr + kk2 * C::KB * 8192 + kk * 2048, 8192, 1024);
-              umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_o, (jp | kk2 | kk) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kk2 * 16384 + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(vaddr + kk2 * C::KB * 8192 + kk * 2048, 8192, 1024);
+                umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_o, (np | kk2 | kk) ? 1u : 0u);
+              }
             }
+            umma_commit(&ring_empty[vslot]);
+            umma_commit(&p_empty[b]);                  // first arrival: the MMAs have read P_np
+            bulk_wait_group_read<1>();                 // the store of P_(np-1) has read its buffer
+            if (np > 0) mbar_arrive(&p_empty[(np - 1) & 1]);
+            ++np;
+            progress = true;
           }
-          umma_commit(&ring_empty[vslot]);
-          umma_commit(&p_empty[b]);                  // first arrival: the MMAs have read P_jp
-          bulk_wait_group_read<1>();                 // the store of P_(jp-1) has read its buffer
-          if (jp > 0) mbar_arrive(&p_empty[(jp - 1) & 1]);
+        }
+        if (progress) {
+          t_idle = globaltimer_ns();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (globaltimer_ns() - t_idle > tmo) {
+          if (status) atomicCAS(status, 0, TTL_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
         }
       }
       bulk_wait_group_read<0>();
