@@ -9,7 +9,7 @@
 // Two passes over the key tiles 0..qt of query tile qt (128 keys each):
 //   pass 1: S = Q K^T (tcgen05, fp32 in TMEM); per row the max and the sum of 2^(s log2e/sqrt(d) - max)
 //           over the keys <= the query -- exact row statistics, so P needs no later rescaling;
-//   pass 2: S again; P = 2^(s log2e/sqrt(d) - M) / sum as bf16, written to shared memory (the A
+//   pass 2: S again; P = 2^(s log2e/sqrt(d) - M - log2 sum) as bf16, written to shared memory (the A
 //           operand of the next MMA) and to HBM (saved for the backward); O += P V in TMEM.
 // The probabilities the backward reads are therefore written once; nothing re-reads them here.
 //
@@ -394,8 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       l = L;
     }
     named_bar_sync(1, 256);   // every half has read the exchange before P overwrites it
-    const float nm = -m;
-    const float inv_l = 1.0f / l;
+    // P = 2^(s k - m) / l = 2^(s k - (m + log2 l)): the normalisation rides in the exponent.  A row
+    // past the end of the sequence (never stored) gets finite values.
+    const float nm = row_ok ? -(m + __log2f(l)) : 0.0f;
     // pass 2: probabilities, into the P buffer the MMA warp feeds to P V and stores to HBM
     uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
     for (int j = 0; ok && j < ntiles; ++j, ++sj) {
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int col = u * 8 + e;
-            e8[e] = ex2_approx(fmaf(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]), k, nm)) * inv_l;
+            e8[e] = ex2_approx(fmaf(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]), k, nm));
           }
           w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
                             pack_bf16x2(e8[6], e8[7]));
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
           for (int e = 0; e < 8; ++e) {
             const int col = u * 8 + e;
             const float s = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
-            e8[e] = col < nv ? ex2_approx(fmaf(s, k, nm)) * inv_l : 0.0f;
+            e8[e] = col < nv ? ex2_approx(fmaf(s, k, nm)) : 0.0f;
           }
           w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
                             pack_bf16x2(e8[6], e8[7]));
