@@ -9,8 +9,9 @@
 // Two passes over the key tiles 0..qt of query tile qt (128 keys each):
 //   pass 1: S = Q K^T (tcgen05, fp32 in TMEM); per row the max and the sum of 2^(s log2e/sqrt(d) - max)
 //           over the keys <= the query -- exact row statistics, so P needs no later rescaling;
-//   pass 2: S again; P = 2^(s log2e/sqrt(d) - M - log2 sum) as bf16, written to shared memory (the A
-//           operand of the next MMA) and to HBM (saved for the backward); O += P V in TMEM.
+//   pass 2: S again; P = 2^(s log2e/sqrt(d) - M - log2 sum) as bf16, written to tensor memory (the
+//           A operand of O += P V) and to a shared tile that a TMA store writes to HBM (saved
+//           for the backward).
 // The probabilities the backward reads are therefore written once; nothing re-reads them here.
 //
 // Roles (320 threads): warp 0 issues TMA loads (Q once; then K_0..K_n-1 for pass 1 and K_0, V_0,
@@ -20,8 +21,10 @@
 // tile j overlaps the previous tile's P V.  Every wait is bounded (TTL_ERR_TIMEOUT on expiry).
 //
 // Layouts: Q, K tiles K-major (d contiguous, 64-column 128-byte-swizzled boxes of 128 rows);
-// V tiles MN-major (64 d x 64 keys boxes); P tiles K-major like Q; TMEM columns [0,128) and
-// [128,256) are the two score buffers, [256, 256 + d) the O accumulator.
+// V tiles MN-major (64 d x 64 keys boxes).  TMEM columns [0,128) and [128,256) are the two score
+// buffers, [256, 256 + d) the O accumulator, [384,448) and [448,512) the two P buffers (bf16,
+// keys 2i and 2i + 1 in column i).  The MMAs here are bound by shared-memory bandwidth, so P V
+// reads P from tensor memory; the shared copy of P only feeds the coalesced TMA store.
 
 #include <cmath>
 #include <cstring>
@@ -55,8 +58,8 @@ struct CoreCfg {
   static constexpr int KB = D / 64;                       // 64-wide d blocks
   static constexpr int Q_BYTES = KB * kBQ * 128;          // 16 KiB per d block
   static constexpr int SLOT = KB * kBKV * 128;            // a K tile or a V tile
-  static constexpr int P_BYTES = kBQ * kBKV * 2;          // 32 KiB
   static constexpr int OFF_Q = 0;
+  static constexpr int P_BYTES = kBQ * kBKV * 2;          // 32 KiB: a P tile on its way to HBM
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
   static constexpr int OFF_P = OFF_RING + kRing * SLOT;
   // float2 [2][128] row-statistics exchange between the two passes, in the P buffers (which
@@ -65,6 +68,10 @@ struct CoreCfg {
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;       // barriers + alignment slack
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+  // tensor memory: two score buffers, O, two P buffers (bf16, two per 32-bit column)
+  static constexpr int T_O = 2 * kBKV;
+  static constexpr int T_P = 2 * kBKV + 128;
+  static_assert(T_P + 2 * (kBKV / 2) <= kTmemCols, "tensor memory layout");
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -139,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], 8);   // every softmax warp
       mbar_init(&p_full[b], 8);
-      mbar_init(&p_empty[b], 2);   // the P V MMAs and the TMA store of the tile have both read it
+      mbar_init(&p_empty[b], 2);   // the P V MMAs (TMEM P) and the TMA store (shared P) have read it
     }
     mbar_init(o_full, 1);
     mbar_init(done_bar, 1);
@@ -209,7 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       tc_fence_after_sync();
       const uint32_t qaddr = smem_u32(sQ);
       const uint32_t ring0 = smem_u32(sRing);
-      const uint32_t paddr = smem_u32(sP);
       const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKV, false, false);
       const uint32_t idesc_o = idesc_bf16_f32(kBQ, D, false, true);
       int sj = 0;            // S tiles issued (both passes), selects the score buffer
@@ -271,17 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
           if (mbar_test_wait(&ring_full[vslot], static_cast<uint32_t>(pos / kRing) & 1u) &&
               mbar_test_wait(&p_full[b], static_cast<uint32_t>(np >> 1) & 1u)) {
             tc_fence_after_sync();
-            // P_np -> HBM: two 64-key boxes straight from the MMA's A operand tile
+            // P_np -> HBM: two 64-key boxes of the shared copy
             tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, np * kBKV, q0, c);
             tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, np * kBKV + 64, q0, c);
             bulk_commit_group();
+            // O += P_np V_np with P from tensor memory (A operand, 8 columns per 16 keys)
             const uint32_t vaddr = ring0 + vslot * C::SLOT;
             for (int kk2 = 0; kk2 < 2; ++kk2) {          // 64-key blocks
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kk2 * 16384 + kk * 32, 16, 1024);
+                const uint32_t at = tmem_base + C::T_P + b * (kBKV / 2) + (kk2 * 4 + kk) * 8;
                 const uint64_t bd = smem_desc_sw128(vaddr + kk2 * C::KB * 8192 + kk * 2048, 8192, 1024);
-                umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_o, (np | kk2 | kk) ? 1u : 0u);
+                umma_bf16_ts(tmem_base + C::T_O, at, bd, idesc_o, (np | kk2 | kk) ? 1u : 0u);
               }
             }
             umma_commit(&ring_empty[vslot]);
@@ -397,8 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
     // P = 2^(s k - m) / l = 2^(s k - (m + log2 l)): the normalisation rides in the exponent.  A row
     // past the end of the sequence (never stored) gets finite values.
     const float nm = row_ok ? -(m + __log2f(l)) : 0.0f;
-    // pass 2: probabilities, into the P buffer the MMA warp feeds to P V and stores to HBM
+    // pass 2: probabilities, into the TMEM P buffer the MMA warp feeds to P V, and into a
+    // 128-byte-swizzled shared tile that the MMA warp stores to HBM by TMA
     uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+    const uint32_t p_tmem = lane_base + C::T_P + half * 32;
     for (int j = 0; ok && j < ntiles; ++j, ++sj) {
       const int b = sj & 1;
       ok = mbar_wait(&s_full[b], static_cast<uint32_t>(sj >> 1) & 1u, abort_flag, status, tmo);
@@ -415,43 +424,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);
       const int nv = q - (j * kBKV + half * 64) + 1;
-      uint4 w[8];
+      uint32_t w[32];   // keys 2i, 2i + 1 of this warp's 64 in word i
       if (nv >= 64) {   // below the diagonal: no mask
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float e8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = u * 8 + e;
-            e8[e] = ex2_approx(fmaf(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]), k, nm));
-          }
-          w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
-                            pack_bf16x2(e8[6], e8[7]));
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t a0 = i < 16 ? r0[2 * i] : r1[2 * i - 32];
+          const uint32_t a1 = i < 16 ? r0[2 * i + 1] : r1[2 * i - 31];
+          w[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(a0), k, nm)), ex2_approx(fmaf(__uint_as_float(a1), k, nm)));
         }
       } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float e8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = u * 8 + e;
-            const float s = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
-            e8[e] = col < nv ? ex2_approx(fmaf(s, k, nm)) : 0.0f;
-          }
-          w[u] = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
-                            pack_bf16x2(e8[6], e8[7]));
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t a0 = i < 16 ? r0[2 * i] : r1[2 * i - 32];
+          const uint32_t a1 = i < 16 ? r0[2 * i + 1] : r1[2 * i - 31];
+          w[i] = pack_bf16x2(2 * i < nv ? ex2_approx(fmaf(__uint_as_float(a0), k, nm)) : 0.0f,
+                             2 * i + 1 < nv ? ex2_approx(fmaf(__uint_as_float(a1), k, nm)) : 0.0f);
         }
       }
-      // the P buffer is free once the P V and the store that read it two tiles ago are done
+      // the P buffers are free once the P V and the store that read them two tiles ago are done
       const int pb = j & 1;
       ok = mbar_wait(&p_empty[pb], static_cast<uint32_t>((j >> 1) & 1) ^ 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
+      tc_fence_after_sync();
+      tmem_st_32x32b_x32(p_tmem + pb * (kBKV / 2), w);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(my_row + pb * C::P_BYTES + ((u ^ (r & 7)) << 4)) = w[u];
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(my_row + pb * C::P_BYTES + ((u ^ (r & 7)) << 4)) =
+            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
     }
@@ -463,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
 #pragma unroll
       for (int cc = 0; cc < D / 2; cc += 32) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(lane_base + 2 * kBKV + half * (D / 2) + cc, o);
+        tmem_ld_32x32b_x32(lane_base + C::T_O + half * (D / 2) + cc, o);
         tmem_ld_wait();
         if (row_ok) {
 #pragma unroll
