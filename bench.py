@@ -437,6 +437,43 @@ def bench_gtp(ttl, torch, dev, pk, args):
                     "finalize_gbs": round(sum(r[3] for r in fi) / (sum(r[1] for r in fi) * 1e-3) / 1e9, 1) if fi else None}
         if ga:
             res[key]["gather_gbs"] = round(sum(r[3] for r in ga) / (sum(r[1] for r in ga) * 1e-3) / 1e9, 1)
+    # The gather kernel alone (in the chain it shares HBM with the GEMM it hides behind): the
+    # L layers' shards gathered back to back into L distinct slots on this stream (512 MiB of
+    # traffic, beyond L2), L2 flushed before each repetition, median of 5.
+    flush = [torch.zeros(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev) for _ in range(2)]
+    dst = [torch.empty((K, N), device=dev, dtype=torch.bfloat16) for _ in range(L)]
+    gather_bytes = L * 2.0 * K * N * 2
+    times = []
+    for _ in range(5):
+        _flush(torch, flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for l in range(L):
+            ttl.gtp_gather(shards[l], dst[l])
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = sorted(times)[len(times) // 2]
+    # the same bytes moved by torch's own device copy (one contiguous [K, N] source per layer),
+    # timed the same way: the ceiling for copies of this size
+    src = [torch.empty((K, N), device=dev, dtype=torch.bfloat16) for _ in range(L)]
+    ctimes = []
+    for _ in range(5):
+        _flush(torch, flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for l in range(L):
+            dst[l].copy_(src[l])
+        e1.record()
+        torch.cuda.synchronize()
+        ctimes.append(e0.elapsed_time(e1))
+    cms = sorted(ctimes)[len(ctimes) // 2]
+    res["gather_isolated"] = {"us_per_layer": round(ms * 1e3 / L, 1),
+                              "gbs": round(gather_bytes / (ms * 1e-3) / 1e9, 1),
+                              "frac": round(gather_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                              "torch_copy_same_bytes_gbs": round(gather_bytes / (cms * 1e-3) / 1e9, 1),
+                              "bytes": gather_bytes, "l2": "flushed before each repetition of the 8 launches"}
+    del flush, dst, src
     res["peak_tflops"] = pk["bf16_tflops_sustained"]
     res["peak_gbs"] = pk["hbm_gbs"]
     del X, shards, dY, Y, dX, slots, staging, main_grad, runner

@@ -156,7 +156,23 @@ struct DlogitsShards {
   __nv_bfloat16* d[kMaxShards];
 };
 
-// grid (T, t): dZ = (exp(z - lse) - onehot) / T.
+// One float4 of logits (columns 4k..4k+3) -> dZ.
+__device__ __forceinline__ void ce_dlogits_vec(float4 v, int64_t k, float* row, __nv_bfloat16* drow, float L,
+                                               float invT, int64_t tg, int write_f32) {
+  float r[4] = {__expf(v.x - L), __expf(v.y - L), __expf(v.z - L), __expf(v.w - L)};
+  const int64_t c0 = k * 4;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) r[q] = (r[q] - (tg == c0 + q ? 1.0f : 0.0f)) * invT;
+  uint2 packed;
+  packed.x = pack_bf16x2(r[0], r[1]);
+  packed.y = pack_bf16x2(r[2], r[3]);
+  __stcs(reinterpret_cast<uint2*>(drow) + k, packed);
+  if (write_f32) __stcs(reinterpret_cast<float4*>(row) + k, make_float4(r[0], r[1], r[2], r[3]));
+}
+
+// grid (T, t): dZ = (exp(z - lse) - onehot) / T.  Each thread issues kDlU independent 16-byte
+// loads before it computes, so enough bytes are in flight to cover HBM latency.
+constexpr int kDlU = 4;
 __global__ void __launch_bounds__(256) ce_dlogits_kernel(const __grid_constant__ DlogitsShards S, const int64_t* target, int64_t T,
                                                          int64_t Vs, const float* lse, int write_f32) {
   const int64_t tok = blockIdx.x;
@@ -167,19 +183,16 @@ __global__ void __launch_bounds__(256) ce_dlogits_kernel(const __grid_constant__
   const float invT = 1.0f / static_cast<float>(T);
   const int64_t tg = target[tok] - static_cast<int64_t>(i) * Vs;
   const int64_t n4 = Vs / 4;
-  for (int64_t k = threadIdx.x; k < n4; k += blockDim.x) {
-    float4 v = __ldcs(reinterpret_cast<const float4*>(row) + k);
-    float r[4] = {__expf(v.x - L), __expf(v.y - L), __expf(v.z - L), __expf(v.w - L)};
-    const int64_t c0 = k * 4;
-    if (tg >= c0 && tg < c0 + 4) r[tg - c0] -= 1.0f;
+  const int64_t step = blockDim.x;
+  int64_t k = threadIdx.x;
+  for (; k + (kDlU - 1) * step < n4; k += kDlU * step) {
+    float4 v[kDlU];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) r[q] *= invT;
-    uint2 packed;
-    packed.x = pack_bf16x2(r[0], r[1]);
-    packed.y = pack_bf16x2(r[2], r[3]);
-    __stcs(reinterpret_cast<uint2*>(drow) + k, packed);
-    if (write_f32) __stcs(reinterpret_cast<float4*>(row) + k, make_float4(r[0], r[1], r[2], r[3]));
+    for (int u = 0; u < kDlU; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(row) + k + u * step);
+#pragma unroll
+    for (int u = 0; u < kDlU; ++u) ce_dlogits_vec(v[u], k + u * step, row, drow, L, invT, tg, write_f32);
   }
+  for (; k < n4; k += step) ce_dlogits_vec(__ldcs(reinterpret_cast<const float4*>(row) + k), k, row, drow, L, invT, tg, write_f32);
 }
 
 }  // namespace ttl

@@ -24,16 +24,26 @@ struct GatherSet {
   const uint4* p[kMaxShards];
 };
 
-// slot vector v belongs to shard v / vps at offset v % vps (16-byte vectors).
+// Block b of a grid of G handles the contiguous vector range [b n / G, (b + 1) n / G): every
+// block gets the same work, so a launch that is all one wave has no tail.
+__device__ __forceinline__ void block_range(int64_t n, int64_t& begin, int64_t& end) {
+  const int64_t per = (n + gridDim.x - 1) / gridDim.x;
+  begin = static_cast<int64_t>(blockIdx.x) * per;
+  end = begin + per < n ? begin + per : n;
+}
+
+// slot vector v belongs to shard v / vps at offset v % vps (16-byte vectors).  Each thread keeps
+// U independent loads in flight.
 __global__ void __launch_bounds__(256) gtp_gather_kernel(const __grid_constant__ GatherSet S, uint4* slot, int64_t nvec, int64_t vps) {
   constexpr int U = 4;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * U + threadIdx.x; base < nvec; base += step) {
+  int64_t begin, end;
+  block_range(nvec, begin, end);
+  for (int64_t base = begin + threadIdx.x; base < end; base += static_cast<int64_t>(blockDim.x) * U) {
     uint4 x[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t v = base + static_cast<int64_t>(u) * blockDim.x;
-      if (v < nvec) {
+      if (v < end) {
         const int j = static_cast<int>(v / vps);
         x[u] = __ldcs(S.p[j] + (v - j * vps));
       }
@@ -41,7 +51,7 @@ __global__ void __launch_bounds__(256) gtp_gather_kernel(const __grid_constant__
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t v = base + static_cast<int64_t>(u) * blockDim.x;
-      if (v < nvec) slot[v] = x[u];
+      if (v < end) slot[v] = x[u];
     }
   }
 }
@@ -53,26 +63,28 @@ struct FinalizeSet {
 
 // main_grad[j] += staging[j] over g shards of nvec4_per float4 vectors each.
 __global__ void __launch_bounds__(256) gtp_finalize_kernel(const __grid_constant__ FinalizeSet S, int g, int64_t nvec4_per) {
+  constexpr int U = 4;
   const int64_t total = nvec4_per * g;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * 2;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * 2 + threadIdx.x; base < total; base += step) {
-    float4 a[2], b[2];
-    int j[2];
-    int64_t o[2];
+  int64_t begin, end;
+  block_range(total, begin, end);
+  for (int64_t base = begin + threadIdx.x; base < end; base += static_cast<int64_t>(blockDim.x) * U) {
+    float4 a[U], b[U];
+    int j[U];
+    int64_t o[U];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t v = base + static_cast<int64_t>(u) * blockDim.x;
-      j[u] = v < total ? static_cast<int>(v / nvec4_per) : 0;
+      j[u] = v < end ? static_cast<int>(v / nvec4_per) : 0;
       o[u] = v - j[u] * nvec4_per;
-      if (v < total) {
+      if (v < end) {
         a[u] = S.mg[j[u]][o[u]];
         b[u] = __ldcs(S.st[j[u]] + o[u]);
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t v = base + static_cast<int64_t>(u) * blockDim.x;
-      if (v < total) {
+      if (v < end) {
         float4 r = a[u];
         r.x += b[u].x;
         r.y += b[u].y;
@@ -86,10 +98,22 @@ __global__ void __launch_bounds__(256) gtp_finalize_kernel(const __grid_constant
 
 namespace {
 
-unsigned grid_for(int64_t n, int per_thread) {
-  const int64_t want = (n + 256LL * per_thread - 1) / (256LL * per_thread);
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+// One wave of 256-thread blocks (as many per SM as the kernel's registers allow, from the
+// occupancy query), fewer if n is small; the kernels split n evenly over the blocks.
+unsigned grid_for(int64_t n, int blocks_per_sm) {
+  const int64_t want = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * blocks_per_sm;
   return static_cast<unsigned>(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+template <typename Kernel>
+int resident_blocks(Kernel kernel) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = 1;
+  }
+  return n;
 }
 
 int check_shards(int g, const void* const* arr, const char* what) {
@@ -123,7 +147,8 @@ int finalize(int g, int64_t rows, int64_t N, const float* const* staging, float*
   }
   const int64_t n4 = rows * N / 4;
   TraceScope trace(s, TTL_K_FINALIZE, 0.0, 3.0 * 16.0 * static_cast<double>(n4) * g);
-  gtp_finalize_kernel<<<grid_for(n4 * g, 2), 256, 0, s>>>(S, g, n4);
+  static const int bps = resident_blocks(gtp_finalize_kernel);
+  gtp_finalize_kernel<<<grid_for(n4 * g, bps), 256, 0, s>>>(S, g, n4);
   return cuda_check(cudaGetLastError(), "gtp_finalize_kernel launch");
 }
 
@@ -148,7 +173,8 @@ extern "C" int ttl_gtp_gather(int g, int64_t K, int64_t N, const ttl_bf16* const
     for (int j = 0; j < g; ++j) S.p[j] = reinterpret_cast<const uint4*>(shards[j]);
     const int64_t nvec = K * N / 8;
     TraceScope trace(s, TTL_K_GTP_GATHER, 0.0, 2.0 * 16.0 * static_cast<double>(nvec));
-    gtp_gather_kernel<<<grid_for(nvec, 4), 256, 0, s>>>(S, reinterpret_cast<uint4*>(slot), nvec, nvec / g);
+    static const int bps = resident_blocks(gtp_gather_kernel);
+    gtp_gather_kernel<<<grid_for(nvec, bps), 256, 0, s>>>(S, reinterpret_cast<uint4*>(slot), nvec, nvec / g);
     if ((rc = cuda_check(cudaGetLastError(), "gtp_gather_kernel launch"))) return rc;
   }
   if (done_event) return cuda_check(cudaEventRecord(static_cast<cudaEvent_t>(done_event), s), "cudaEventRecord");
