@@ -28,6 +28,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "ttl_device.cuh"
 #include "ttl_internal.h"
@@ -396,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
     {
       const float2 o = xch[(1 - half) * kBQ + r];
       const float M = fmaxf(m, o.x);
-      const float L = (m == -INFINITY ? 0.0f : l * ex2_approx(m - M)) + (o.x == -INFINITY ? 0.0f : o.y * ex2_approx(o.x - M));
+      const float L = (m == -INFINITY ? 0.0f : l * ex2_approx(m - M)) +
+                      (o.x == -INFINITY ? 0.0f : o.y * ex2_approx(o.x - M));
       m = M;
       l = L;
     }
@@ -430,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
         for (int i = 0; i < 32; ++i) {
           const uint32_t a0 = i < 16 ? r0[2 * i] : r1[2 * i - 32];
           const uint32_t a1 = i < 16 ? r0[2 * i + 1] : r1[2 * i - 31];
-          w[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(a0), k, nm)), ex2_approx(fmaf(__uint_as_float(a1), k, nm)));
+          w[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(a0), k, nm)),
+                             ex2_approx(fmaf(__uint_as_float(a1), k, nm)));
         }
       } else {
 #pragma unroll
@@ -1184,6 +1187,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kv_kernel(const __grid_c
 
 }  // namespace
 
+// Raises a core kernel's dynamic shared-memory limit, once per kernel and device (thread-safe).
+enum CoreKernelSlot { kFwd128, kFwd64, kBwd128, kBwd64, kKv128, kKv64, kCoreKernelSlots };
+constexpr int kMaxCoreDevices = 64;
+static int set_core_smem(const void* fn, int slot, int bytes, const char* what) {
+  static std::mutex mu;
+  static bool done[kCoreKernelSlots][kMaxCoreDevices] = {};
+  int dev = 0;
+  int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= kMaxCoreDevices) return set_error(TTL_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[slot][dev]) return TTL_OK;
+  rc = cuda_check(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), what);
+  if (!rc) done[slot][dev] = true;
+  return rc;
+}
+
 int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* Q, const void* const* K,
                   const void* const* V, void* const* Pout, void* const* Oout, int64_t qc, int64_t kc,
                   cudaStream_t stream) {
@@ -1222,27 +1242,17 @@ int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
   TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
                 2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
   if (d == 128) {
-    static bool attr = false;
-    if (!attr) {
-      if ((rc = cuda_check(cudaFuncSetAttribute(attn_fwd_core_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                CoreCfg<128>::SMEM),
-                           "cudaFuncSetAttribute(attn core)"))) {
-        delete p;
-        return rc;
-      }
-      attr = true;
+    if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_fwd_core_kernel<128>), kFwd128, CoreCfg<128>::SMEM,
+                            "cudaFuncSetAttribute(attn core)"))) {
+      delete p;
+      return rc;
     }
     attn_fwd_core_kernel<128><<<blocks, kThreads, CoreCfg<128>::SMEM, stream>>>(*p);
   } else {
-    static bool attr = false;
-    if (!attr) {
-      if ((rc = cuda_check(cudaFuncSetAttribute(attn_fwd_core_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                CoreCfg<64>::SMEM),
-                           "cudaFuncSetAttribute(attn core)"))) {
-        delete p;
-        return rc;
-      }
-      attr = true;
+    if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_fwd_core_kernel<64>), kFwd64, CoreCfg<64>::SMEM,
+                            "cudaFuncSetAttribute(attn core)"))) {
+      delete p;
+      return rc;
     }
     attn_fwd_core_kernel<64><<<blocks, kThreads, CoreCfg<64>::SMEM, stream>>>(*p);
   }
@@ -1290,27 +1300,17 @@ int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
   TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
                 2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
   if (d == 128) {
-    static bool attr = false;
-    if (!attr) {
-      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_core_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                BwdCfg<128>::SMEM),
-                           "cudaFuncSetAttribute(attn bwd core)"))) {
-        delete p;
-        return rc;
-      }
-      attr = true;
+    if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_core_kernel<128>), kBwd128, BwdCfg<128>::SMEM,
+                            "cudaFuncSetAttribute(attn bwd core)"))) {
+      delete p;
+      return rc;
     }
     attn_bwd_core_kernel<128><<<blocks, kThreads, BwdCfg<128>::SMEM, stream>>>(*p);
   } else {
-    static bool attr = false;
-    if (!attr) {
-      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_core_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                BwdCfg<64>::SMEM),
-                           "cudaFuncSetAttribute(attn bwd core)"))) {
-        delete p;
-        return rc;
-      }
-      attr = true;
+    if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_core_kernel<64>), kBwd64, BwdCfg<64>::SMEM,
+                            "cudaFuncSetAttribute(attn bwd core)"))) {
+      delete p;
+      return rc;
     }
     attn_bwd_core_kernel<64><<<blocks, kThreads, BwdCfg<64>::SMEM, stream>>>(*p);
   }
@@ -1360,27 +1360,17 @@ int attn_bwd_kv(int t, int64_t T, int nql, int nkvl, int grp, int d, const void*
   TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
                 2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 3.0 * kc) * t);
   if (d == 128) {
-    static bool attr = false;
-    if (!attr) {
-      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_kv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                KvCfg<128>::SMEM),
-                           "cudaFuncSetAttribute(attn kv core)"))) {
-        delete p;
-        return rc;
-      }
-      attr = true;
+    if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel<128>), kKv128, KvCfg<128>::SMEM,
+                            "cudaFuncSetAttribute(attn kv core)"))) {
+      delete p;
+      return rc;
     }
     attn_bwd_kv_kernel<128><<<blocks, kThreads, KvCfg<128>::SMEM, stream>>>(*p);
   } else {
-    static bool attr = false;
-    if (!attr) {
-      if ((rc = cuda_check(cudaFuncSetAttribute(attn_bwd_kv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                KvCfg<64>::SMEM),
-                           "cudaFuncSetAttribute(attn kv core)"))) {
-        delete p;
-        return rc;
-      }
-      attr = true;
+    if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel<64>), kKv64, KvCfg<64>::SMEM,
+                            "cudaFuncSetAttribute(attn kv core)"))) {
+      delete p;
+      return rc;
     }
     attn_bwd_kv_kernel<64><<<blocks, kThreads, KvCfg<64>::SMEM, stream>>>(*p);
   }
