@@ -2,9 +2,9 @@
 
 The t tensor-parallel shards of the method are t device buffers on one GPU; the hot path
 (column/row-parallel GEMMs with fused activations, the partial-sum all-reduce, the GTP_remat
-weight path, vocab-parallel cross-entropy and embedding, the head-split attention block) runs in the hand-written CUDA kernels of
-``_lib/libttl.so`` behind the C ABI in ``include/ttl.h``.  This package is the thin Python
-binding over that ABI.
+weight path, vocab-parallel cross-entropy and embedding, the head-split attention block) runs
+in the hand-written CUDA kernels of ``_lib/libttl.so`` behind the C ABI in ``include/ttl.h``.
+This package is the thin Python binding over that ABI.
 """
 from ._binding import (  # noqa: F401
     ACT, CE_FORWARD_ONLY, attn_bwd_buffers, attn_fwd_buffers, CE_FP32_DLOGITS, LIB_PATH, STATIC_WS_BYTES, TTL_ERR_ALIGN, TTL_ERR_ARG, TTL_ERR_CUDA, TTL_ERR_DEVICE,
