@@ -270,16 +270,20 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
       tmem_ld_wait();
       const int col0 = n_base_paired + ch * 32;
       if (row_ok && col0 < pr.N) {
-        float gv[32], uv[32], hv[32];
+        float gv[32], uv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           gv[j] = __uint_as_float(g[j]);
           uv[j] = __uint_as_float(u[j]);
-          hv[j] = gv[j] * sigmoid_f(gv[j]) * uv[j];
         }
         store_row32_bf16(pr.out0, pr.ld_out, row, col0, pr.N, gv);
         store_row32_bf16(pr.out1, pr.ld_out, row, col0, pr.N, uv);
-        store_row32_bf16(pr.out2, pr.ld_out, row, col0, pr.N, hv);
+        if (epi == EPI_SWIGLU_FWD) {
+          float hv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) hv[j] = gv[j] * sigmoid_f(gv[j]) * uv[j];
+          store_row32_bf16(pr.out2, pr.ld_out, row, col0, pr.N, hv);
+        }
       }
     }
     return;
@@ -770,8 +774,9 @@ int GemmBatch::add_maps_consecutive(const void* const* ptrs, int n, int64_t rows
 
 Problem* GemmBatch::add_problem(int64_t M, int64_t N, bool a_mn, bool b_mn, int epi, bool paired, bool join) {
   if (err_) return nullptr;
-  if (join && (p_->nprob == 0 || p_->probs[p_->nprob - 1].M != M || p_->probs[p_->nprob - 1].paired != paired))
-    join = false;   // a group needs the same M and tile width; otherwise start a new one
+  if (join && (p_->nprob == 0 || p_->probs[p_->nprob - 1].M != M))
+    join = false;   // a group needs the same M; otherwise start a new one.  Its problems may
+                    // mix paired and unpaired tiles: each tile is decoded against its own problem.
   if (p_->nprob >= kMaxProblems) {
     err_ = set_error(TTL_ERR_ARG, "GEMM batch: too many problems (max %d)", kMaxProblems);
     return nullptr;

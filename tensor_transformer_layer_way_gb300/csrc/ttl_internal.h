@@ -64,6 +64,9 @@ enum Epilogue : int {
                        // the cross-entropy partials: out1[row * ext1 + 2 (tn0 + tn) + half] =
                        // (max, sum exp(z - max)) over those columns; out2[row] = the logit at
                        // target aux0[row] - ext0 when that column is in the tile
+  EPI_PAIR_BF16 = 7,   // paired tile: out0 = bf16(accumulator columns [0,128)) from map_b,
+                       // out1 = bf16(columns [128,256)) from map_b2 (two narrow products as one
+                       // full-width MMA, e.g. the K and V projections of a shard)
 };
 
 // One K-range of a problem: k-blocks of 64 read from map_a at K offset a_k0 and from
@@ -75,8 +78,8 @@ struct Seg {
 };
 
 // One output matrix [M, N]; tiles of 128 rows x 256 accumulator columns.  A paired tile
-// (SwiGLU forward) covers 128 output columns: accumulator columns [0,128) come from
-// map_b and [128,256) from map_b2 at the same N coordinates.
+// (SwiGLU forward, EPI_PAIR_BF16) covers 128 output columns: accumulator columns [0,128)
+// come from map_b and [128,256) from map_b2 at the same N coordinates.
 struct Problem {
   int32_t M, N;
   int32_t tiles_m, tiles_n;
