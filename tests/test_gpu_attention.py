@@ -82,6 +82,8 @@ SMALL = [
     (2, 136, 128, 2, 2, 64),      # one query head per KV head, ragged T below two tiles
     (2, 64, 64, 4, 2, 64),        # every GEMM at most 128 rows: single-CTA tiles
     (8, 392, 128, 8, 8, 64),      # eight shards of one head each, ragged T
+    (1, 200, 128, 4, 2, 128),     # two KV heads per shard: K|V projections span two paired tiles
+    (2, 264, 256, 8, 4, 64),      # two KV heads per shard at d = 64, ragged T
 ]
 
 
