@@ -43,31 +43,35 @@ __device__ __forceinline__ void unpack8_bf16(uint4 w, float* v) {
   v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
 }
 
-// One warp per (shard, head, query) row: D[q] = sum_k dO[q, k] O[q, k] over the head's d
-// columns (the rowsum term of the softmax backward).
+// One warp per (shard, query) row, covering all of the shard's query heads (their nql d columns
+// are contiguous): D[(i nql + c) T + q] = sum over head c's d columns of dO[q, .] O[q, .] (the
+// rowsum term of the softmax backward).  Each 256-column sweep loads 512 contiguous bytes per
+// operand; the d / 8 lanes of one head then reduce among themselves.
 __global__ void __launch_bounds__(kRowWarps * 32) attn_rowdot_kernel(const __grid_constant__ AttnRows R,
                                                                      float* __restrict__ D, int64_t rows,
                                                                      int64_t T, int64_t nql, int d) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
-  if (row >= rows) return;
+  if (row >= rows) return;   // rows = t T: the whole warp leaves together
   const int lane = threadIdx.x & 31;
-  const int64_t per_shard = nql * T;
-  const int i = static_cast<int>(row / per_shard);
-  const int64_t r = row - i * per_shard;
-  const int64_t c = r / T;
-  const int64_t q = r - c * T;
-  const int64_t hcol = q * nql * d + c * d;
-  float acc = 0.0f;
-  for (int k0 = lane * 8; k0 < d; k0 += 256) {
-    float a[8], b[8];
-    unpack8_bf16(*reinterpret_cast<const uint4*>(R.dO[i] + hcol + k0), a);
-    unpack8_bf16(*reinterpret_cast<const uint4*>(R.o[i] + hcol + k0), b);
+  const int i = static_cast<int>(row / T);
+  const int64_t q = row - i * T;
+  const int64_t cols = nql * d;
+  const __nv_bfloat16* a = R.dO[i] + q * cols;
+  const __nv_bfloat16* o = R.o[i] + q * cols;
+  const int lph = d / 8;     // lanes per head in a sweep (8 or 16)
+  for (int64_t base = 0; base < cols; base += 256) {
+    const int64_t k0 = base + lane * 8;
+    float acc = 0.0f;
+    if (k0 < cols) {
+      float x[8], y[8];
+      unpack8_bf16(*reinterpret_cast<const uint4*>(a + k0), x);
+      unpack8_bf16(*reinterpret_cast<const uint4*>(o + k0), y);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc = fmaf(a[j], b[j], acc);
+      for (int j = 0; j < 8; ++j) acc = fmaf(x[j], y[j], acc);
+    }
+    for (int off = lph >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (k0 < cols && (lane & (lph - 1)) == 0) D[(static_cast<int64_t>(i) * nql + k0 / d) * T + q] = acc;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) D[row] = acc;
 }
 
 struct Shape {
@@ -291,15 +295,15 @@ extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
   }
   if ((rc = batch.flush(st))) return rc;
 
-  // D = rowsum(dO_c O_c) for every (shard, head, query) row.
+  // D = rowsum(dO_c O_c) for every (shard, head, query) row; one warp per (shard, query).
   {
     AttnRows R = {};
     for (int i = 0; i < t; ++i) {
       R.dO[i] = dO_of(i);
       R.o[i] = bf(O_save[i]);
     }
-    const int64_t rows = static_cast<int64_t>(t) * s.nql * T;
-    TraceScope tr(st, TTL_K_SOFTMAX, 0.0, static_cast<double>(rows) * (4.0 * d + 4.0));
+    const int64_t rows = static_cast<int64_t>(t) * T;
+    TraceScope tr(st, TTL_K_SOFTMAX, 0.0, static_cast<double>(rows) * s.nql * (4.0 * d + 4.0));
     attn_rowdot_kernel<<<static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps), kRowWarps * 32, 0, st>>>(
         R, Drow, rows, T, s.nql, d);
     if ((rc = cuda_check(cudaGetLastError(), "attn_rowdot_kernel launch"))) return rc;
