@@ -14,11 +14,13 @@
 //           for the backward).
 // The probabilities the backward reads are therefore written once; nothing re-reads them here.
 //
-// Roles (320 threads): warp 0 issues TMA loads (Q once; then K_0..K_n-1 for pass 1 and K_0, V_0,
-// K_1, V_1, ... for pass 2 through a 4-slot ring), warp 1 issues the MMAs, warps 2..9 run the
-// softmax: two warps per TMEM lane quadrant, each on 64 of a tile's 128 keys (and, at the end,
-// half of O's d columns).  The MMA warp issues S_j before P_(j-1) V_(j-1), so the softmax of
-// tile j overlaps the previous tile's P V.  Every wait is bounded (TTL_ERR_TIMEOUT on expiry).
+// Roles (352 threads): warp 0 issues TMA loads (Q once; then K_0..K_n-1 for pass 1 and K_0,
+// V_0, K_1, V_1, ... for pass 2 through a 4-slot ring); warp 1 issues the MMAs; warp 10 issues
+// the TMA stores of P; warps 2..9 run the softmax: two warps per TMEM lane quadrant, each
+// on 64 of a tile's 128 keys (and, at the end, half of O's d columns).  In pass 2 the MMA warp
+// issues whichever is ready first, the next S or the next P V, so the softmax of tile j
+// overlaps the previous tile's P V, and it never waits for a store.  Every wait is bounded
+// (TTL_ERR_TIMEOUT on expiry).
 //
 // Layouts: Q, K tiles K-major (d contiguous, 64-column 128-byte-swizzled boxes of 128 rows);
 // V tiles MN-major (64 d x 64 keys boxes).  TMEM columns [0,128) and [128,256) are the two score
@@ -40,6 +42,7 @@ constexpr int kBQ = 128;            // queries per CTA
 constexpr int kBKV = 128;           // keys per tile
 constexpr int kRing = 4;            // K / V slots
 constexpr int kThreads = 320;
+constexpr int kFwdThreads = 352;   // forward core: + one warp for the P stores
 constexpr int kTmemCols = 512;
 
 struct CoreParams {
@@ -103,7 +106,7 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid_constant__ CoreParams P) {
+__global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_core_kernel(const __grid_constant__ CoreParams P) {
   using C = CoreCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -210,6 +213,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
                   reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
     }
     __syncwarp();
+  } else if (warp == kThreads / 32) {
+    // ------------------------------------------------------------------ P stores (own warp)
+    if (lane == 0) {
+      // P_j leaves for HBM (two 64-key boxes) as soon as the softmax has written it.  This thread
+      // alone waits for each store to have read the shared tile, so the MMA warp never waits on
+      // a store; its arrival is the second one the P buffer needs (the first: the P V MMAs).
+      bool ok = true;
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int b = j & 1;
+        ok = mbar_wait(&p_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
+        if (!ok) break;
+        tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, j * kBKV, q0, c);
+        tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, j * kBKV + 64, q0, c);
+        bulk_commit_group();
+        bulk_wait_group_read<0>();
+        mbar_arrive(&p_empty[b]);
+      }
+      bulk_wait_group_all();   // every store complete before the CTA's shared memory goes away
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -278,10 +301,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
           if (mbar_test_wait(&ring_full[vslot], static_cast<uint32_t>(pos / kRing) & 1u) &&
               mbar_test_wait(&p_full[b], static_cast<uint32_t>(np >> 1) & 1u)) {
             tc_fence_after_sync();
-            // P_np -> HBM: two 64-key boxes of the shared copy
-            tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES, np * kBKV, q0, c);
-            tma_store_3d(&P.pm[shard], sP + b * C::P_BYTES + 16384, np * kBKV + 64, q0, c);
-            bulk_commit_group();
             // O += P_np V_np with P from tensor memory (A operand, 8 columns per 16 keys)
             const uint32_t vaddr = ring0 + vslot * C::SLOT;
             for (int kk2 = 0; kk2 < 2; ++kk2) {          // 64-key blocks
@@ -293,9 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
               }
             }
             umma_commit(&ring_empty[vslot]);
-            umma_commit(&p_empty[b]);                  // first arrival: the MMAs have read P_np
-            bulk_wait_group_read<1>();                 // the store of P_(np-1) has read its buffer
-            if (np > 0) mbar_arrive(&p_empty[(np - 1) & 1]);
+            umma_commit(&p_empty[b]);                  // the MMAs have read P_np
             ++np;
             progress = true;
           }
@@ -310,15 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_core_kernel(const __grid
           ok = false;
         }
       }
-      bulk_wait_group_read<0>();
-      if (ntiles > 0) mbar_arrive(&p_empty[(ntiles - 1) & 1]);
       if (ok) umma_commit(o_full);
-      // Every MMA issued here must finish before TMEM is released, and every store before the
-      // CTA's shared memory goes away.
+      // Every MMA issued here must finish before TMEM is released.
       umma_commit(done_bar);
       int dummy_abort = 0;
       mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
-      bulk_wait_group_all();
     }
     __syncwarp();
   } else {
@@ -1247,14 +1260,14 @@ int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
       delete p;
       return rc;
     }
-    attn_fwd_core_kernel<128><<<blocks, kThreads, CoreCfg<128>::SMEM, stream>>>(*p);
+    attn_fwd_core_kernel<128><<<blocks, kFwdThreads, CoreCfg<128>::SMEM, stream>>>(*p);
   } else {
     if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_fwd_core_kernel<64>), kFwd64, CoreCfg<64>::SMEM,
                             "cudaFuncSetAttribute(attn core)"))) {
       delete p;
       return rc;
     }
-    attn_fwd_core_kernel<64><<<blocks, kThreads, CoreCfg<64>::SMEM, stream>>>(*p);
+    attn_fwd_core_kernel<64><<<blocks, kFwdThreads, CoreCfg<64>::SMEM, stream>>>(*p);
   }
   delete p;
   return cuda_check(cudaGetLastError(), "attn_fwd_core_kernel launch");
