@@ -42,7 +42,9 @@ constexpr int kBQ = 128;            // queries per CTA
 constexpr int kBKV = 128;           // keys per tile
 constexpr int kRing = 4;            // K / V slots
 constexpr int kThreads = 320;
-constexpr int kFwdThreads = 352;   // forward core: + one warp for the P stores
+// Every core adds a warp of its own for its P traffic (the forward's stores, the backward's
+// loads): a second polling thread inside the producer warp would run interleaved with it.
+constexpr int kCoreThreads = kThreads + 32;
 constexpr int kTmemCols = 512;
 
 struct CoreParams {
@@ -106,7 +108,7 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_core_kernel(const __grid_constant__ CoreParams P) {
+__global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __grid_constant__ CoreParams P) {
   using C = CoreCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -558,11 +560,11 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
 //   softmax warps overwrite it in place (each thread its own row) with
 //   dS_j = P_j (dP_j - D) / sqrt(d) (P is zero above the diagonal, so is dS), and
 //   dQ += dS_j K_j accumulates in TMEM.  dQ is stored at the end.
-// Roles as in the forward core: warp 0 lane 0 loads dO, then V_j / K_j through the 4-slot ring;
-// warp 0 lane 1 loads the P tiles into the two P buffers; warp 1 issues the MMAs (dP_j, then
-// dQ_(j-1)); warps 2..9 compute dS, two per TMEM lane quadrant.
+// Roles (352 threads): warp 0 loads dO, then V_j / K_j through the 4-slot ring; warp 10 loads
+// the P tiles into the two P buffers; warp 1 issues the MMAs (dP_j, then dQ_(j-1)); warps 2..9
+// compute dS, two per TMEM lane quadrant.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid_constant__ BwdParams P) {
+__global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __grid_constant__ BwdParams P) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -661,8 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_core_kernel(const __grid
       for (int i = issued - pending; i < issued; ++i)
         mbar_wait(&ring_full[i % kRing], static_cast<uint32_t>(i / kRing) & 1u,
                   reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
-    } else if (lane == 1) {
-      // ---------------------------------------------------------------- P tiles
+    }
+    __syncwarp();
+  } else if (warp == kThreads / 32) {
+    // ------------------------------------------------------------------ P tiles (own warp)
+    if (lane == 0) {
       bool ok = true;
       int started = 0;   // P tiles whose load was issued
       for (int j = 0; j < 2 && j < ntiles; ++j) {
@@ -884,11 +889,11 @@ struct KvCfg {
 //   dS = P (dP - D) / sqrt(d) (zero above the diagonal, where P is zero); dK += dS^T Q_c.
 // Neither P^T nor dS^T is ever formed: the MMAs read the [queries x keys] tiles as MN-major A
 // operands, and the [queries x d] Q and dO tiles loaded K-major double as MN-major B operands.
-// Roles: warp 0 lane 0 loads V once, then dO_j, Q_j through the 4-slot ring; warp 0 lane 1 loads
+// Roles (352 threads): warp 0 loads V once, then dO_j, Q_j through the 4-slot ring; warp 10 loads
 // P_j into the two P buffers; warp 1 issues dP_j, dV_j, then dK_(j-1); warps 2..9 compute dS
 // (two per TMEM lane quadrant) and at the end store dK and dV.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kv_kernel(const __grid_constant__ KvParams P) {
+__global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __grid_constant__ KvParams P) {
   using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -985,8 +990,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kv_kernel(const __grid_c
       for (int i = issued - pending; i < issued; ++i)
         mbar_wait(&ring_full[i % kRing], static_cast<uint32_t>(i / kRing) & 1u,
                   reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
-    } else if (lane == 1) {
-      // ---------------------------------------------------------------- P tiles
+    }
+    __syncwarp();
+  } else if (warp == kThreads / 32) {
+    // ------------------------------------------------------------------ P tiles (own warp)
+    if (lane == 0) {
       bool ok = true;
       int started = 0;
       auto prefetch_pair = [&](int j) {
@@ -1260,14 +1268,14 @@ int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
       delete p;
       return rc;
     }
-    attn_fwd_core_kernel<128><<<blocks, kFwdThreads, CoreCfg<128>::SMEM, stream>>>(*p);
+    attn_fwd_core_kernel<128><<<blocks, kCoreThreads, CoreCfg<128>::SMEM, stream>>>(*p);
   } else {
     if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_fwd_core_kernel<64>), kFwd64, CoreCfg<64>::SMEM,
                             "cudaFuncSetAttribute(attn core)"))) {
       delete p;
       return rc;
     }
-    attn_fwd_core_kernel<64><<<blocks, kFwdThreads, CoreCfg<64>::SMEM, stream>>>(*p);
+    attn_fwd_core_kernel<64><<<blocks, kCoreThreads, CoreCfg<64>::SMEM, stream>>>(*p);
   }
   delete p;
   return cuda_check(cudaGetLastError(), "attn_fwd_core_kernel launch");
@@ -1318,14 +1326,14 @@ int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
       delete p;
       return rc;
     }
-    attn_bwd_core_kernel<128><<<blocks, kThreads, BwdCfg<128>::SMEM, stream>>>(*p);
+    attn_bwd_core_kernel<128><<<blocks, kCoreThreads, BwdCfg<128>::SMEM, stream>>>(*p);
   } else {
     if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_core_kernel<64>), kBwd64, BwdCfg<64>::SMEM,
                             "cudaFuncSetAttribute(attn bwd core)"))) {
       delete p;
       return rc;
     }
-    attn_bwd_core_kernel<64><<<blocks, kThreads, BwdCfg<64>::SMEM, stream>>>(*p);
+    attn_bwd_core_kernel<64><<<blocks, kCoreThreads, BwdCfg<64>::SMEM, stream>>>(*p);
   }
   delete p;
   return cuda_check(cudaGetLastError(), "attn_bwd_core_kernel launch");
@@ -1378,14 +1386,14 @@ int attn_bwd_kv(int t, int64_t T, int nql, int nkvl, int grp, int d, const void*
       delete p;
       return rc;
     }
-    attn_bwd_kv_kernel<128><<<blocks, kThreads, KvCfg<128>::SMEM, stream>>>(*p);
+    attn_bwd_kv_kernel<128><<<blocks, kCoreThreads, KvCfg<128>::SMEM, stream>>>(*p);
   } else {
     if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel<64>), kKv64, KvCfg<64>::SMEM,
                             "cudaFuncSetAttribute(attn kv core)"))) {
       delete p;
       return rc;
     }
-    attn_bwd_kv_kernel<64><<<blocks, kThreads, KvCfg<64>::SMEM, stream>>>(*p);
+    attn_bwd_kv_kernel<64><<<blocks, kCoreThreads, KvCfg<64>::SMEM, stream>>>(*p);
   }
   delete p;
   return cuda_check(cudaGetLastError(), "attn_bwd_kv_kernel launch");
