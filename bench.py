@@ -282,16 +282,18 @@ def bench_e2e(ttl, torch, dev, dist, args, X, dY, Wg, Wu, Wd, fo, bo):
 
     Every step copies its inputs X and dY in from pinned host memory and its results (Z and
     dX, one buffer each) back out.  The copies run on a separate copy stream so that step
-    i+1's inputs load and step i-1's results drain while step i computes: two input slots on
-    the device and two staging slots for the results, ordered by events.  All copies of all
-    K steps are inside the timed region, and the last result is checked on the host."""
+    i+1's inputs load and step i-1's results drain while step i computes: two input slots and
+    two sets of output buffers on the device, used alternately and ordered by events (a step
+    does not overwrite a set until its previous results have reached the host).  All copies
+    of all K steps are inside the timed region, and the last result is checked on the host."""
     T, h, act = MLP["T"], MLP["h"], MLP["act"]
+    t, f = MLP["t"], MLP["f"]
     main = torch.cuda.current_stream()
     cp = torch.cuda.Stream()
     Xin = [X, torch.empty_like(X)]
     dYin = [dY, torch.empty_like(dY)]
-    Zst = [torch.empty_like(X) for _ in range(2)]
-    dXst = [torch.empty_like(X) for _ in range(2)]
+    fos = [fo, ttl.mlp_fwd_buffers(t, act, T, h, f, dev)]
+    bos = [bo, ttl.mlp_bwd_buffers(t, act, T, h, f, dev)]
     # Two distinct host batches, alternated, so each step brings in different data.
     Xh = [X.cpu().pin_memory(), (X.cpu().float() * -1).to(torch.bfloat16).pin_memory()]
     dYh = [dY.cpu().pin_memory(), (dY.cpu().float() * -1).to(torch.bfloat16).pin_memory()]
@@ -317,17 +319,15 @@ def bench_e2e(ttl, torch, dev, dist, args, X, dY, Wg, Wu, Wd, fo, bo):
             if i + 1 < n:
                 load(i + 1)
             main.wait_event(ev_in[k])
-            ttl.tp_mlp_fwd(Xin[k], Wg, Wd, act=act, A_up=Wu, out=fo)
-            ttl.tp_mlp_bwd(Xin[k], dYin[k], Wg, Wd, fo, act=act, A_up=Wu, out=bo)
+            main.wait_event(ev_drained[k])         # output set k of step i-2 has reached the host
+            ttl.tp_mlp_fwd(Xin[k], Wg, Wd, act=act, A_up=Wu, out=fos[k])
+            ttl.tp_mlp_bwd(Xin[k], dYin[k], Wg, Wd, fos[k], act=act, A_up=Wu, out=bos[k])
             ev_free[k].record(main)
-            main.wait_event(ev_drained[k])         # staging slot k drained to the host
-            Zst[k].copy_(fo["Z"][0])
-            dXst[k].copy_(bo["dX"][0])
             ev_res[k].record(main)
             with torch.cuda.stream(cp):
                 cp.wait_event(ev_res[k])
-                Zh[k].copy_(Zst[k], non_blocking=True)
-                dXh[k].copy_(dXst[k], non_blocking=True)
+                Zh[k].copy_(fos[k]["Z"][0], non_blocking=True)
+                dXh[k].copy_(bos[k]["dX"][0], non_blocking=True)
                 ev_drained[k].record(cp)
         main.wait_stream(cp)
 
@@ -341,8 +341,10 @@ def bench_e2e(ttl, torch, dev, dist, args, X, dY, Wg, Wu, Wd, fo, bo):
     torch.cuda.synchronize()
     dist.barrier()
     ms = dist.max(e0.elapsed_time(e1))
-    if not torch.equal(Zh[(args.steps - 1) % 2].to(dev), fo["Z"][0]):
+    last = (args.steps - 1) % 2
+    if not torch.equal(Zh[last].to(dev), fos[last]["Z"][0]):
         raise RuntimeError("e2e: the host copy of the last result does not match the device result")
+    del fos, bos
     return {"value": round(dist.world * MLP_FLOPS * args.steps / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
             "h2d_bytes_per_step": 2 * T * h * 2, "d2h_bytes_per_step": 2 * T * h * 2,
             "ms_per_step": round(ms / args.steps, 4),
