@@ -24,8 +24,9 @@ struct GatherSet {
   const uint4* p[kMaxShards];
 };
 
-// Block b of a grid of G handles the contiguous vector range [b n / G, (b + 1) n / G): every
-// block gets the same work, so a launch that is all one wave has no tail.
+// Block b of a grid of G handles the contiguous vector range [b c, min(n, (b + 1) c)) with
+// c = ceil(n / G): every block gets the same work (the last one at most c less), so a launch
+// that is all one wave has no tail.
 __device__ __forceinline__ void block_range(int64_t n, int64_t& begin, int64_t& end) {
   const int64_t per = (n + gridDim.x - 1) / gridDim.x;
   begin = static_cast<int64_t>(blockIdx.x) * per;
