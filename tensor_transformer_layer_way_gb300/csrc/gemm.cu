@@ -45,7 +45,7 @@ constexpr int BN = kGemmBN;        // accumulator columns per tile
 constexpr int BK = 64;             // K per stage
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int GROUP_M = 16;
-constexpr int NUM_THREADS = 320;   // producer warp, MMA warp, 8 epilogue warps
+constexpr int NUM_THREADS = 192;   // producer warp, MMA warp, 4 epilogue warps (one per TMEM lane quadrant)
 
 template <bool PAIR>
 struct Cfg {
@@ -56,48 +56,58 @@ struct Cfg {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = PAIR ? 7 : 4;
   static constexpr int TX_BYTES = PAIR ? 2 * STAGE : STAGE;   // counted on the (leader's) full barrier
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr int SCHED_BYTES = 1280;   // the shared copy of the tile schedule
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + SCHED_BYTES;
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
 };
-static_assert(sizeof(GemmParams) <= 32764, "kernel parameter block beyond the 32 KiB limit");
 
 struct TileCoord {
   int p, tm, tn;
 };
+
+// The tile schedule, copied into shared memory at kernel start.  Decoding a tile from the
+// parameter block (about 32 KiB, far more than the constant cache holds) misses that cache at
+// every tile change, while the tensor pipe runs dry.
+struct SchedTable {
+  int32_t g_start[kMaxProblems], g_tm[kMaxProblems], g_tn[kMaxProblems], g_first[kMaxProblems],
+      g_count[kMaxProblems];
+  int32_t p_tn0[kMaxProblems];
+  int32_t p_kb[kMaxProblems];      // k-blocks of each of the problem's tiles (all segments)
+  uint32_t p_flags[kMaxProblems];  // bit 0: A MN-major, bit 1: B MN-major, bit 2: 128-column MMAs
+  int32_t ngroups;
+};
+static_assert(sizeof(SchedTable) <= Cfg<true>::SCHED_BYTES, "schedule table beyond its space");
 
 // Linear tile index -> (problem, m-tile, n-tile).  Inside a tile group the order is: bands
 // of GROUP_M m-tiles; within a band, n-tiles across all of the group's problems; within
 // an n-tile, the band's m-tiles.  Persistent workers taking consecutive indices therefore
 // share A rows (same band) and B columns (same n-tile) in L2.
 // `gi` is the caller's running group index: a worker visits increasing tile indices, so the
-// search for the tile's group resumes where the previous one ended (the parameter block
-// lives in constant memory, and a scan over dozens of groups per tile costs microseconds).
-__device__ __forceinline__ TileCoord decode_tile(const GemmParams& P, int tile, int& gi) {
+// search for the tile's group resumes where the previous one ended.
+__device__ __forceinline__ TileCoord decode_tile_s(const SchedTable& S, int tile, int& gi) {
 #pragma unroll 1
-  while (gi + 1 < P.ngroups && tile >= P.groups[gi + 1].tile_start) ++gi;
-  const TileGroup& g = P.groups[gi];
-  const int local = tile - g.tile_start;
-  const int per_band = GROUP_M * g.tiles_n;
+  while (gi + 1 < S.ngroups && tile >= S.g_start[gi + 1]) ++gi;
+  const int local = tile - S.g_start[gi];
+  const int per_band = GROUP_M * S.g_tn[gi];
   const int band = local / per_band;
   const int first_m = band * GROUP_M;
-  const int gm = min(GROUP_M, g.tiles_m - first_m);
+  const int gm = min(GROUP_M, S.g_tm[gi] - first_m);
   const int r = local - band * per_band;
   const int tn = r / gm;
-  // the problem holding n-tile tn: binary search over the group's first n-tiles
-  int lo = g.first, hi = g.first + g.count - 1;
+  int lo = S.g_first[gi], hi = S.g_first[gi] + S.g_count[gi] - 1;
 #pragma unroll 1
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (P.probs[mid].tn0 <= tn) lo = mid;
+    if (S.p_tn0[mid] <= tn) lo = mid;
     else hi = mid - 1;
   }
-  const int p = lo;
   TileCoord c;
-  c.p = p;
+  c.p = lo;
   c.tm = first_m + r % gm;
-  c.tn = tn - P.probs[p].tn0;
+  c.tn = tn - S.p_tn0[lo];
   return c;
 }
+static_assert(sizeof(GemmParams) <= 32764, "kernel parameter block beyond the 32 KiB limit");
 
 // ------------------------------------------------------------------ epilogue math
 
@@ -253,9 +263,9 @@ __device__ __forceinline__ void epilogue_chunk(const Problem& pr, int row, int n
 }
 
 // Applies the problem's epilogue to one accumulator tile slice held in this CTA's TMEM
-// (128 rows; this thread owns one row) and stores it.  Two warps share each TMEM lane
-// quadrant: `half` selects the accumulator columns [half BN/2, (half + 1) BN/2) (a paired
-// tile: output columns [half BN/4, (half + 1) BN/4) of both halves).
+// (128 rows; this thread owns one row) and stores it.  `half` selects the accumulator columns
+// [half BN/2, (half + 1) BN/2) (a paired tile: output columns [half BN/4, (half + 1) BN/4) of
+// both halves); an epilogue warp calls it for half 0, then half 1.
 __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase, int row, int n_base_paired,
                                               int n_base, int half) {
   const bool row_ok = row < pr.M;
@@ -327,6 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
   uint64_t* done_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  SchedTable* sched = reinterpret_cast<SchedTable*>(smem + C::STAGES * C::STAGE + 256);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -342,7 +353,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], PAIR ? 16 : 8);  // every epilogue warp of the pair arrives
+      mbar_init(&tempty_bar[a], PAIR ? 8 : 4);   // every epilogue warp of the pair arrives
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -351,6 +362,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
   if (warp == 0) {
     for (int i = lane; i < P.nmaps; i += 32) tma_prefetch_map(&P.maps[i]);
   }
+  for (int i = threadIdx.x; i < kMaxProblems; i += blockDim.x) {
+    if (i < P.ngroups) {
+      const TileGroup& g = P.groups[i];
+      sched->g_start[i] = g.tile_start;
+      sched->g_tm[i] = g.tiles_m;
+      sched->g_tn[i] = g.tiles_n;
+      sched->g_first[i] = g.first;
+      sched->g_count[i] = g.count;
+    }
+    if (i < P.nprob) {
+      const Problem& pr = P.probs[i];
+      int kb = 0;
+      for (int s = 0; s < pr.nseg; ++s) kb += pr.seg[s].kblocks;
+      sched->p_tn0[i] = pr.tn0;
+      sched->p_kb[i] = kb;
+      sched->p_flags[i] = (pr.a_mn ? 1u : 0u) | (pr.b_mn ? 2u : 0u) | (pr.half_n ? 4u : 0u);
+    }
+  }
+  if (threadIdx.x == 0) sched->ngroups = P.ngroups;
   if (warp == 1) {
     if (PAIR) {
       tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -378,7 +408,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       bool ok = true;
       int gi = 0;
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
-        const TileCoord c = decode_tile(P, tile, gi);
+        const TileCoord c = decode_tile_s(*sched, tile, gi);
         const Problem& pr = P.probs[c.p];
         int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
         int slab = 0;
@@ -483,22 +513,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       const uint32_t sbase = smem_u32(smem);
       int gi = 0;
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
-        const TileCoord c = decode_tile(P, tile, gi);
-        const Problem& pr = P.probs[c.p];
+        const int pi = decode_tile_s(*sched, tile, gi).p;
+        const uint32_t fl = sched->p_flags[pi];
+        const int nkb = sched->p_kb[pi];
+        const bool a_mn = fl & 1u, b_mn = fl & 2u;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        const uint32_t idesc = idesc_bf16_f32(C::TILE_M, pr.half_n ? BN / 2 : BN, pr.a_mn != 0, pr.b_mn != 0);
-        const uint32_t a_step = pr.a_mn ? 2048u : 32u;
-        const uint32_t b_step = pr.b_mn ? 2048u : 32u;
-        const uint32_t a_lbo = pr.a_mn ? 8192u : 16u;
-        const uint32_t b_lbo = pr.b_mn ? 8192u : 16u;
+        const uint32_t idesc = idesc_bf16_f32(C::TILE_M, (fl & 4u) ? BN / 2 : BN, a_mn, b_mn);
+        const uint32_t a_step = a_mn ? 2048u : 32u;
+        const uint32_t b_step = b_mn ? 2048u : 32u;
+        const uint32_t a_lbo = a_mn ? 8192u : 16u;
+        const uint32_t b_lbo = b_mn ? 8192u : 16u;
         uint32_t accumulate = 0;
-        for (int s = 0; ok && s < pr.nseg; ++s) {
-          for (int kb = 0; kb < pr.seg[s].kblocks; ++kb) {
+        {   // the tile's k-blocks over all its segments, in order
+          for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&full_bar[stage], phase, abort_flag, status, tmo)) {
               ok = false;
               break;
@@ -540,8 +572,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue warps
+    // One warp per TMEM lane quadrant, storing both halves of the accumulator columns in turn.
+    // (Two warps per quadrant finished each tile sooner but ran as a denser burst, which slowed
+    // the next tile's first MMAs on the schedulers they share with the MMA and producer warps.)
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;       // which half of the accumulator columns it stores
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -549,23 +583,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     const int my_row0 = static_cast<int>(rank) * 128 + row_in_tile;
     int gi = 0, gi_next = 0;
     if (unit < P.total_tiles) {
-      const TileCoord c0 = decode_tile(P, unit, gi_next);
-      prefetch_aux_row(P.probs[c0.p], c0.tm * C::TILE_M + my_row0, c0.tn * BN + half * (BN / 2));
+      const TileCoord c0 = decode_tile_s(*sched, unit, gi_next);
+      for (int half = 0; half < 2; ++half)
+        prefetch_aux_row(P.probs[c0.p], c0.tm * C::TILE_M + my_row0, c0.tn * BN + half * (BN / 2));
     }
     for (int tile = unit; tile < P.total_tiles; tile += nunits) {
-      const TileCoord c = decode_tile(P, tile, gi);
+      const TileCoord c = decode_tile_s(*sched, tile, gi);
       const Problem& pr = P.probs[c.p];
       const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
       // The next tile's auxiliary rows travel to L2 while this tile's epilogue runs.
       if (tile + nunits < P.total_tiles) {
-        const TileCoord cn = decode_tile(P, tile + nunits, gi_next);
-        prefetch_aux_row(P.probs[cn.p], cn.tm * C::TILE_M + my_row0, cn.tn * BN + half * (BN / 2));
+        const TileCoord cn = decode_tile_s(*sched, tile + nunits, gi_next);
+        for (int half = 0; half < 2; ++half)
+          prefetch_aux_row(P.probs[cn.p], cn.tm * C::TILE_M + my_row0, cn.tn * BN + half * (BN / 2));
       }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const int row = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + row_in_tile;
-      epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN, half);
+      for (int half = 0; half < 2; ++half) epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN, half);
       tc_fence_before_sync();
       __syncwarp();
       // This warp's accumulator reads are complete (tcgen05.wait::ld in the epilogue): the
