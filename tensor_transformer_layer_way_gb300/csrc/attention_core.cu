@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, abort_flag, status, tmo);
       tc_fence_after_sync();
-      const uint32_t qaddr = smem_u32(sQ);
       const uint32_t ring0 = smem_u32(sRing);
+      const uint64_t qd = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKV, false, false);
       const uint32_t idesc_o = idesc_bf16_f32(kBQ, D, false, true);
       int sj = 0;            // S tiles issued (both passes), selects the score buffer
@@ -250,12 +250,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
         const uint32_t sph = static_cast<uint32_t>(sj >> 1) & 1u;
         if (!mbar_wait(&s_empty[b], sph ^ 1u, abort_flag, status, tmo)) return false;
         tc_fence_after_sync();
-        const uint32_t kaddr = ring0 + slot * C::SLOT;
+        const uint64_t kd = smem_desc_sw128(ring0 + slot * C::SLOT, 16, 1024);
         for (int kb = 0; kb < C::KB; ++kb) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc_sw128(qaddr + kb * 16384 + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kaddr + kb * 16384 + kk * 32, 16, 1024);
+            const uint64_t ad = desc_advance(qd, kb * 16384 + kk * 32);
+            const uint64_t bd = desc_advance(kd, kb * 16384 + kk * 32);
             umma_bf16(tmem_base + b * kBKV, ad, bd, idesc_s, (kb | kk) ? 1u : 0u);
           }
         }
@@ -304,12 +304,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
               mbar_test_wait(&p_full[b], static_cast<uint32_t>(np >> 1) & 1u)) {
             tc_fence_after_sync();
             // O += P_np V_np with P from tensor memory (A operand, 8 columns per 16 keys)
-            const uint32_t vaddr = ring0 + vslot * C::SLOT;
+            const uint64_t vd = smem_desc_sw128(ring0 + vslot * C::SLOT, 8192, 1024);
             for (int kk2 = 0; kk2 < 2; ++kk2) {          // 64-key blocks
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t at = tmem_base + C::T_P + b * (kBKV / 2) + (kk2 * 4 + kk) * 8;
-                const uint64_t bd = smem_desc_sw128(vaddr + kk2 * C::KB * 8192 + kk * 2048, 8192, 1024);
+                const uint64_t bd = desc_advance(vd, kk2 * C::KB * 8192 + kk * 2048);
                 umma_bf16_ts(tmem_base + C::T_O, at, bd, idesc_o, (np | kk2 | kk) ? 1u : 0u);
               }
             }
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
     if (lane == 0) {
       bool ok = mbar_wait(a_full, 0, abort_flag, status, tmo);
       tc_fence_after_sync();
-      const uint32_t aaddr = smem_u32(sA);
+      const uint64_t dod = smem_desc_sw128(smem_u32(sA), 16, 1024);   // the dO tile (A of dP)
       const uint32_t ring0 = smem_u32(sRing);
       const uint32_t paddr = smem_u32(sP);
       const uint32_t idesc_dp = idesc_bf16_f32(kBQ, kBKV, false, false);
@@ -729,12 +729,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
             break;
           }
           tc_fence_after_sync();
-          const uint32_t vaddr = ring0 + vslot * C::SLOT;
+          const uint64_t vd = smem_desc_sw128(ring0 + vslot * C::SLOT, 16, 1024);
           for (int kb = 0; kb < C::KB; ++kb) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(aaddr + kb * 16384 + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(vaddr + kb * 16384 + kk * 32, 16, 1024);
+              const uint64_t ad = desc_advance(dod, kb * 16384 + kk * 32);
+              const uint64_t bd = desc_advance(vd, kb * 16384 + kk * 32);
               umma_bf16(tmem_base + b * kBKV, ad, bd, idesc_dp, (kb | kk) ? 1u : 0u);
             }
           }
@@ -750,12 +750,13 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
             break;
           }
           tc_fence_after_sync();
-          const uint32_t kaddr = ring0 + kslot * C::SLOT;
+          const uint64_t pd = smem_desc_sw128(paddr + b * C::P_BYTES, 16, 1024);
+          const uint64_t kd = smem_desc_sw128(ring0 + kslot * C::SLOT, 8192, 1024);
           for (int kk2 = 0; kk2 < 2; ++kk2) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kk2 * 16384 + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(kaddr + kk2 * C::KB * 8192 + kk * 2048, 8192, 1024);
+              const uint64_t ad = desc_advance(pd, kk2 * 16384 + kk * 32);
+              const uint64_t bd = desc_advance(kd, kk2 * C::KB * 8192 + kk * 2048);
               umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_dq, (jp | kk2 | kk) ? 1u : 0u);
             }
           }
@@ -1032,7 +1033,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
     if (lane == 0) {
       bool ok = mbar_wait(v_full, 0, abort_flag, status, tmo);
       tc_fence_after_sync();
-      const uint32_t vaddr = smem_u32(sV);
+      const uint64_t vkd = smem_desc_sw128(smem_u32(sV), 16, 1024);   // V, K-major B of dP
       const uint32_t ring0 = smem_u32(sRing);
       const uint32_t paddr = smem_u32(sP);
       const uint32_t idesc_dp = idesc_bf16_f32(kBQ, kBKV, false, false);   // [queries x keys]
@@ -1059,11 +1060,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
           }
           tc_fence_after_sync();
           const uint32_t daddr = ring0 + dslot * C::SLOT;
+          const uint64_t dd = smem_desc_sw128(daddr, 16, 1024);
           for (int kb = 0; kb < C::KB; ++kb) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(daddr + kb * 16384 + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(vaddr + kb * 16384 + kk * 32, 16, 1024);
+              const uint64_t ad = desc_advance(dd, kb * 16384 + kk * 32);
+              const uint64_t bd = desc_advance(vkd, kb * 16384 + kk * 32);
               umma_bf16(tmem_base + b * kBKV, ad, bd, idesc_dp, (kb | kk) ? 1u : 0u);
             }
           }
@@ -1075,10 +1077,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
             break;
           }
           tc_fence_after_sync();
+          const uint64_t pmd = smem_desc_sw128(paddr + b * C::P_BYTES, 16384, 1024);
+          const uint64_t dmd = smem_desc_sw128(daddr, 16384, 1024);
 #pragma unroll
           for (int kq = 0; kq < kBQ / 16; ++kq) {   // K = the 128 queries, 16 per MMA
-            const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kq * 2048, 16384, 1024);
-            const uint64_t bd = smem_desc_sw128(daddr + kq * 2048, 16384, 1024);
+            const uint64_t ad = desc_advance(pmd, kq * 2048);
+            const uint64_t bd = desc_advance(dmd, kq * 2048);
             umma_bf16(t_dv, ad, bd, idesc_acc, (j | kq) ? 1u : 0u);
           }
           umma_commit(&pv_done[b]);
@@ -1094,11 +1098,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
             break;
           }
           tc_fence_after_sync();
-          const uint32_t qaddr = ring0 + qslot * C::SLOT;
+          const uint64_t smd = smem_desc_sw128(paddr + b * C::P_BYTES, 16384, 1024);
+          const uint64_t qmd = smem_desc_sw128(ring0 + qslot * C::SLOT, 16384, 1024);
 #pragma unroll
           for (int kq = 0; kq < kBQ / 16; ++kq) {
-            const uint64_t ad = smem_desc_sw128(paddr + b * C::P_BYTES + kq * 2048, 16384, 1024);
-            const uint64_t bd = smem_desc_sw128(qaddr + kq * 2048, 16384, 1024);
+            const uint64_t ad = desc_advance(smd, kq * 2048);
+            const uint64_t bd = desc_advance(qmd, kq * 2048);
             umma_bf16(t_dk, ad, bd, idesc_acc, (jp | kq) ? 1u : 0u);
           }
           umma_commit(&pb_empty[b]);

@@ -140,6 +140,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// A shared-memory descriptor moved `bytes` (a multiple of 16) further along: the start field
+// holds address >> 4 in the low 14 bits, and shared-memory addresses stay below 2^18, so the
+// addition never carries out of the field.  Cheaper than rebuilding the descriptor per MMA.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                   // D format: f32
