@@ -537,11 +537,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
             }
             tc_fence_after_sync();
             const uint32_t sa = sbase + stage * C::STAGE;
-            const uint32_t sb = sa + C::A_BYTES;
+            const uint64_t ad0 = smem_desc_sw128(sa, a_lbo, 1024);
+            const uint64_t bd0 = smem_desc_sw128(sa + C::A_BYTES, b_lbo, 1024);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t adesc = smem_desc_sw128(sa + kk * a_step, a_lbo, 1024);
-              const uint64_t bdesc = smem_desc_sw128(sb + kk * b_step, b_lbo, 1024);
+              const uint64_t adesc = desc_advance(ad0, kk * a_step);
+              const uint64_t bdesc = desc_advance(bd0, kk * b_step);
               if (PAIR) umma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
               else umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
               accumulate = 1;
