@@ -130,10 +130,21 @@ __device__ __forceinline__ float gelu_tanh_grad_f(float x) {
 
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
-// Stores 32 consecutive bf16 values of one row (columns col0..col0+31), masking at N.
+// Stores 32 consecutive bf16 values of one row (columns col0..col0+31), masking at N.  A whole,
+// 32-byte aligned chunk goes out as two 32-byte stores: each one fills an L2 sector, where a
+// 16-byte store fills half of one (this thread's row is the only one in the sector).  The same
+// change to the fp32 stores (CE logits) gained nothing and is not made.
 __device__ __forceinline__ void store_row32_bf16(void* base, int64_t ld, int row, int col0, int N,
                                                  const float* v) {
   __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + static_cast<int64_t>(row) * ld + col0;
+  if (col0 + 32 <= N && (reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    st_global_v8(p, w);
+    st_global_v8(p + 16, w + 8);
+    return;
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (col0 + q * 8 < N) {
