@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-components", action="store_true", help="skip the shard_reduce/gtp/ce legs")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="token rows of the oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="the CPU baseline repeats the oracle sample until this much time has passed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["sp_mlp", "shard_reduce", "gtp_chain", "vocab_ce", "vocab_embedding",
                                        "tp_attention"],
@@ -685,16 +687,20 @@ def oracle_sample(tokens: int):
     return X, W, dY
 
 
-def time_oracle(tokens: int, reps: int, warm: int = 0):
+def time_oracle(tokens: int, reps: int, warm: int = 0, min_seconds: float = 0.0):
+    """Times the oracle's fwd+bwd on `tokens` rows: `warm` untimed runs, then at least `reps`
+    timed ones and more until `min_seconds` of timed work has passed."""
     from oracle import tp_mlp
     X, W, dY = oracle_sample(tokens)
     times = []
-    for i in range(warm + reps):
+    i = 0
+    while i < warm + reps or sum(times) < min_seconds:
         t0 = time.perf_counter()
         fwd = tp_mlp.tp_mlp_forward(X, W, MLP["t"], MLP["act"])
         tp_mlp.tp_mlp_backward(X, W, MLP["t"], MLP["act"], dY, fwd)
         if i >= warm:
             times.append(time.perf_counter() - t0)
+        i += 1
     flops = MLP_FLOPS * tokens / MLP["T"]
     return flops, times
 
@@ -706,11 +712,15 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def cpu_baseline(tokens: int) -> dict:
-    flops, times = time_oracle(tokens, 1)
-    return {"value": round(flops / times[0] / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+def cpu_baseline(tokens: int, seconds: float) -> dict:
+    """The oracle on `tokens` of the workload's token rows (full weights), repeated until
+    `seconds` of wall time have passed; throughput over all repetitions."""
+    flops, times = time_oracle(tokens, 1, min_seconds=seconds)
+    total = sum(times)
+    return {"value": round(flops * len(times) / total / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(),
+            "kind": "oracle",
             "sample": f"fp64 numpy oracle, sharded t=8 SwiGLU MLP fwd+bwd on {tokens} of 8192 tokens "
-                      f"(full weights), {times[0]:.2f} s"}
+                      f"(full weights), {len(times)} repetitions, {total:.1f} s"}
 
 
 def run_reference(args, dist):
@@ -747,7 +757,7 @@ def main():
         else:
             out = run_ours(args, dist)
             if dist.rank == 0 and not args.no_cpu_baseline:
-                out["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+                out["cpu_baseline"] = cpu_baseline(args.cpu_tokens, args.cpu_seconds)
         if dist.rank == 0 and out is not None:
             print(json.dumps(out), flush=True)
     finally:
