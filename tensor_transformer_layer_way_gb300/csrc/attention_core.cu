@@ -7,25 +7,28 @@
 // attention, scale 1/sqrt(d), query head j reading KV head j / (n_q / n_kv).
 //
 // Two passes over the key tiles 0..qt of query tile qt (128 keys each):
-//   pass 1: S = Q K^T (tcgen05, fp32 in TMEM); per row the max and the sum of 2^(s log2e/sqrt(d) - max)
-//           over the keys <= the query -- exact row statistics, so P needs no later rescaling;
+//   pass 1: S = Q K^T (tcgen05, fp32 in TMEM), two key tiles per 256-column MMA group; per row the
+//           max and the sum of 2^(s log2e/sqrt(d) - max) over the keys <= the query -- exact row
+//           statistics, so P needs no later rescaling;
 //   pass 2: S again; P = 2^(s log2e/sqrt(d) - M - log2 sum) as bf16, written to tensor memory (the
 //           A operand of O += P V) and to a shared tile that a TMA store writes to HBM (saved
 //           for the backward).
 // The probabilities the backward reads are therefore written once; nothing re-reads them here.
 //
-// Roles (352 threads): warp 0 issues TMA loads (Q once; then K_0..K_n-1 for pass 1 and K_0,
-// V_0, K_1, V_1, ... for pass 2 through a 4-slot ring); warp 1 issues the MMAs; warp 10 issues
-// the TMA stores of P; warps 2..9 run the softmax: two warps per TMEM lane quadrant, each
-// on 64 of a tile's 128 keys (and, at the end, half of O's d columns).  In pass 2 the MMA warp
+// Roles (352 threads): warp 0 issues TMA loads (Q once; then the pairs (K_0, K_1), (K_2, K_3), ...
+// for pass 1, each filling two adjacent slots, and K_0, V_0, K_1, V_1, ... for pass 2 through a
+// 4-slot ring); warp 1 issues the MMAs; warp 10 issues the TMA stores of P; warps 2..9 run the
+// softmax: two warps per TMEM lane quadrant, each on half of a score group's keys (and, at the
+// end, half of O's d columns).  In pass 2 the MMA warp
 // issues whichever is ready first, the next S or the next P V, so the softmax of tile j
 // overlaps the previous tile's P V, and it never waits for a store.  Every wait is bounded
 // (TTL_ERR_TIMEOUT on expiry).
 //
 // Layouts: Q, K tiles K-major (d contiguous, 64-column 128-byte-swizzled boxes of 128 rows);
-// V tiles MN-major (64 d x 64 keys boxes).  TMEM columns [0,128) and [128,256) are the two score
-// buffers, [256, 256 + d) the O accumulator, [384,448) and [448,512) the two P buffers (bf16,
-// keys 2i and 2i + 1 in column i).  The MMAs here are bound by shared-memory bandwidth, so P V
+// V tiles MN-major (64 d x 64 keys boxes).  Pass 1: TMEM columns [0,256) and [256,512) are its two
+// 256-key score buffers.  Pass 2: [0,128) and [128,256) are the two score buffers, [256, 256 + d)
+// the O accumulator, [384,448) and [448,512) the two P buffers (bf16, keys 2i and 2i + 1 in
+// column i).  The MMAs here are bound by shared-memory bandwidth, so P V
 // reads P from tensor memory; the shared copy of P only feeds the coalesced TMA store.
 
 #include <cmath>
@@ -107,6 +110,51 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 // All committed store groups have completed.
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Folds 64 scores of one row (r0: keys 0..31, r1: keys 32..63 of the chunk, fp32 bits) into
+// the row's running max m and sum l of 2^(s k - m); only the first nv keys count (nv <= 0: none).
+__device__ __forceinline__ void row_stats64(const uint32_t (&r0)[32], const uint32_t (&r1)[32], int nv, float k,
+                                            float& m, float& l) {
+  if (nv >= 64) {   // below the diagonal: no mask
+    float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      x0 = fmaxf(x0, __uint_as_float(r0[e]));
+      x1 = fmaxf(x1, __uint_as_float(r0[e + 1]));
+      x2 = fmaxf(x2, __uint_as_float(r1[e]));
+      x3 = fmaxf(x3, __uint_as_float(r1[e + 1]));
+    }
+    const float mnew = fmaxf(m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * k);
+    const float nm = -mnew;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      s0 += ex2_approx(fmaf(__uint_as_float(r0[e]), k, nm));
+      s1 += ex2_approx(fmaf(__uint_as_float(r0[e + 1]), k, nm));
+      s2 += ex2_approx(fmaf(__uint_as_float(r1[e]), k, nm));
+      s3 += ex2_approx(fmaf(__uint_as_float(r1[e + 1]), k, nm));
+    }
+    l = l * ex2_approx(m - mnew) + ((s0 + s1) + (s2 + s3));
+    m = mnew;
+  } else if (nv > 0) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      mx = fmaxf(mx, e < nv ? __uint_as_float(r0[e]) : -INFINITY);
+      mx = fmaxf(mx, e + 32 < nv ? __uint_as_float(r1[e]) : -INFINITY);
+    }
+    const float mnew = fmaxf(m, mx * k);
+    const float nm = -mnew;
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      s0 += e < nv ? ex2_approx(fmaf(__uint_as_float(r0[e]), k, nm)) : 0.0f;
+      s1 += e + 32 < nv ? ex2_approx(fmaf(__uint_as_float(r1[e]), k, nm)) : 0.0f;
+    }
+    l = l * ex2_approx(m - mnew) + (s0 + s1);
+    m = mnew;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __grid_constant__ CoreParams P) {
   using C = CoreCfg<D>;
@@ -139,6 +187,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
   const int g = c / P.grp;                  // its KV head within the shard
   const int q0 = qt * kBQ;
   const int ntiles = qt + 1;   // key tiles 0..qt (qt * 128 < T)
+  const int npairs = (ntiles + 1) >> 1;   // pass-1 score groups of two key tiles
+  const int p1_pos = 2 * npairs;          // ring positions of pass 1
   int* status = P.status;
   const uint64_t tmo = P.timeout_ns;
 
@@ -180,8 +230,9 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
       bool ok = true;
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(sQ + kb * 16384, &P.q[shard], q_full, c * D + kb * 64, q0);
-      // ring sequence: pass 1 K_0..K_{n-1}, pass 2 K_0, V_0, K_1, V_1, ...
-      const int nseq = 3 * ntiles;
+      // ring sequence: pass 1 the pairs (K_0, K_1), (K_2, K_3), ... two positions each; pass 2
+      // K_0, V_0, K_1, V_1, ...
+      const int nseq = p1_pos + 2 * ntiles;
       int issued = 0;
       for (int seq = 0; ok && seq < nseq; ++seq) {
         const int slot = seq % kRing;
@@ -191,9 +242,26 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
           break;
         }
         uint8_t* dst = sRing + slot * C::SLOT;
-        const bool is_v = seq >= ntiles && ((seq - ntiles) & 1);
-        const int j = seq < ntiles ? seq : (seq - ntiles) >> 1;
         mbar_arrive_expect_tx(&ring_full[slot], C::SLOT);
+        if (seq < p1_pos) {
+          // Pass-1 pair m fills the slot pair starting at slot 2m % kRing (even, so the two slots
+          // are adjacent) as one 256-row K-major operand: box (K_{2m+x}, d block kb) at byte
+          // kb * 32 KiB + x * 16 KiB.  Position 2m + h carries the boxes in [h SLOT, (h+1) SLOT).
+          // A K_{2m+1} past the last tile lies above the diagonal (or past T: zero fill); its
+          // scores are masked.
+          const int m = seq >> 1, h = seq & 1;
+          uint8_t* pair_base = dst - h * C::SLOT;
+          for (int kb = 0; kb < C::KB; ++kb)
+            for (int x = 0; x < 2; ++x) {
+              const int off = kb * 32768 + x * 16384;
+              if (off / C::SLOT == h)
+                tma_load_2d(pair_base + off, &P.k[shard], &ring_full[slot], g * D + kb * 64, (2 * m + x) * kBKV);
+            }
+          ++issued;
+          continue;
+        }
+        const bool is_v = (seq - p1_pos) & 1;
+        const int j = (seq - p1_pos) >> 1;
         if (!is_v) {
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_2d(dst + kb * 16384, &P.k[shard], &ring_full[slot], g * D + kb * 64, j * kBKV);
@@ -272,20 +340,44 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
         tc_fence_after_sync();
         return slot;
       };
-      // pass 1: scores only (K_j at position j)
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int slot = wait_pos(j);
-        ok = slot >= 0 && issue_s(slot);
+      // pass 1: scores only, 256 keys per group (K_2m, K_2m+1 at positions 2m, 2m + 1) into a
+      // 256-column score buffer at column 256 b: O and the P buffers are not used yet, so the
+      // whole tensor memory holds two such buffers.  Twice the work per MMA instruction halves
+      // this thread's waits, commits and bookkeeping per key.
+      const uint32_t idesc_w = idesc_bf16_f32(kBQ, 2 * kBKV, false, false);
+      for (int m = 0; ok && m < npairs; ++m) {
+        const int s0 = wait_pos(2 * m);
+        const int s1 = s0 < 0 ? -1 : wait_pos(2 * m + 1);
+        const int b = sj & 1;
+        ok = s1 >= 0 && mbar_wait(&s_empty[b], (static_cast<uint32_t>(sj >> 1) & 1u) ^ 1u, abort_flag, status, tmo);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint64_t kd = smem_desc_sw128(ring0 + s0 * C::SLOT, 16, 1024);
+        for (int kb = 0; kb < C::KB; ++kb) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = desc_advance(qd, kb * 16384 + kk * 32);
+            const uint64_t bd = desc_advance(kd, kb * 32768 + kk * 32);
+            umma_bf16(tmem_base + b * 2 * kBKV, ad, bd, idesc_w, (kb | kk) ? 1u : 0u);
+          }
+        }
+        umma_commit(&ring_empty[s0]);
+        umma_commit(&ring_empty[s1]);
+        umma_commit(&s_full[b]);
+        ++sj;
       }
+      // Pass 2's score buffers (columns [0, 256)) overlap pass 1's buffer 0, whose last group may
+      // be the one just issued: wait until the softmax has read it.
+      if (ok) ok = mbar_wait(&s_empty[(sj - 1) & 1], static_cast<uint32_t>((sj - 1) >> 1) & 1u, abort_flag, status, tmo);
       // pass 2: issue whichever is ready first -- the next score tile S_ns (K_ns at ring position
-      // n + 2 ns, a free score buffer) or the next P_np V_np (V_np at n + 2 np + 1, P_np written)
-      // -- so that a P V never waits behind a late K tile, nor an S behind a late softmax.
+      // p1 + 2 ns, a free score buffer) or the next P_np V_np (V_np at p1 + 2 np + 1, P_np
+      // written) -- so that a P V never waits behind a late K tile, nor an S behind a late softmax.
       int ns = 0, np = 0;
       uint64_t t_idle = globaltimer_ns();
       while (ok && np < ntiles) {
         bool progress = false;
         if (ns < ntiles) {
-          const int pos = ntiles + 2 * ns;
+          const int pos = p1_pos + 2 * ns;
           const int slot = pos % kRing;
           const int b = sj & 1;
           if (mbar_test_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u) &&
@@ -297,7 +389,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
           }
         }
         if (ok && np < ns) {
-          const int pos = ntiles + 2 * np + 1;
+          const int pos = p1_pos + 2 * np + 1;
           const int vslot = pos % kRing;
           const int b = np & 1;
           if (mbar_test_wait(&ring_full[vslot], static_cast<uint32_t>(pos / kRing) & 1u) &&
@@ -339,7 +431,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
   } else {
     // ------------------------------------------------------------------ softmax warps
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;          // keys [half 64, half 64 + 64) of each tile
+    const int half = (warp - 2) >> 2;          // pass 2: keys [64 half, 64 half + 64) of each tile
     const int r = quad * 32 + lane;            // row within the query tile
     const int q = q0 + r;                      // query index
     const bool row_ok = q < P.T;
@@ -347,9 +439,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
     int sj = 0;
-    // pass 1: running max and sum over the keys <= q
+    // pass 1: running max and sum over the keys <= q, 256 keys per score group (this warp: 128
+    // of them, in two chunks of 64)
     float m = -INFINITY, l = 0.0f;
-    for (int j = 0; j < ntiles; ++j, ++sj) {
+    for (int pg = 0; pg < npairs; ++pg, ++sj) {
       const int b = sj & 1;
       ok = ok && mbar_wait(&s_full[b], static_cast<uint32_t>(sj >> 1) & 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -357,54 +450,19 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
         break;
       }
       tc_fence_after_sync();
-      uint32_t r0[32], r1[32];
-      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64, r0);
-      tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64 + 32, r1);
+      uint32_t ra[32], rb[32], rc[32], rd[32];
+      const uint32_t col = lane_base + b * 2 * kBKV + half * kBKV;
+      tmem_ld_32x32b_x32(col, ra);
+      tmem_ld_32x32b_x32(col + 32, rb);
+      tmem_ld_32x32b_x32(col + 64, rc);
+      tmem_ld_32x32b_x32(col + 96, rd);
       tmem_ld_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);
-      const int key0 = j * kBKV + half * 64;
-      const int nv = min(64, q - key0 + 1);    // valid keys of this row among the 64
-      if (nv >= 64) {                          // below the diagonal: no mask
-        float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          x0 = fmaxf(x0, __uint_as_float(r0[e]));
-          x1 = fmaxf(x1, __uint_as_float(r0[e + 1]));
-          x2 = fmaxf(x2, __uint_as_float(r1[e]));
-          x3 = fmaxf(x3, __uint_as_float(r1[e + 1]));
-        }
-        const float mnew = fmaxf(m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * k);
-        const float nm = -mnew;
-        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          s0 += ex2_approx(fmaf(__uint_as_float(r0[e]), k, nm));
-          s1 += ex2_approx(fmaf(__uint_as_float(r0[e + 1]), k, nm));
-          s2 += ex2_approx(fmaf(__uint_as_float(r1[e]), k, nm));
-          s3 += ex2_approx(fmaf(__uint_as_float(r1[e + 1]), k, nm));
-        }
-        l = l * ex2_approx(m - mnew) + ((s0 + s1) + (s2 + s3));
-        m = mnew;
-      } else if (nv > 0) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          mx = fmaxf(mx, e < nv ? __uint_as_float(r0[e]) : -INFINITY);
-          mx = fmaxf(mx, e + 32 < nv ? __uint_as_float(r1[e]) : -INFINITY);
-        }
-        const float mnew = fmaxf(m, mx * k);
-        const float nm = -mnew;
-        float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          s0 += e < nv ? ex2_approx(fmaf(__uint_as_float(r0[e]), k, nm)) : 0.0f;
-          s1 += e + 32 < nv ? ex2_approx(fmaf(__uint_as_float(r1[e]), k, nm)) : 0.0f;
-        }
-        l = l * ex2_approx(m - mnew) + (s0 + s1);
-        m = mnew;
-      }
+      const int key0 = pg * 2 * kBKV + half * kBKV;
+      row_stats64(ra, rb, q - key0 + 1, k, m, l);
+      row_stats64(rc, rd, q - key0 - 63, k, m, l);
     }
     // combine the two halves of each row (every softmax warp reaches this barrier)
     xch[half * kBQ + r] = make_float2(m, l);
