@@ -991,7 +991,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
     mbar_init(v_full, 1);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&ring_full[s], 1);
-      mbar_init(&ring_empty[s], 2);   // a dO tile: the dP and the dV MMAs; a Q tile: two commits after dK
+      mbar_init(&ring_empty[s], 1);   // one commit after the tile's last MMA (dV for dO, dK for Q)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dp_full[b], 1);
@@ -1128,7 +1128,6 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
             }
           }
           umma_commit(&dp_full[b]);
-          umma_commit(&ring_empty[dslot]);          // first of the dO tile's two releases
           // dV += P_j^T dO_j: A = P tile read MN-major (keys contiguous), B = dO tile read MN-major
           if (!mbar_wait(&pb_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo)) {
             ok = false;
@@ -1144,7 +1143,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
             umma_bf16(t_dv, ad, bd, idesc_acc, (j | kq) ? 1u : 0u);
           }
           umma_commit(&pv_done[b]);
-          umma_commit(&ring_empty[dslot]);          // second release of the dO tile
+          umma_commit(&ring_empty[dslot]);          // the dO tile's last MMA (dP's are earlier)
         }
         if (ok && j > 0) {
           // dK += dS_(j-1)^T Q_(j-1): A = dS (in the P buffer) MN-major, B = Q tile MN-major
@@ -1165,7 +1164,6 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
             umma_bf16(t_dk, ad, bd, idesc_acc, (jp | kq) ? 1u : 0u);
           }
           umma_commit(&pb_empty[b]);
-          umma_commit(&ring_empty[qslot]);          // a Q tile is released by two commits
           umma_commit(&ring_empty[qslot]);
           qslot_prev = qslot;
         }
