@@ -706,10 +706,13 @@ def time_oracle(tokens: int, reps: int, warm: int = 0, min_seconds: float = 0.0)
 
 
 def cpu_cores():
+    """Host threads the oracle's numpy runs on: the usable cores, capped by OMP_NUM_THREADS."""
     try:
-        return len(os.sched_getaffinity(0))
+        n = len(os.sched_getaffinity(0))
     except AttributeError:
-        return os.cpu_count()
+        n = os.cpu_count()
+    omp = os.environ.get("OMP_NUM_THREADS", "")
+    return min(n, int(omp)) if omp.isdigit() and int(omp) > 0 else n
 
 
 def cpu_baseline(tokens: int, seconds: float) -> dict:
@@ -741,6 +744,15 @@ def run_reference(args, dist):
 
 def main():
     args = parse()
+    if args.impl == "reference" and os.environ.get("RANK", "0") == "0":
+        # Under torchrun every rank gets OMP_NUM_THREADS=1; rank 0 alone runs the oracle here (the
+        # other ranks exit without work), so it takes every core.  Set before numpy is loaded.
+        try:
+            ncores = str(len(os.sched_getaffinity(0)))
+        except AttributeError:
+            ncores = str(os.cpu_count())
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+            os.environ[var] = ncores
     dist = Dist(args.gpus)
     try:
         if args.only:
@@ -756,7 +768,7 @@ def main():
             out = run_reference(args, dist)
         else:
             out = run_ours(args, dist)
-            if dist.rank == 0 and not args.no_cpu_baseline:
+            if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
                 out["cpu_baseline"] = cpu_baseline(args.cpu_tokens, args.cpu_seconds)
         if dist.rank == 0 and out is not None:
             print(json.dumps(out), flush=True)
