@@ -722,6 +722,7 @@ def cpu_baseline(tokens: int, seconds: float) -> dict:
     total = sum(times)
     return {"value": round(flops * len(times) / total / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(),
             "kind": "oracle",
+            "extrapolated_full_step_s": round(total / len(times) * MLP["T"] / tokens, 1),
             "sample": f"fp64 numpy oracle, sharded t=8 SwiGLU MLP fwd+bwd on {tokens} of 8192 tokens "
                       f"(full weights), {len(times)} repetitions, {total:.1f} s"}
 
