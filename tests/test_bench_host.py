@@ -56,3 +56,24 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["metric"].startswith("TP-sharded MLP fwd+bwd")
+
+
+def test_reference_arm_takes_every_core_when_launched_with_one_thread():
+    # torchrun hands every rank OMP_NUM_THREADS=1; rank 0 of the reference arm runs the oracle alone
+    # and must report (and use) every usable core.
+    env = dict(os.environ, OMP_NUM_THREADS="1", RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--cpu-tokens", "8"], capture_output=True, text=True, timeout=600,
+                       env=env)
+    assert r.returncode == 0, r.stderr
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][0])
+    assert d["cpu_baseline"]["cores"] == len(os.sched_getaffinity(0))
+
+
+def test_cpu_cores_honours_omp_num_threads(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("OMP_NUM_THREADS", "1")
+    assert bench.cpu_cores() == 1
+    monkeypatch.delenv("OMP_NUM_THREADS")
+    assert bench.cpu_cores() == len(os.sched_getaffinity(0))
