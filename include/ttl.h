@@ -330,7 +330,7 @@ int ttl_vocab_parallel_embedding_bwd(int t, int64_t T, int64_t h, int64_t V, con
  *   ws   unused: ttl_tp_attn_fwd_workspace_size() returns 0 and ws may be null.  The scores
  *        and the softmax statistics stay on chip: one fused kernel per 128-query tile computes
  *        the scores twice in tensor memory (exact row statistics, then the probabilities, which
- *        feed P V straight from shared memory)
+ *        feed P V from tensor memory)
  * t | n_q, t | n_kv, n_kv | n_q, d = 64 or 128, T and h multiples of 8.  Errors:
  * TTL_ERR_ARG (null or short arguments), TTL_ERR_SHAPE, TTL_ERR_ALIGN (pointers not 16-byte
  * aligned); nothing is launched when the call returns an error. */

@@ -152,3 +152,19 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(b, "_lib", None)
     with pytest.raises(ImportError):
         b.lib()
+
+
+def test_every_declaration_is_documented():
+    # Each entry point carries the contract right above it: a comment block (its own, or its
+    # section's when declarations share one) with nothing but blank lines between them.
+    lines = open(os.path.join(ROOT, "include", "ttl.h")).read().splitlines()
+    for i, line in enumerate(lines):
+        m = re.match(r"^(?:int|size_t|const char\*)\s+(ttl_[a-z0-9_]+)\s*\(", line)
+        if not m:
+            continue
+        j = i - 1
+        # blank lines, and the lines of declarations grouped under the same comment
+        while j >= 0 and (not lines[j].strip() or not lines[j].lstrip().startswith(("/*", "*", "#", "}"))
+                          and not lines[j].rstrip().endswith("*/")):
+            j -= 1
+        assert j >= 0 and lines[j].rstrip().endswith("*/"), f"{m.group(1)} has no comment block above it"
