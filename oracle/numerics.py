@@ -67,8 +67,3 @@ def round_to_bf16(x) -> np.ndarray:
         out[nan] = np.float32(np.nan)
     return out
 
-
-def bf16_bits(x) -> np.ndarray:
-    """The 16-bit patterns of float32 values that are already bf16-representable."""
-    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from conftest import golden
-from oracle import accounting, gtp, vocab_ce
+from oracle import accounting, gtp, tp_mlp, vocab_ce
 
 MiB = 1 << 20
 
@@ -80,6 +80,94 @@ def test_deferred_finalize_visibility_and_result():
     assert d["updated_after_step"][0] == list(range(L))
 
 
+
+# GTP GEMMs on the gathered slice (GTP page, concepts "GTP_remat" and "Prefetch chain": the
+# gathered TP slice is an ordinary GEMM operand, forward X W and backward dY W^T).
+
+def _triple_loop(A, B):
+    M, K = A.shape
+    K2, N = B.shape
+    assert K == K2
+    C = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += float(A[m, k]) * float(B[k, n])
+            C[m, n] = acc
+    return C
+
+
+def test_gtp_forward_gemm_printed_example_and_scalar_loops():
+    g = golden("tp_split_2x2.json")
+    assert gtp.forward_gemm(np.array(g["X"], float), np.array(g["A"], float)).tolist() == g["XA"]
+    rng = np.random.default_rng(21)
+    M, K, N = 3, 8, 5                                   # M, K, N all different
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((K, N))
+    Y = gtp.forward_gemm(X, W)
+    assert Y.shape == (M, N)
+    np.testing.assert_allclose(Y, _triple_loop(X, W), rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_gtp_forward_on_gathered_shards_is_the_row_split_sum(g):
+    """Shard j holds rows j of the slice, i.e. the row-split weight of the TP/SP page's block
+    identity [X_1, X_2][A_1; A_2] = X_1 A_1 + X_2 A_2: the GEMM on the gathered slice must equal
+    the sum of the per-shard partials on the matching column blocks of X."""
+    rng = np.random.default_rng(30 + g)
+    M, K, N = 5, 16, 3
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((K, N))
+    sh = gtp.shard_rows(W, g)
+    kb = K // g
+    parts = tp_mlp.row_parallel_partials([X[:, j * kb:(j + 1) * kb] for j in range(g)], sh)
+    np.testing.assert_allclose(gtp.forward_gemm(X, gtp.gather(sh)), sum(parts), rtol=1e-12, atol=1e-13)
+    # the slice as one column-parallel shard gives the same output
+    np.testing.assert_allclose(gtp.forward_gemm(X, gtp.gather(sh)),
+                               tp_mlp.column_parallel_forward(X, [W])[0], rtol=1e-13, atol=1e-14)
+
+
+def test_gtp_dgrad_gemm_scalar_loops_and_finite_differences():
+    """dgrad is the gradient of sum(Y * dY) with respect to X, for Y = X W: checked by central
+    differences of the forward GEMM (a square, non-symmetric W would hide W in place of W^T
+    from a shape check, so both a square and a rectangular case run)."""
+    rng = np.random.default_rng(22)
+    for (M, K, N) in [(4, 5, 5), (3, 6, 4)]:
+        X = rng.standard_normal((M, K))
+        W = rng.standard_normal((K, N))
+        dY = rng.standard_normal((M, N))
+        dX = gtp.dgrad_gemm(dY, W)
+        assert dX.shape == (M, K)
+        np.testing.assert_allclose(dX, _triple_loop(dY, np.ascontiguousarray(W.T)), rtol=1e-13, atol=1e-14)
+        eps = 1e-6
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            a = X.copy(); a[idx] += eps
+            b = X.copy(); b[idx] -= eps
+            num[idx] = (np.sum(gtp.forward_gemm(a, W) * dY) - np.sum(gtp.forward_gemm(b, W) * dY)) / (2 * eps)
+        np.testing.assert_allclose(dX, num, rtol=1e-7, atol=1e-8)
+    # torch autograd of the same scalar
+    Xt = torch.tensor(X, requires_grad=True)
+    (Xt @ torch.tensor(W) * torch.tensor(dY)).sum().backward()
+    np.testing.assert_allclose(gtp.dgrad_gemm(dY, W), Xt.grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_gtp_dgrad_on_gathered_shards_equals_per_shard_row_blocks():
+    """dX = dY W^T on the gathered slice: its column block j equals dY shard_j^T, the backward of
+    shard j's rows alone (what a rank that holds only shard j could compute)."""
+    rng = np.random.default_rng(23)
+    M, K, N, g = 4, 16, 6, 8
+    dY = rng.standard_normal((M, N))
+    W = rng.standard_normal((K, N))
+    sh = gtp.shard_rows(W, g)
+    dX = gtp.dgrad_gemm(dY, gtp.gather(sh))
+    kb = K // g
+    for j in range(g):
+        np.testing.assert_allclose(dX[:, j * kb:(j + 1) * kb], _triple_loop(dY, np.ascontiguousarray(sh[j].T)),
+                                   rtol=1e-13, atol=1e-14)
+
+
 # ---------------------------------------------------------------- vocab-parallel CE
 
 def test_vocab_shard_sizes():
@@ -108,6 +196,27 @@ def test_sharded_ce_equals_textbook_and_torch(t):
     assert math.isclose(r["loss"], tl.item(), rel_tol=1e-12)
     np.testing.assert_allclose(ref["dZ"], lt.grad.numpy(), rtol=1e-10, atol=1e-15)
     np.testing.assert_allclose(r["dH"], ref["dZ"] @ W, rtol=1e-12, atol=1e-14)
+
+
+
+def test_ce_shard_helpers_directly():
+    """The per-shard pieces on their own: the logits GEMM against scalar loops (W is [V, h], so
+    Z_i = H W_i^T), and one shard's dlogits against torch's gradient columns of that shard."""
+    rng = np.random.default_rng(13)
+    T, h, V, t = 4, 3, 10, 2
+    H = rng.standard_normal((T, h))
+    W = rng.standard_normal((V, h))
+    target = np.array([0, 9, 5, 4])
+    Vs = V // t
+    Z1 = vocab_ce.lm_head_logits(H, W[Vs:])
+    np.testing.assert_allclose(Z1, _triple_loop(H, np.ascontiguousarray(W[Vs:].T)), rtol=1e-13, atol=1e-14)
+    lt = torch.tensor(H @ W.T, requires_grad=True)
+    torch.nn.functional.cross_entropy(lt, torch.tensor(target), reduction="mean").backward()
+    lse = np.log(np.exp(H @ W.T).sum(axis=1))
+    for i in range(t):
+        Zi = vocab_ce.lm_head_logits(H, W[i * Vs:(i + 1) * Vs])
+        d = vocab_ce.dlogits_shard(Zi, target, i * Vs, lse, T)
+        np.testing.assert_allclose(d, lt.grad.numpy()[:, i * Vs:(i + 1) * Vs], rtol=1e-10, atol=1e-15)
 
 
 def test_ce_special_cases_and_invariants():

@@ -154,3 +154,27 @@ def test_row_softmax_without_normalisation_is_caught(monkeypatch):
         return np.exp(s - s.max())                                # the division by the sum dropped
     monkeypatch.setattr(attention, "_softmax_vec", bad)
     _expect_failure(tatt.test_row_functions_match_torch_autograd)
+
+
+def test_gtp_dgrad_without_transpose_is_caught(monkeypatch):
+    def bad(dY, W):
+        return np.asarray(dY, float) @ np.asarray(W, float)      # W instead of W^T (square case)
+    monkeypatch.setattr(gtp, "dgrad_gemm", bad)
+    _expect_failure(tgce.test_gtp_dgrad_gemm_scalar_loops_and_finite_differences)
+
+
+def test_gtp_forward_with_transposed_slice_is_caught(monkeypatch):
+    def bad(X, W):
+        return np.asarray(X, float) @ np.asarray(W, float).T
+    monkeypatch.setattr(gtp, "forward_gemm", bad)
+    _expect_failure(tgce.test_gtp_forward_gemm_printed_example_and_scalar_loops)
+
+
+def test_row_backward_with_wrong_shard_weight_is_caught(monkeypatch):
+    def bad(X_slices, W_shards, dY):
+        dY = np.asarray(dY, float)
+        dW = [np.asarray(x, float).T @ dY for x in X_slices]
+        dX = [dY @ np.asarray(w, float).T for w in W_shards[::-1]]   # shard order reversed
+        return dW, dX
+    monkeypatch.setattr(tp_mlp, "row_parallel_backward", bad)
+    _expect_failure(ttp.test_row_parallel_backward_2x2_example_and_finite_differences)

@@ -45,6 +45,47 @@ def test_column_parallel_t3_printed_table():
     assert dX[0].tolist() == g["dX_all_reduced"]
 
 
+
+def test_row_parallel_backward_2x2_example_and_finite_differences():
+    """Row layer backward (table "Column 和 Row 各在哪里通信": dY is full on every shard, both
+    gradients are local).  The printed 2x2 row split X = [1, 2], A = [[1,2],[3,4]] is run
+    backwards with dY = [1, 1]: dX_i = dY A_i^T gives [3] and [7], dA_i = X_i^T dY gives
+    [[1, 1]] and [[2, 2]].  Then central differences of sum_i sum(P_i * dY) on a random case, and
+    the invariant that the dX slices side by side are the unsharded dY A^T."""
+    g = golden("tp_split_2x2.json")
+    X = np.array(g["X"], float)
+    A = np.array(g["A"], float)
+    X_sl = [X[:, 0:1], X[:, 1:2]]
+    dY = np.array([[1.0, 1.0]])
+    dW, dX = tp_mlp.row_parallel_backward(X_sl, tp_mlp.split_rows(A, 2), dY)
+    assert [d.tolist() for d in dX] == [[[3.0]], [[7.0]]]
+    assert [d.tolist() for d in dW] == [[[1.0, 1.0]], [[2.0, 2.0]]]
+
+    rng = np.random.default_rng(41)
+    T, k, n, t = 3, 6, 4, 3
+    Xf = rng.standard_normal((T, k))
+    W = rng.standard_normal((k, n))
+    dY = rng.standard_normal((T, n))
+    Wsh = tp_mlp.split_rows(W, t)
+    X_sl = [Xf[:, i * (k // t):(i + 1) * (k // t)] for i in range(t)]
+    dW, dX = tp_mlp.row_parallel_backward(X_sl, Wsh, dY)
+
+    def loss(xs, ws):
+        return sum(np.sum(p * dY) for p in tp_mlp.row_parallel_partials(xs, ws))
+    eps = 1e-6
+    for i in range(t):
+        for idx in np.ndindex(X_sl[i].shape):
+            a = [x.copy() for x in X_sl]; a[i][idx] += eps
+            b = [x.copy() for x in X_sl]; b[i][idx] -= eps
+            assert abs((loss(a, Wsh) - loss(b, Wsh)) / (2 * eps) - dX[i][idx]) < 1e-7
+        for idx in np.ndindex(Wsh[i].shape):
+            a = [w.copy() for w in Wsh]; a[i][idx] += eps
+            b = [w.copy() for w in Wsh]; b[i][idx] -= eps
+            assert abs((loss(X_sl, a) - loss(X_sl, b)) / (2 * eps) - dW[i][idx]) < 1e-7
+    np.testing.assert_allclose(np.concatenate(dX, axis=1), dY @ W.T, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(np.concatenate(dW, axis=0), Xf.T @ dY, rtol=1e-13, atol=1e-14)
+
+
 def test_relu_counterexample_row_then_column_is_wrong():
     g = golden("relu_counterexample.json")
     relu = lambda x: np.maximum(x, 0.0)  # noqa: E731
