@@ -5,9 +5,15 @@ Tolerances (bf16 operands, fp32 accumulation):
   * bf16 GEMM outputs: relative Frobenius error <= 5e-3 and max-abs error <= 2e-2 * max|ref|;
   * fp32 reductions and the CE loss: relative error <= 1e-5;
   * gathers, scatters, copies and the ordered bf16 reductions: bit-exact;
-  * the attention block's outputs, which sit at the end of a chain of up to seven bf16
-    roundings (Q/K/V, P, O, dO, dS, dQ/dK/dV, the output itself), each at most 2^-9 relative:
-    relative Frobenius error <= 5 * 2^-9 ~ 1e-2 and max-abs error <= 2e-2 * max|ref|.
+  * the attention block's outputs sit at the end of a chain of up to seven bf16 roundings
+    (Q/K/V, P, O, dO, dS, dQ/dK/dV, the output itself).  They are compared twice:
+      - against the oracle's rounding mirror (the same float64 arithmetic rounded to bf16 where
+        the bf16 data path materialises a tensor) at the GEMM bounds above, 5e-3 and 2e-2;
+      - against the plain float64 oracle at relative Frobenius error <= 1.05e-2 and max-abs
+        <= 2e-2 * max|ref|.  The 1.05e-2 is the triangle inequality over the two measured legs:
+        5e-3 allowed between the kernels and the mirror, plus 5.5e-3 for the mirror's own
+        distance from float64 (largest measured over the eight small test blocks: 5.14e-3, on
+        dWk; the cancellation in dS = P (dP - D) amplifies the roundings of dP and D).
 """
 import numpy as np
 import torch
@@ -15,8 +21,10 @@ import torch
 REL_FRO = 5e-3
 MAX_ABS_FRAC = 2e-2
 REL_FP32 = 1e-5
-ATTN_REL_FRO = 1e-2
-ATTN_MAX_ABS_FRAC = 2e-2
+ATTN_MIRROR_REL_FRO = 5e-3
+ATTN_MIRROR_MAX_ABS_FRAC = 2e-2
+ATTN_FP64_REL_FRO = 5e-3 + 5.5e-3
+ATTN_FP64_MAX_ABS_FRAC = 2e-2
 
 
 def f64(t: torch.Tensor) -> np.ndarray:

@@ -1,6 +1,7 @@
 """Head-split TP attention block, forward and backward through the C ABI, vs the fp64 oracle
-(GPU).  Small shapes are compared element by element; the Qwen3-8B shape (T=8192, h=4096,
-32 query / 8 KV heads of 128, t=8) on sampled rows and through causality properties."""
+and its bf16 rounding mirror (GPU).  Small shapes are compared element by element; the
+Qwen3-8B shape (T=8192, h=4096, 32 query / 8 KV heads of 128, t=8) on sampled rows and through
+causality properties."""
 import os
 import subprocess
 import sys
@@ -12,7 +13,8 @@ import torch
 import synth_inputs as si
 import tensor_transformer_layer_way_gb300 as ttl
 from oracle import attention
-from parity import ATTN_MAX_ABS_FRAC, ATTN_REL_FRO, dev, f64, gemm_errors
+from parity import (ATTN_FP64_MAX_ABS_FRAC, ATTN_FP64_REL_FRO, ATTN_MIRROR_MAX_ABS_FRAC, ATTN_MIRROR_REL_FRO,
+                    dev, f64, gemm_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,24 +43,32 @@ def _run(inp, t, n_q, n_kv, d, backward=True):
 
 
 class _Errors:
-    """Collects (name, relative Frobenius error, max-abs / max|ref|) and checks each against
-    the attention tolerance (single projections: the GEMM one); prints the table."""
+    """Collects each output's errors against the float64 oracle and, where given, against the
+    rounding mirror, and checks them: the mirror at the GEMM bounds, float64 at the attention
+    bounds (single projections: the GEMM bounds against both).  Prints the table."""
 
     def __init__(self):
         self.rows = []
 
-    def add(self, got, ref, name, gemm=False):
+    def add(self, got, ref, name, mirror=None, gemm=False):
         rf, maf = gemm_errors(got, ref, name)
-        self.rows.append((name, rf, maf, gemm))
+        mrf, mmaf = gemm_errors(got, mirror, name) if mirror is not None else (None, None)
+        self.rows.append((name, rf, maf, mrf, mmaf, gemm))
 
     def check(self):
-        for name, rf, maf, gemm in self.rows:
-            print(f"{name:14s} rel_fro {rf:.3e}  max_abs/max {maf:.3e}")
-        for name, rf, maf, gemm in self.rows:
-            lim_rf = 5e-3 if gemm else ATTN_REL_FRO
-            lim_ma = 2e-2 if gemm else ATTN_MAX_ABS_FRAC
-            assert rf <= lim_rf, f"{name}: relative Frobenius error {rf:.3e} > {lim_rf}"
-            assert maf <= lim_ma, f"{name}: max-abs error {maf:.3e} of max|ref| > {lim_ma}"
+        for name, rf, maf, mrf, mmaf, gemm in self.rows:
+            m = f"  mirror {mrf:.3e} / {mmaf:.3e}" if mrf is not None else ""
+            print(f"{name:14s} fp64 rel_fro {rf:.3e}  max_abs/max {maf:.3e}{m}")
+        for name, rf, maf, mrf, mmaf, gemm in self.rows:
+            lim_rf = 5e-3 if gemm else ATTN_FP64_REL_FRO
+            lim_ma = 2e-2 if gemm else ATTN_FP64_MAX_ABS_FRAC
+            assert rf <= lim_rf, f"{name}: relative Frobenius error {rf:.3e} > {lim_rf} (fp64)"
+            assert maf <= lim_ma, f"{name}: max-abs error {maf:.3e} of max|ref| > {lim_ma} (fp64)"
+            if mrf is not None:
+                assert mrf <= ATTN_MIRROR_REL_FRO, f"{name}: relative Frobenius error {mrf:.3e} > " \
+                                                   f"{ATTN_MIRROR_REL_FRO} (mirror)"
+                assert mmaf <= ATTN_MIRROR_MAX_ABS_FRAC, f"{name}: max-abs error {mmaf:.3e} of max|ref| > " \
+                                                         f"{ATTN_MIRROR_MAX_ABS_FRAC} (mirror)"
 
 
 def _W64(inp):
@@ -95,22 +105,24 @@ def test_small_blocks_match_oracle(t, T, h, n_q, n_kv, d):
     X, dY = f64(inp["X"]), f64(inp["dY"])
     rf = attention.tp_attention_forward(X, W, t, n_q, n_kv, d)
     rb = attention.tp_attention_backward(X, W, t, n_q, n_kv, d, dY, rf)
+    mf = attention.tp_attention_forward(X, W, t, n_q, n_kv, d, mirror=True)
+    mb = attention.tp_attention_backward(X, W, t, n_q, n_kv, d, dY, mf, mirror=True)
     lower = np.tril(np.ones((T, T), dtype=bool))
     err = _Errors()
     for i in range(t):
         for k in ("Q", "K", "V"):
-            err.add(f64(fwd[k][i]), rf[k][i], f"{k}[{i}]", gemm=True)
-        err.add(f64(fwd["O"][i]), rf["O"][i], f"O[{i}]")
+            err.add(f64(fwd[k][i]), rf[k][i], f"{k}[{i}]", mf[k][i], gemm=True)
+        err.add(f64(fwd["O"][i]), rf["O"][i], f"O[{i}]", mf["O"][i])
         for c in range(n_q // t):
             Pg = f64(fwd["P"][i][c])
-            err.add(Pg[lower], rf["P"][i][c][lower], f"P[{i}][{c}]")
+            err.add(Pg[lower], rf["P"][i][c][lower], f"P[{i}][{c}]", mf["P"][i][c][lower])
         _check_p_band(fwd["P"][i], T)
         assert torch.equal(fwd["Y"][i], fwd["Y"][0])
         for k in ("dWq", "dWk", "dWv", "dWo"):
-            err.add(f64(bwd[k][i]), rb[k][i], f"{k}[{i}]")
+            err.add(f64(bwd[k][i]), rb[k][i], f"{k}[{i}]", mb[k][i])
         assert torch.equal(bwd["dX"][i], bwd["dX"][0])
-    err.add(f64(fwd["Y"][0]), rf["Y"], "Y")
-    err.add(f64(bwd["dX"][0]), rb["dX"], "dX")
+    err.add(f64(fwd["Y"][0]), rf["Y"], "Y", mf["Y"])
+    err.add(f64(bwd["dX"][0]), rb["dX"], "dX", mb["dX"])
     err.check()
 
 
@@ -179,10 +191,11 @@ def test_qwen3_forward_sampled_rows(qwen3):
     fwd, _ = _run(inp, s.t, s.n_q, s.n_kv, s.d, backward=False)
     rows = si.sample_indices(s.T, 24, s.seed).numpy()
     ref = attention.forward_rows(f64(inp["X"]), _W64(inp), s.n_q, s.n_kv, s.d, rows)
+    mir = attention.forward_rows(f64(inp["X"]), _W64(inp), s.n_q, s.n_kv, s.d, rows, t=s.t, mirror=True)
     for i in range(s.t):
         assert torch.equal(fwd["Y"][i], fwd["Y"][0])
     err = _Errors()
-    err.add(f64(fwd["Y"][0][rows]), ref, "Y[sampled]")
+    err.add(f64(fwd["Y"][0][rows]), ref, "Y[sampled]", mir)
     err.check()
     for i in (0, s.t - 1):
         Ps = fwd["P"][i][:, rows, :].float()
@@ -219,12 +232,14 @@ def test_qwen3_backward_with_dY_on_the_first_rows_only():
     X, dY = f64(inp["X"])[:m], f64(inp["dY"])[:m]
     rf = attention.tp_attention_forward(X, W, s.t, s.n_q, s.n_kv, s.d)
     rb = attention.tp_attention_backward(X, W, s.t, s.n_q, s.n_kv, s.d, dY, rf)
+    mf = attention.tp_attention_forward(X, W, s.t, s.n_q, s.n_kv, s.d, mirror=True)
+    mb = attention.tp_attention_backward(X, W, s.t, s.n_q, s.n_kv, s.d, dY, mf, mirror=True)
     assert torch.count_nonzero(bwd["dX"][0][m:]) == 0
     err = _Errors()
-    err.add(f64(bwd["dX"][0][:m]), rb["dX"], "dX[:m]")
+    err.add(f64(bwd["dX"][0][:m]), rb["dX"], "dX[:m]", mb["dX"])
     for i in range(s.t):
         for k in ("dWq", "dWk", "dWv", "dWo"):
-            err.add(f64(bwd[k][i]), rb[k][i], f"{k}[{i}]")
+            err.add(f64(bwd[k][i]), rb[k][i], f"{k}[{i}]", mb[k][i])
     err.check()
     del fwd, bwd
     torch.cuda.empty_cache()

@@ -122,3 +122,70 @@ def test_gradient_of_rows_beyond_the_last_nonzero_dY_row_is_zero():
     for k in ("dWq", "dWk", "dWv", "dWo"):
         for i in range(t):
             np.testing.assert_allclose(full[k][i], cut[k][i], rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- the bf16 rounding mirror
+
+def _mirror_case(seed=8):
+    rng = np.random.default_rng(seed)
+    T, h, n_q, n_kv, d, t = 24, 16, 4, 2, 8, 2
+    W = {"Wq": rng.standard_normal((h, n_q * d)) / 4, "Wk": rng.standard_normal((h, n_kv * d)) / 4,
+         "Wv": rng.standard_normal((h, n_kv * d)) / 4, "Wo": rng.standard_normal((n_q * d, h)) / 6}
+    X = rng.standard_normal((T, h))
+    dY = rng.standard_normal((T, h))
+    return X, W, dY, t, n_q, n_kv, d
+
+
+def _block(X, W, dY, t, n_q, n_kv, d, mirror):
+    f = attention.tp_attention_forward(X, W, t, n_q, n_kv, d, mirror=mirror)
+    b = attention.tp_attention_backward(X, W, t, n_q, n_kv, d, dY, f, mirror=mirror)
+    return f, b
+
+
+def _outputs(f, b, t):
+    out = {"Y": f["Y"], "dX": b["dX"]}
+    for i in range(t):
+        for k in ("Q", "K", "V", "O"):
+            out[f"{k}{i}"] = f[k][i]
+        for c, p in enumerate(f["P"][i]):
+            out[f"P{i}_{c}"] = p
+        for k in ("dWq", "dWk", "dWv", "dWo"):
+            out[f"{k}{i}"] = b[k][i]
+    return out
+
+
+def test_mirror_with_rounding_switched_off_is_the_float64_block(monkeypatch):
+    """The mirror adds nothing but roundings: with the rounding replaced by the identity it
+    returns exactly the float64 block, output for output."""
+    X, W, dY, t, n_q, n_kv, d = _mirror_case()
+    ref = _outputs(*_block(X, W, dY, t, n_q, n_kv, d, False), t)
+    monkeypatch.setattr(attention, "round_to_bf16", lambda a: np.asarray(a, dtype=np.float64))
+    got = _outputs(*_block(X, W, dY, t, n_q, n_kv, d, True), t)
+    for k in ref:
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+
+
+def test_mirror_outputs_are_bf16_values_near_the_float64_block():
+    """Every mirrored output is a bf16 value (the rounding happened), and the chain of roundings
+    moves each output by a few bf16 half-ulps: relative Frobenius distance from the float64
+    block between 1e-4 and 2e-2 (about 2^-9 per rounding; the cancellation in dS = P (dP - D)
+    amplifies the errors of dP and D, most in the query-side gradients of short sequences)."""
+    from oracle import numerics
+    X, W, dY, t, n_q, n_kv, d = _mirror_case()
+    ref = _outputs(*_block(X, W, dY, t, n_q, n_kv, d, False), t)
+    got = _outputs(*_block(X, W, dY, t, n_q, n_kv, d, True), t)
+    for k, v in got.items():
+        np.testing.assert_array_equal(numerics.round_to_bf16(v).astype(np.float64), v, err_msg=k)
+        rf = np.linalg.norm(v - ref[k]) / np.linalg.norm(ref[k])
+        assert 1e-4 < rf < 2e-2, (k, rf)
+
+
+def test_mirror_forward_rows_equal_the_mirrored_block():
+    X, W, dY, t, n_q, n_kv, d = _mirror_case(9)
+    f = attention.tp_attention_forward(X, W, t, n_q, n_kv, d, mirror=True)
+    rows = np.array([0, 5, 17, 23])
+    got = attention.forward_rows(X, W, n_q, n_kv, d, rows, t=t, mirror=True)
+    # the same roundings on row-wise products: equal up to a rare one-ulp flip where the
+    # float64 product lands within its last bits of a bf16 rounding boundary
+    assert np.linalg.norm(got - f["Y"][rows]) <= 1e-3 * np.linalg.norm(f["Y"][rows])
+    assert np.mean(got == f["Y"][rows]) > 0.95
