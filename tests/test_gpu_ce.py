@@ -85,7 +85,11 @@ def test_fused_and_separate_statistics_agree():
 
 @pytest.mark.parametrize("fused", [True, False])
 def test_vocab_parallel_ce_full_size_sampled(fused):
-    """H [8192, 4096], W [151936, 4096] in 8 vocab shards of 18992 rows (fp32 logits 4.98 GB)."""
+    """H [8192, 4096], W [151936, 4096] in 8 vocab shards of 18992 rows (fp32 logits 4.98 GB).
+    On sampled token rows, for every shard: the fp32 logits over all 18992 columns (the last
+    256-wide tile holds only 48 of them), the three statistics, and the bf16 dlogits; then the
+    combined statistics, the per-token loss and dH.  The mean loss is checked as the mean of
+    the per-token losses, which the oracle pins on the sample."""
     cfg = si.VOCAB_CE_T8
     inp = si.ce_inputs(cfg.T, cfg.h, cfg.V, cfg.seed)
     out = _run(inp["H"], inp["W"], inp["target"], cfg.t, fused=fused)
@@ -93,10 +97,22 @@ def test_vocab_parallel_ce_full_size_sampled(fused):
     rows = si.sample_indices(cfg.T, 48, cfg.seed).numpy()
     ref = vocab_ce.vocab_parallel_ce(f64(inp["H"]), f64(inp["W"]), inp["target"].numpy(), cfg.t, rows=rows)
     stats = f32(out["stats"]).reshape(3 * cfg.t + 2, cfg.T)
+    r = torch.as_tensor(rows).cuda()
+    Vs = cfg.V // cfg.t
+    tail = (Vs // 256) * 256                       # first column of the ragged last tile
+    assert Vs - tail == 48
+    for i in range(cfg.t):
+        Z = f32(out["logits"][i][r])
+        assert_fp32_close(Z, ref["Z"][i], f"logits[{i}] rows")
+        assert_fp32_close(Z[:, tail:], ref["Z"][i][:, tail:], f"logits[{i}] rows, ragged last tile")
+        assert_fp32_close(stats[3 * i][rows], ref["stats"][i][0], f"max[{i}] rows")
+        assert_fp32_close(stats[3 * i + 1][rows], ref["stats"][i][1], f"sumexp[{i}] rows")
+        assert_fp32_close(stats[3 * i + 2][rows], ref["stats"][i][2], f"target logit[{i}] rows")
+        assert_gemm_close(f64(out["dlogits"][i][r]), ref["dZ"][i], f"dlogits[{i}] rows")
+    assert_fp32_close(stats[3 * cfg.t][rows], ref["lse"], "lse (sampled rows)")
     assert_fp32_close(stats[3 * cfg.t + 1][rows], ref["loss_tok"], "loss per token (sampled rows)")
     loss_tok = stats[3 * cfg.t + 1].astype(np.float64)
     assert abs(out["loss"].item() - loss_tok.mean()) <= 1e-5 * abs(loss_tok.mean())
-    r = torch.as_tensor(rows).cuda()
-    for i in (0, cfg.t - 1):
-        assert_gemm_close(f64(out["dlogits"][i][r]), ref["dZ"][i], f"dlogits[{i}] rows")
     assert_gemm_close(f64(out["dH"][r]), ref["dH"], "dH rows")
+    del out
+    torch.cuda.empty_cache()

@@ -79,10 +79,13 @@ def test_empty_is_noop():
 
 @pytest.mark.parametrize("t", [2, 4, 8, 16])
 def test_full_size_sweep_sampled(t):
-    """b=1, s=4096, h=8192 partial sums (64 MiB each), as timed by the bench."""
+    """b=1, s=4096, h=8192 partial sums (64 MiB each), as timed by the bench: the literal
+    reduce-scatter then all-gather, and the fused all-reduce the MLP and attention blocks call.
+    Sampled rows against the oracle's mirror bit for bit; whole buffers against each other."""
     cfg = si.REDUCE_SWEEP
     bufs = si.partial_sum_buffers(t, cfg.T, cfg.h, seed=cfg.seed)
     rows = torch.arange(0, cfg.T, cfg.T // 32)[:32]           # 32 rows, spread over every slab
+    rows = torch.unique(torch.cat([rows, torch.tensor([cfg.T - 1])]))
     host_rows = [f32(x[rows]) for x in bufs]
     ref = collectives.all_reduce_mirror(host_rows)[0]
     d = dev(bufs)
@@ -98,3 +101,14 @@ def test_full_size_sweep_sampled(t):
         assert torch.equal(d[0], d[j])
     for k, r in enumerate(rows.tolist()):
         np.testing.assert_array_equal(_bits(f32(d[t - 1][r])), _bits(ref[k]))
+    fused = dev(bufs)
+    del bufs
+    ttl.shard_all_reduce(fused)
+    assert ttl.device_status() == 0
+    for j in range(t):
+        assert torch.equal(fused[j], d[0]), f"fused all-reduce buffer {j} differs from RS + AG"
+    r = rows.cuda()
+    for j in (0, t - 1):
+        np.testing.assert_array_equal(_bits(f32(fused[j][r])), _bits(ref), err_msg=f"fused buffer {j}")
+    del d, fused
+    torch.cuda.empty_cache()
