@@ -216,9 +216,12 @@ int ttl_sp_mlp_bwd(int t, int act, int64_t T, int64_t h, int64_t f, const ttl_bf
  *   a fixed TTL_STATIC_WS_BYTES array inside the library, present on every GPU that loads the
  *   library until the process exits.  A shape whose ttl_tp_mlp_bwd_workspace_size() exceeds
  *   it is rejected with TTL_ERR_UNSUPPORTED before anything runs.
- *   No device memory is allocated or freed.  The first call on each device looks up the
- *   scratch's device address with that device current; make that first call before any
- *   stream capture.
+ *   No device memory is allocated or freed.  The scratch used is the current device's, so
+ *   the current device must be the one that holds every pointer argument and the stream.
+ *   The first call on each device looks up the scratch's device address with that device
+ *   current and keeps it for the life of the process; make that first call before any stream
+ *   capture, and do not call this entry point again on a device after cudaDeviceReset (the
+ *   kept address would be stale).
  *   All calls share the one scratch array, and it keeps whatever the last call left in it
  *   (nothing in it needs to start at zero: every element is written before it is read).
  *   Calls that overlap on the GPU (e.g. on two streams at once) race on it and give wrong

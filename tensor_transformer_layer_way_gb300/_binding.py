@@ -351,22 +351,26 @@ def sp_mlp_bwd(X_slabs, dZ_slabs, A, B, fwd, *, act="gelu_tanh", A_up=None, out=
     return out
 
 
+# The size of the library's built-in scratch, TTL_STATIC_WS_BYTES in include/ttl.h (a CPU test
+# checks that the two agree).
 STATIC_WS_BYTES = 16 << 20
 
 
 def tp_mlp_bwd_static_ws(X, dY, A, B, fwd, *, act="gelu_tanh", A_up=None, out, stream=None):
     """tp_mlp_bwd using the library's built-in 16 MiB scratch instead of a caller workspace,
     for callers that cannot allocate device memory.  ``out`` (dA, dA_up, dB, db1, db2, dX) must be
-    provided.  Calls that overlap on the GPU share the scratch and race."""
+    provided.  Calls that overlap on the GPU share the scratch and race.  The call runs with
+    X's device current, because the library takes the scratch of the current device."""
     t = len(A)
     T, h = X.shape
     f = A[0].shape[1] * t
     _need(X, "X")
     _need(dY, "dY", shape=(T, h))
-    _check(lib().ttl_tp_mlp_bwd_static_ws(t, ACT[act], T, h, f, _p(X), _p(dY), _arr(A), _arr(A_up), _arr(B),
-                                          _arr(fwd["U"]), _arr(fwd["V"]), _arr(fwd["H"]), _arr(out["dA"]),
-                                          _arr(out["dA_up"]), _arr(out["dB"]), _arr(out["db1"]), _p(out["db2"]),
-                                          _arr(out["dX"]), _stream(stream)))
+    with torch.cuda.device(X.device):
+        _check(lib().ttl_tp_mlp_bwd_static_ws(t, ACT[act], T, h, f, _p(X), _p(dY), _arr(A), _arr(A_up), _arr(B),
+                                              _arr(fwd["U"]), _arr(fwd["V"]), _arr(fwd["H"]), _arr(out["dA"]),
+                                              _arr(out["dA_up"]), _arr(out["dB"]), _arr(out["db1"]),
+                                              _p(out["db2"]), _arr(out["dX"]), _stream(stream)))
     return out
 
 

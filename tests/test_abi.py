@@ -55,9 +55,9 @@ def test_reduce_validation(lib):
     assert lib.ttl_shard_reduce_scatter(3, 8, 8, _arr(A16, B16, 0x30000), None, None) == 2  # t does not divide rows
     assert lib.ttl_shard_all_gather(2, 8, 8, _arr(A16, B16 + 2), None) == 3       # misaligned
     assert lib.ttl_shard_all_reduce(2, 8, 8, _arr(A16, A16), None, None) == 1     # aliasing buffers
+    assert b"alias" in lib.ttl_last_error()
     assert lib.ttl_shard_all_reduce(2, -1, 8, _arr(A16, B16), None, None) == 1    # negative
     assert lib.ttl_shard_all_reduce(2, 0, 8, _arr(A16, B16), None, None) == 0     # empty: no-op, no GPU needed
-    assert b"alias" in lib.ttl_last_error() or True
 
 
 def test_mlp_validation(lib):
@@ -168,3 +168,12 @@ def test_every_declaration_is_documented():
                           and not lines[j].rstrip().endswith("*/")):
             j -= 1
         assert j >= 0 and lines[j].rstrip().endswith("*/"), f"{m.group(1)} has no comment block above it"
+
+
+def test_static_scratch_size_matches_the_header():
+    import re
+    import tensor_transformer_layer_way_gb300 as ttl
+    hdr = open(os.path.join(ROOT, "include", "ttl.h")).read()
+    m = re.search(r"#define\s+TTL_STATIC_WS_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", hdr)
+    assert m, "TTL_STATIC_WS_BYTES not found in include/ttl.h"
+    assert ttl.STATIC_WS_BYTES == int(m.group(1)) << int(m.group(2))

@@ -35,11 +35,27 @@ def _compare(ref, got, act):
             assert_gemm_close(f64(g), f64(r), f"{k}[{i}]")
 
 
+def _dirty_scratch(act):
+    """One call on a different, larger problem (the other activation, another seed, 2 MiB of
+    scratch or more), so that the scratch holds values unrelated to the checked case."""
+    other = "swiglu" if act == "gelu_tanh" else "gelu_tanh"
+    t, T, h, f = 2, 512, 128, 2048
+    X, dY, A, B, Au, fwd = _case(other, t, T, h, f, seed=77)
+    out = ttl.mlp_bwd_buffers(t, other, T, h, f, X.device)
+    ttl.tp_mlp_bwd_static_ws(X, dY, A, B, fwd, act=other, A_up=Au, out=out)
+    torch.cuda.synchronize()
+    assert ttl.device_status() == 0
+
+
 @pytest.mark.parametrize("act,t,T,h,f", [("gelu_tanh", 2, 128, 256, 1024), ("swiglu", 4, 200, 136, 384)])
 def test_static_scratch_matches_workspace_entry_point_twice(act, t, T, h, f):
+    """Two checked calls in a row, each after a call on another problem has left different
+    values in the scratch, so a read of a scratch element before this call writes it would
+    show up as a mismatch."""
     X, dY, A, B, Au, fwd = _case(act, t, T, h, f, seed=31)
     ref = ttl.tp_mlp_bwd(X, dY, A, B, fwd, act=act, A_up=Au)
-    for _ in range(2):                      # the second call runs on the first call's leftovers
+    for _ in range(2):
+        _dirty_scratch(act)
         out = ttl.mlp_bwd_buffers(t, act, T, h, f, X.device)
         ttl.tp_mlp_bwd_static_ws(X, dY, A, B, fwd, act=act, A_up=Au, out=out)
         torch.cuda.synchronize()
