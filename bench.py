@@ -98,15 +98,19 @@ class Dist:
 # ------------------------------------------------------------------ clocks and peaks
 
 class Clocks:
-    """nvidia-smi sampled every 100 ms while running; summarised into the JSON line."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampled every 100 ms from start() to stop(); each sample carries its own
+    timestamp, so the summary can be taken over any window of the run (the headline's warm-up
+    and timed region, or one component)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
         self.index = index
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.p = None
+        self.samples = []
 
     def start(self):
         try:
@@ -116,42 +120,83 @@ class Clocks:
         except OSError:
             self.p = None
 
-    def stop(self) -> dict:
+    def stop(self):
         if self.p is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
         time.sleep(0.25)
         self.p.terminate()
         self.p.wait(timeout=5)
         self.f.flush()
         self.f.seek(0)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
         for line in self.f.read().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+            reasons = {n for n, v in zip(self.NAMES, parts[6:10]) if v.lower().startswith("active")}
+            self.samples.append((ts, sm, smax, reasons))
         os.unlink(self.f.name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
+
+    def window(self, t0=None, t1=None) -> dict:
+        """Median SM clock, max clock and the throttle reasons seen between t0 and t1."""
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sel = [x for x in self.samples if (t0 is None or x[0] >= t0 - 0.05) and (t1 is None or x[0] <= t1 + 0.05)]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_max_mhz": max(x[2] for x in sel),
+                "samples": len(sel), "reasons": sorted(set().union(*(x[3] for x in sel)))}
 
 
 def peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
+        clk = d.get("clocks_under_load", {})
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "sustained_sm_mhz": clk.get("sm_mhz_median"), "sm_max_mhz": d.get("sm_max_mhz", 2070.0),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sustained_sm_mhz": None,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def tensor_peak(pk: dict, clk: dict):
+    """The dense bf16 peak that matches the clocks a measurement ran at.  The burst figure was
+    taken at the maximum SM clock; the sustained one after seconds back to back, under the
+    power cap, at a lower median clock.  A window whose median SM clock is within 5% of the
+    maximum ran under burst conditions; any other window is judged against the sustained
+    figure.  Returns (peak TFLOP/s, a one-line reason)."""
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz") or pk["sm_max_mhz"]
+    if sm is not None and smax and sm >= 0.95 * smax:
+        return pk["bf16_tflops"], (f"{pk['source']} bf16_tflops (burst): median SM clock {sm:.0f} MHz "
+                                   f"within 5% of the {smax:.0f} MHz maximum")
+    why = "no clock samples" if sm is None else f"median SM clock {sm:.0f} MHz below 95% of {smax:.0f} MHz"
+    return pk["bf16_tflops_sustained"], f"{pk['source']} bf16_tflops_sustained (power-capped): {why}"
+
+
+def roofline(bound: str, kernel: str, achieved: float, pk: dict, clk: dict, traffic=None, **extra) -> dict:
+    """The roofline object of one dominant kernel: ``achieved`` in TFLOP/s (tensor) or GB/s
+    (hbm), against the measured peak that fits the clocks it ran at.  For tensor-bound
+    kernels it also gives the rate scaled to the maximum SM clock (time x median MHz)."""
+    if bound == "tensor":
+        peak, why = tensor_peak(pk, clk)
+        unit = "TFLOP/s"
+    else:
+        peak, why, unit = pk["hbm_gbs"], f"{pk['source']} hbm_gbs (copy bandwidth)", "GB/s"
+    out = {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+           "frac": round(achieved / peak, 4), "peak_source": why, "traffic": traffic}
+    if bound == "tensor" and clk.get("sm_mhz"):
+        out["achieved_at_max_clock"] = round(achieved * (clk["sm_max_mhz"] or pk["sm_max_mhz"]) / clk["sm_mhz"], 1)
+        out["frac_of_burst_at_max_clock"] = round(out["achieved_at_max_clock"] / pk["bf16_tflops"], 4)
+    out["clocks"] = clk
+    out.update(extra)
+    return out
 
 
 def committed_traffic(kernel: str):
@@ -195,88 +240,114 @@ def run_ours(args, dist):
         ttl.tp_mlp_fwd(X, Wg, Wd, act=act, A_up=Wu, out=fo)
         ttl.tp_mlp_bwd(X, dY, Wg, Wd, fo, act=act, A_up=Wu, out=bo)
 
-    # Clocks are sampled from the start of the warm-up to the end of the timed region, so a
-    # short timed region still has samples under load.
+    # Clocks are sampled for the whole run; the headline's window runs from the start of the
+    # warm-up to the end of the timed region, so a short timed region still has samples.
     clocks = Clocks(dist.local)
     clocks.start()
+    w0 = time.time()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if ttl.device_status() != 0:
         raise RuntimeError("device status set during warm-up: " + ttl.last_error())
 
+    # Timed region: the K steps alone (no launch tracer), an event between consecutive steps.
     dist.barrier()
     torch.cuda.synchronize()
-    ttl.trace_enable(True, 1 << 16)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record()
+    for i in range(args.steps):
         step()
-    e1.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    clk = clocks.stop()
-    recs = ttl.trace_read(1 << 16)
-    ttl.trace_enable(False)
+    w1 = time.time()
+    ms = ev[0].elapsed_time(ev[-1])
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     if ttl.device_status() != 0:
         raise RuntimeError("device status set during the timed region: " + ttl.last_error())
     ms_max = dist.max(ms)
     value = dist.world * MLP_FLOPS * args.steps / (ms_max * 1e-3) / 1e12
+    med = statistics.median(per_step)
+
+    # A separate traced pass of the same step gives every launch's duration and work.
+    n_tr = min(args.steps, 20)
+    ttl.trace_enable(True, 1 << 16)
+    for _ in range(n_tr):
+        step()
+    torch.cuda.synchronize()
+    recs = ttl.trace_read(1 << 16)
+    ttl.trace_enable(False)
+    launches_per_step = len(recs) / n_tr
 
     gemm = [r for r in recs if r[0] == "gemm"]
     red = [r for r in recs if r[0] == "reduce"]
     g_ms = sum(r[1] for r in gemm)
     g_fl = sum(r[2] for r in gemm)
-    achieved = g_fl / (g_ms * 1e-3) / 1e12
-    peak = pk["bf16_tflops_sustained"]
-    roofline = {"bound": "tensor", "kernel": "gemm_tcgen05_kernel", "achieved": round(achieved, 1),
-                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)",
-                "traffic": committed_traffic("gemm_tcgen05_kernel"),
-                "launches_per_step": len(gemm) / args.steps,
-                "flops_per_launch": g_fl / max(len(gemm), 1),
-                "avg_launch_ms": g_ms / max(len(gemm), 1),
-                "share_of_step": round(g_ms / ms, 4)}
-    r_ms = sum(r[1] for r in red)
-    r_by = sum(r[3] for r in red)
-    allreduce = {"kernel": "shard_reduce_kernel<8,AR>", "achieved_gbs": round(r_by / (r_ms * 1e-3) / 1e9, 1),
-                 "peak_gbs": pk["hbm_gbs"], "frac": round(r_by / (r_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-                 "share_of_step": round(r_ms / ms, 4)}
-
-    # One step's launches with their FLOPs (or bytes) and times, from the last timed step.
-    per_step = len(recs) // args.steps
-    last = recs[-per_step:] if per_step else []
-    roofline["launches_last_step"] = [
-        {"kind": r[0], "ms": round(r[1], 4), "tflops": round(r[2] / (r[1] * 1e-3) / 1e12, 1) if r[2] else None,
-         "gbs": round(r[3] / (r[1] * 1e-3) / 1e9, 1) if not r[2] else None} for r in last]
-
+    comps = {}
+    marks = {"headline": (w0, w1)}
     e2e = bench_e2e(ttl, torch, dev, dist, args, X, dY, Wg, Wu, Wd, fo, bo)
     del fo, bo
     torch.cuda.empty_cache()
-
-    comps = {}
     if not args.no_components:
-        comps["sp_mlp"] = bench_sp_mlp(ttl, torch, dev, pk, args)
-        comps["shard_reduce"] = bench_shard_reduce(ttl, torch, dev, pk, args)
-        comps["gtp_chain"] = bench_gtp(ttl, torch, dev, pk, args)
-        comps["vocab_ce"] = bench_ce(ttl, torch, dev, pk, args)
-        comps["vocab_embedding"] = bench_embedding(ttl, torch, dev, pk, args)
-        comps["tp_attention"] = bench_attention(ttl, torch, dev, pk, args)
+        for name, fn in (("sp_mlp", bench_sp_mlp), ("shard_reduce", bench_shard_reduce), ("gtp_chain", bench_gtp),
+                         ("vocab_ce", bench_ce), ("vocab_embedding", bench_embedding),
+                         ("tp_attention", bench_attention)):
+            c0 = time.time()
+            comps[name] = fn(ttl, torch, dev, pk, args)
+            marks[name] = (c0, time.time())
+    clocks.stop()
+    clk = clocks.window(*marks["headline"])
+    for name in comps:
+        finish_rooflines(comps[name], pk, clocks.window(*marks[name]))
+
+    roof = roofline("tensor", "gemm_tcgen05_kernel", g_fl / (g_ms * 1e-3) / 1e12, pk, clk,
+                    traffic=committed_traffic("gemm_tcgen05_kernel"),
+                    launches_per_step=len(gemm) / n_tr, flops_per_launch=g_fl / max(len(gemm), 1),
+                    avg_launch_ms=g_ms / max(len(gemm), 1), share_of_step=round(g_ms / n_tr / med, 4),
+                    timing=f"per-launch CUDA events in a separate traced pass of {n_tr} steps")
+    r_ms = sum(r[1] for r in red)
+    r_by = sum(r[3] for r in red)
+    allreduce = roofline("hbm", "shard_reduce_kernel<8,AR>", r_by / (r_ms * 1e-3) / 1e9, pk, clk,
+                         traffic=committed_traffic("shard_reduce_kernel<8,AR>"),
+                         share_of_step=round(r_ms / n_tr / med, 4))
+    # One step's launches with their FLOPs (or bytes) and times, from the traced pass.
+    per = int(launches_per_step)
+    roof["launches_last_step"] = [
+        {"kind": r[0], "ms": round(r[1], 4), "tflops": round(r[2] / (r[1] * 1e-3) / 1e12, 1) if r[2] else None,
+         "gbs": round(r[3] / (r[1] * 1e-3) / 1e9, 1) if not r[2] else None} for r in recs[-per:]]
+    peak = roof["peak"]
 
     out = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": dist.world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+           "median_ms_per_step": round(med, 4), "value_at_median_step": round(MLP_FLOPS / (med * 1e-3) / 1e12, 1),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
            "data": "synthetic (seeded randn drawn on the device, Qwen3-8B MLP shapes)",
            "config": {"workload": WORKLOAD, "t": t, "tokens": T, "h": h, "ffn": f, "act": act,
                       "parallelism": f"{dist.world} independent replica(s), t={t} logical shards each",
-                      "l2": "working set larger than L2 (288 MiB of weights + 1.5 GiB of activations); no flush"},
-           "pct_of_bf16_peak": round(value / dist.world / peak, 4),
-           "roofline": roofline, "allreduce_in_step": allreduce,
-           "e2e": e2e, "gpu_launches": len(recs), "clocks": clk}
+                      "l2": "working set larger than L2 (288 MiB of weights + 1.5 GiB of activations); no flush",
+                      "timing": "CUDA events between consecutive steps, no launch tracer in the timed region"},
+           "pct_of_bf16_peak": round(value / dist.world / peak, 4), "peak_used": roof["peak_source"],
+           "roofline": roof, "allreduce_in_step": allreduce,
+           "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)), "clocks": clk}
     out.update(comps)
     return out
+
+
+def finish_rooflines(comp: dict, pk: dict, clk: dict):
+    """Components return their rooflines as ("pending", bound, kernel, achieved, traffic, extra)
+    tuples; the peak is filled in once the component's clock window is known."""
+    for k, v in list(comp.items()):
+        if isinstance(v, tuple) and v and v[0] == "pending":
+            _, bound, kernel, achieved, traffic, extra = v
+            comp[k] = roofline(bound, kernel, achieved, pk, clk, traffic=traffic, **extra)
+        elif isinstance(v, dict):
+            finish_rooflines(v, pk, clk)
+
+
+def pending(bound, kernel, achieved, traffic=None, **extra):
+    return ("pending", bound, kernel, achieved, traffic, extra)
 
 
 def bench_e2e(ttl, torch, dev, dist, args, X, dY, Wg, Wu, Wd, fo, bo):
@@ -382,7 +453,7 @@ def bench_shard_reduce(ttl, torch, dev, pk, args):
             torch.cuda.synchronize()
             recs = [r for r in ttl.trace_read(1024) if r[0] == kind]
             ttl.trace_enable(False)
-            ms = sum(r[1] for r in recs) / len(recs)
+            ms = statistics.median(r[1] for r in recs)
             by = recs[0][3]
             gbs = by / (ms * 1e-3) / 1e9
             row[mode] = {"gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "us": round(ms * 1e3, 1)}
@@ -390,6 +461,11 @@ def bench_shard_reduce(ttl, torch, dev, pk, args):
         del bufs
     del flush
     torch.cuda.empty_cache()
+    ar8 = res["t8"]["ar"]
+    res["roofline"] = pending("hbm", "shard_reduce_kernel<8,AR>", ar8["gbs"],
+                              traffic=committed_traffic("shard_reduce_kernel<8,AR>"),
+                              bytes_per_launch=2 * 8 * T * h * 2, median_us=ar8["us"],
+                              timing=f"median of {reps} launches, L2 flushed before each")
     return res
 
 
@@ -437,7 +513,10 @@ def bench_gtp(ttl, torch, dev, pk, args):
         res[key] = {"ms_per_fwd_bwd": round(wall, 3),
                     "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
                     "gemm_ms": round(gemm_ms, 3),
-                    "exposed_ms": round(wall - gemm_ms - sum(r[1] for r in fi) / reps, 3),
+                    # everything the chain's wall time spends outside the GEMMs: exposed gathers,
+                    # finalize work that is not hidden, launch gaps
+                    "exposed_ms": round(wall - gemm_ms, 3),
+                    "finalize_ms": round(sum(r[1] for r in fi) / reps, 3),
                     "finalize_gbs": round(sum(r[3] for r in fi) / (sum(r[1] for r in fi) * 1e-3) / 1e9, 1) if fi else None}
         if ga:
             res[key]["gather_gbs"] = round(sum(r[3] for r in ga) / (sum(r[1] for r in ga) * 1e-3) / 1e9, 1)
@@ -478,8 +557,8 @@ def bench_gtp(ttl, torch, dev, pk, args):
                               "torch_copy_same_bytes_gbs": round(gather_bytes / (cms * 1e-3) / 1e9, 1),
                               "bytes": gather_bytes, "l2": "flushed before each repetition of the 8 launches"}
     del flush, dst, src
-    res["peak_tflops"] = pk["bf16_tflops_sustained"]
-    res["peak_gbs"] = pk["hbm_gbs"]
+    res["roofline"] = pending("tensor", "gemm_tcgen05_kernel", res["slot_prefetch"]["gemm_tflops"],
+                              path="slot_prefetch chain (gathered slot, side-stream prefetch)")
     del X, shards, dY, Y, dX, slots, staging, main_grad, runner
     torch.cuda.empty_cache()
     return res
@@ -516,14 +595,17 @@ def bench_ce(ttl, torch, dev, pk, args):
             ms = sum(r[1] for r in rr)
             if flops:
                 v = sum(r[2] for r in rr) / (ms * 1e-3) / 1e12
-                return {"tflops": round(v, 1), "frac": round(v / pk["bf16_tflops_sustained"], 4),
-                        "ms": round(ms / reps, 3)}
+                return {"tflops": round(v, 1), "ms": round(ms / reps, 3)}
             v = sum(r[3] for r in rr) / (ms * 1e-3) / 1e9
             return {"gbs": round(v, 1), "frac": round(v / pk["hbm_gbs"], 4), "ms": round(ms / reps, 3)}
 
         res[mode] = {"ms_per_fwd_bwd": round(wall, 3), "loss": float(out["loss"].item()),
                      "gemm": agg("gemm", True), "stats": agg("ce_stats"), "dlogits": agg("ce_dlogits"),
                      "combine_mean": agg("ce_small")}
+    res["roofline"] = pending("tensor", "gemm_tcgen05_kernel", res["fused_stats"]["gemm"]["tflops"],
+                              path="LM-head GEMM with fused statistics + dH GEMM")
+    dl = res["fused_stats"]["dlogits"]
+    res["roofline_hbm"] = pending("hbm", "ce_dlogits_kernel", dl["gbs"])
     del H, W, target, out
     torch.cuda.empty_cache()
     return res
@@ -569,8 +651,8 @@ def bench_sp_mlp(ttl, torch, dev, pk, args):
     res = {"workload": "qwen3_8b_swiglu_mlp_t8_T8192_sequence_parallel_fwd_bwd", "ms_per_step": round(ms, 4),
            "tflops": round(MLP_FLOPS / (ms * 1e-3) / 1e12, 1),
            "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
-           "launches_per_step": len(recs) / n, "collective_kernels_per_step": 0,
-           "frac_of_sustained_bf16": round(MLP_FLOPS / (ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4)}
+           "launches_per_step": len(recs) / n, "collective_kernels_per_step": 0}
+    res["roofline"] = pending("tensor", "gemm_tcgen05_kernel", res["gemm_tflops"])
     del Xs, dZs, Wg, Wu, Wd, fo, bo
     torch.cuda.empty_cache()
     return res
@@ -610,6 +692,8 @@ def bench_embedding(ttl, torch, dev, pk, args):
         kms = sum(r[1] for r in recs) / reps
         res[name] = {"ms": round(ms / reps, 4), "kernel_gbs": round(by / (kms * 1e-3) / 1e9, 1),
                      "frac": round(by / (kms * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "launches": len(recs) // reps}
+    res["roofline"] = pending("hbm", "embed_gather_kernel", res["fwd_fused"]["kernel_gbs"],
+                              bytes_per_launch=T * h * 2 * (1 + t))
     del E, ids, dY, out, dE, flush
     torch.cuda.empty_cache()
     return res
@@ -655,13 +739,15 @@ def bench_attention(ttl, torch, dev, pk, args):
     ms = e0.elapsed_time(e1) / n
     flops = sum(r[2] for r in recs) / n        # algorithmic: causal contractions count their triangle
     gm = [r for r in recs if r[0] == "gemm"]
+    co = [r for r in recs if r[0] == "attn_core"]
     sm = [r for r in recs if r[0] == "softmax"]
     sm_gbs = sum(r[3] for r in sm) / (sum(r[1] for r in sm) * 1e-3) / 1e9
     name = f"attention_t{t}_T{T}_h{h}_q{n_q}_kv{n_kv}_d{d}_fwd_bwd"
     res = {"workload": ("qwen3_8b_" if not args.attn_small else "") + name, "ms_per_step": round(ms, 4),
            "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "flops_per_step": flops,
            "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
-           "frac_of_sustained_bf16": round(flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4),
+           "core_tflops": round(sum(r[2] for r in co) / (sum(r[1] for r in co) * 1e-3) / 1e12, 1),
+           "core_share_of_step": round(sum(r[1] for r in co) / n / ms, 4),
            "softmax_gbs": round(sm_gbs, 1), "softmax_frac_of_hbm": round(sm_gbs / pk["hbm_gbs"], 4),
            "softmax_share_of_step": round(sum(r[1] for r in sm) / n / ms, 4),
            "launches_per_step": len(recs) / n,
@@ -669,6 +755,10 @@ def bench_attention(ttl, torch, dev, pk, args):
                          "tflops": round(r[2] / (r[1] * 1e-3) / 1e12, 1) if r[2] else None,
                          "gbs": round(r[3] / (r[1] * 1e-3) / 1e9, 1) if not r[2] else None}
                         for r in recs[-(len(recs) // n):]]}
+    res["roofline"] = pending("tensor", "attn_fwd_core_kernel + attn_bwd_core_kernel + attn_bwd_kv_kernel",
+                              res["core_tflops"], share_of_step=res["core_share_of_step"])
+    res["step_roofline"] = pending("tensor", "whole block step (cores, projections, row dot, all-reduces)",
+                                   res["tflops"])
     del X, dY, Wq, Wk, Wv, Wo, fo, bo
     torch.cuda.empty_cache()
     return res
@@ -727,6 +817,181 @@ def cpu_baseline(tokens: int, seconds: float) -> dict:
                       f"(full weights), {len(times)} repetitions, {total:.1f} s"}
 
 
+def _repeat(fn, seconds: float, min_reps: int = 1) -> list:
+    times = []
+    while len(times) < min_reps or sum(times) < seconds:
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_reduce(seconds: float) -> dict:
+    """Config 2 in full: the oracle's all_reduce_mirror over t in {2,4,8,16} buffers of
+    [4096, 8192], once on one thread and once on every core (the same function on row bands,
+    one band per thread; numpy releases the GIL inside its array operations).  GB/s counts
+    the same algorithmic bytes as the kernel (2 t S, S = 64 MiB of bf16)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import synth_inputs as si
+    from oracle import collectives
+    n = cpu_cores()
+    T, h = 4096, 8192
+    by_t = {}
+    for t in (2, 4, 8, 16):
+        bufs = [b.float().numpy() for b in si.partial_sum_buffers(t, T, h, seed=2)]
+        nbytes = 2 * t * T * h * 2
+        one = _repeat(lambda: collectives.all_reduce_mirror(bufs), 0.0)
+        step = max(t, (T // n) // t * t)
+        bands = [slice(r, min(T, r + step)) for r in range(0, T, step)]
+
+        def banded():
+            with ThreadPoolExecutor(len(bands)) as ex:
+                list(ex.map(lambda sl: collectives.all_reduce_mirror([b[sl] for b in bufs]), bands))
+        many = _repeat(banded, min(seconds / 8, 2.0), 2)
+        by_t[f"t{t}"] = {"gbs_1_core": round(nbytes / min(one) / 1e9, 2),
+                         "gbs_all_cores": round(nbytes / min(many) / 1e9, 2),
+                         "s_1_core": round(min(one), 3), "s_all_cores": round(min(many), 3)}
+        del bufs
+    return {"value": by_t["t8"]["gbs_all_cores"], "unit": "GB/s", "cores": n, "kind": "oracle",
+            "value_1_core": by_t["t8"]["gbs_1_core"], "by_t": by_t,
+            "sample": "the full workload: all_reduce_mirror (fp32 sum in buffer order, one bf16 rounding) of "
+                      "t = 2, 4, 8, 16 buffers [4096, 8192], on 1 thread and on every core; value is t = 8"}
+
+
+def cpu_gtp(tokens: int, seconds: float) -> dict:
+    """Config 4 on a token sample: all 8 layers with the full [8192, 2048] slices as 8 row
+    shards, the first `tokens` of 4096 token rows: gather + forward GEMM, gather + dgrad GEMM,
+    the literal per-token-group wgrad reduce-scatter, and the deferred finalize."""
+    import numpy as np
+    import synth_inputs as si
+    from oracle import gtp
+    L, K, N, g, M = 8, 8192, 2048, 8, 4096
+    inp = si.gtp_inputs(L, K, N, tokens, seed=4)
+    X = inp["X"].float().numpy().astype(np.float64)
+    W = [w.float().numpy().astype(np.float64) for w in inp["W"]]
+    dY = [d.float().numpy().astype(np.float64) for d in inp["dY"]]
+    shards = [gtp.shard_rows(w, g) for w in W]
+    main_grad = [[np.zeros((K // g, N)) for _ in range(g)] for _ in range(L)]
+
+    def fwd_bwd():
+        for l in range(L):
+            gtp.forward_gemm(X, gtp.gather(shards[l]))
+        staging = [None] * L
+        for l in range(L - 1, -1, -1):
+            gtp.dgrad_gemm(dY[l], gtp.gather(shards[l]))
+            staging[l] = gtp.wgrad_reduce_scatter(X, dY[l], g)
+        gtp.deferred_finalize(main_grad, staging)
+    times = _repeat(fwd_bwd, seconds)
+    flops = 3 * L * 2.0 * tokens * K * N
+    per = sum(times) / len(times)
+    return {"value": round(flops / per / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "extrapolated_full_s": round(per * M / tokens, 2),
+            "sample": f"fp64 numpy oracle, 8-layer GTP chain fwd+bwd on {tokens} of {M} token rows with the full "
+                      f"slices; {len(times)} repetitions; the full-size time is extrapolated (x{M // tokens}, "
+                      "GEMM work scales with tokens)"}
+
+
+def cpu_ce(tokens: int, seconds: float) -> dict:
+    """Config 5 on a token sample: the full [151936, 4096] head in 8 vocab shards, `tokens` of
+    8192 token rows: logits, statistics, combine, dlogits and dH."""
+    import numpy as np
+    import synth_inputs as si
+    from oracle import vocab_ce
+    T, h, V, t = 8192, 4096, 151936, 8
+    inp = si.ce_inputs(tokens, h, V, seed=5)
+    H = inp["H"].float().numpy().astype(np.float64)
+    W = inp["W"].float().numpy().astype(np.float64)
+    target = inp["target"].numpy()
+    del inp
+    times = _repeat(lambda: vocab_ce.vocab_parallel_ce(H, W, target, t), seconds)
+    per = sum(times) / len(times)
+    flops = 2 * 2.0 * tokens * V * h
+    return {"value": round(flops / per / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "extrapolated_full_s": round(per * T / tokens, 2),
+            "sample": f"fp64 numpy oracle, vocab-parallel CE (t=8) on {tokens} of {T} tokens with the full head; "
+                      f"{len(times)} repetitions; the full-size time is extrapolated (x{T // tokens})"}
+
+
+def cpu_sp(tokens: int, seconds: float) -> dict:
+    """The sequence-parallel MLP on a token sample: t = 8 slabs of tokens/8 rows, full weights."""
+    from oracle import tp_mlp
+    X, W, dY = oracle_sample(tokens)
+    t = MLP["t"]
+    w = tokens // t
+    Xs = [X[r * w:(r + 1) * w] for r in range(t)]
+    dZs = [dY[r * w:(r + 1) * w] for r in range(t)]
+
+    def run():
+        fwd = tp_mlp.sp_mlp_forward(Xs, W, t, MLP["act"])
+        tp_mlp.sp_mlp_backward(Xs, W, t, MLP["act"], dZs, fwd)
+    times = _repeat(run, seconds)
+    per = sum(times) / len(times)
+    flops = MLP_FLOPS * tokens / MLP["T"]
+    return {"value": round(flops / per / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "extrapolated_full_s": round(per * MLP["T"] / tokens, 2),
+            "sample": f"fp64 numpy oracle, sequence-parallel SwiGLU MLP fwd+bwd on {tokens} of {MLP['T']} tokens "
+                      f"(8 slabs, full weights); {len(times)} repetitions; full-size time extrapolated"}
+
+
+def cpu_embedding(seconds: float) -> dict:
+    """The embedding lookup on a shard sample: all 8192 ids against 2 of the 8 vocab shards
+    (each [18992, 4096]); the full lookup is extrapolated to 8 shards."""
+    import numpy as np
+    import synth_inputs as si
+    from oracle import embedding
+    T, h, V, t, ns = 8192, 4096, 151936, 8, 2
+    Vs = V // t
+    g = si.generator(6)
+    E = [si.randn_bf16(g, (Vs, h), 0.02).float().numpy().astype(np.float64) for _ in range(ns)]
+    import torch
+    ids = torch.randint(0, V, (T,), generator=g).numpy()
+
+    def run():
+        parts = [embedding.shard_lookup(ids, E[i], i * Vs) for i in range(ns)]
+        out = parts[0]
+        for p in parts[1:]:
+            out = out + p
+    times = _repeat(run, seconds)
+    full = sum(times) / len(times) * t / ns
+    nbytes = T * h * 2 * (1 + t)
+    return {"value": round(nbytes / full / 1e9, 3), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+            "extrapolated_full_s": round(full, 3),
+            "sample": f"fp64 numpy oracle, masked lookup of all {T} ids in {ns} of {t} vocab shards and their sum; "
+                      f"{len(times)} repetitions; time extrapolated to {t} shards; GB/s on the kernel's algorithmic bytes"}
+
+
+def cpu_attention(seconds: float) -> dict:
+    """The attention block's forward on sampled output rows at the Qwen3-8B shape: rows 127,
+    255, 383 and 511 of 8192 (each needs the keys and values of the tokens up to it)."""
+    import numpy as np
+    import synth_inputs as si
+    from oracle import attention
+    T, h, n_q, n_kv, d = 512, 4096, 32, 8, 128
+    inp = si.attn_inputs(T, h, n_q, n_kv, d, seed=6)
+    X = inp["X"].float().numpy().astype(np.float64)
+    W = {k: inp[k].float().numpy().astype(np.float64) for k in ("Wq", "Wk", "Wv", "Wo")}
+    rows = [127, 255, 383, 511]
+    times = _repeat(lambda: attention.forward_rows(X, W, n_q, n_kv, d, rows, t=8), seconds)
+    per = sum(times) / len(times)
+    m = max(rows) + 1
+    flops = 2.0 * m * h * 2 * n_kv * d + sum(2.0 * h * n_q * d * 2 + 4.0 * d * (r + 1) * n_q for r in rows)
+    return {"value": round(flops / per / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, forward output rows {rows} of the T=8192 block (K/V projections of the "
+                      f"first {m} tokens, then per-row attention and W_O); {len(times)} repetitions; forward only, "
+                      "no extrapolation"}
+
+
+def component_cpu_baselines(out: dict, args):
+    """A cpu_baseline object for every component of the JSON line (rank 0, N = 1)."""
+    sec = max(1.0, args.cpu_seconds / 4)
+    legs = {"shard_reduce": lambda: cpu_reduce(sec), "gtp_chain": lambda: cpu_gtp(128, sec),
+            "vocab_ce": lambda: cpu_ce(32, sec), "sp_mlp": lambda: cpu_sp(args.cpu_tokens, sec),
+            "vocab_embedding": lambda: cpu_embedding(sec), "tp_attention": lambda: cpu_attention(sec)}
+    for name, fn in legs.items():
+        if isinstance(out.get(name), dict):
+            out[name]["cpu_baseline"] = fn()
+
+
 def run_reference(args, dist):
     if dist.rank != 0:
         return None
@@ -763,14 +1028,20 @@ def main():
             fn = {"sp_mlp": bench_sp_mlp, "shard_reduce": bench_shard_reduce, "gtp_chain": bench_gtp,
                   "vocab_ce": bench_ce, "vocab_embedding": bench_embedding,
                   "tp_attention": bench_attention}[args.only]
-            out = {"component": args.only,
-                   args.only: fn(ttl, torch, torch.device("cuda", dist.local), peaks(), args)}
+            clocks = Clocks(dist.local)
+            clocks.start()
+            pk = peaks()
+            comp = fn(ttl, torch, torch.device("cuda", dist.local), pk, args)
+            clocks.stop()
+            finish_rooflines(comp, pk, clocks.window())
+            out = {"component": args.only, args.only: comp}
         elif args.impl == "reference":
             out = run_reference(args, dist)
         else:
             out = run_ours(args, dist)
             if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
                 out["cpu_baseline"] = cpu_baseline(args.cpu_tokens, args.cpu_seconds)
+                component_cpu_baselines(out, args)
         if dist.rank == 0 and out is not None:
             print(json.dumps(out), flush=True)
     finally:

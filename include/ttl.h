@@ -89,6 +89,7 @@ int ttl_selftest_wait_timeout(int64_t timeout_us, void* stream);
 #define TTL_K_OTHER 8       /* column sums, zero fills                        */
 #define TTL_K_EMBED 9       /* vocab-parallel embedding lookup / gradient     */
 #define TTL_K_SOFTMAX 10    /* attention row softmax / softmax backward       */
+#define TTL_K_ATTN_CORE 11  /* fused attention cores (scores, softmax, P V)  */
 
 /* Starts (on != 0) or stops tracing on this process.  While on, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the launch stream, and

@@ -165,7 +165,7 @@ def selftest_wait_timeout(timeout_us: int, stream=None) -> int:
 
 
 KERNEL_KINDS = ["gemm", "reduce", "gather", "gtp_gather", "finalize", "ce_stats", "ce_small", "ce_dlogits", "other",
-                "embed", "softmax"]
+                "embed", "softmax", "attn_core"]
 
 
 def trace_enable(on: bool = True, capacity: int = 65536):

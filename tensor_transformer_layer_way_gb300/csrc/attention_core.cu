@@ -1321,7 +1321,7 @@ int attn_fwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
   const double tri = static_cast<double>(T) * (T + 1) / 2.0;
   // Algorithmic work: S = Q K^T and P V over the causal triangle (the second score pass is a
   // recomputation and is not counted); bytes: Q, K, V read once, P and O written once.
-  TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
+  TraceScope tr(stream, TTL_K_ATTN_CORE, 2.0 * 2.0 * tri * d * t * nql,
                 2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
   if (d == 128) {
     if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_fwd_core_kernel<128>), kFwd128, CoreCfg<128>::SMEM,
@@ -1379,7 +1379,7 @@ int attn_bwd_core(int t, int64_t T, int nql, int grp, int d, const void* const* 
   const double tri = static_cast<double>(T) * (T + 1) / 2.0;
   // Algorithmic work: dP = dO V^T and dQ = dS K over the causal triangle; bytes: P read, dO, V,
   // K read and dQ written once.
-  TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
+  TraceScope tr(stream, TTL_K_ATTN_CORE, 2.0 * 2.0 * tri * d * t * nql,
                 2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 2.0 * kc) * t);
   if (d == 128) {
     if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_core_kernel<128>), kBwd128, BwdCfg<128>::SMEM,
@@ -1439,7 +1439,7 @@ int attn_bwd_kv(int t, int64_t T, int nql, int nkvl, int grp, int d, const void*
   const double tri = static_cast<double>(T) * (T + 1) / 2.0;
   // Algorithmic work: dV = P^T dO and dK = dS^T Q over the causal triangle (the dP it recomputes
   // is not counted); bytes: P read once, Q, dO, V read once, dK and dV written once.
-  TraceScope tr(stream, TTL_K_GEMM, 2.0 * 2.0 * tri * d * t * nql,
+  TraceScope tr(stream, TTL_K_ATTN_CORE, 2.0 * 2.0 * tri * d * t * nql,
                 2.0 * tri * t * nql + 2.0 * T * (2.0 * qc + 3.0 * kc) * t);
   if (d == 128) {
     if ((rc = set_core_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel<128>), kKv128, KvCfg<128>::SMEM,

@@ -77,3 +77,36 @@ def test_cpu_cores_honours_omp_num_threads(monkeypatch):
     assert bench.cpu_cores() == 1
     monkeypatch.delenv("OMP_NUM_THREADS")
     assert bench.cpu_cores() == len(os.sched_getaffinity(0))
+
+
+def test_peak_follows_the_clocks_of_the_window():
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1950.0, "bf16_tflops_sustained": 1718.0, "sm_max_mhz": 2070.0,
+          "source": "measured"}
+    assert bench.tensor_peak(pk, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[0] == 1950.0
+    assert bench.tensor_peak(pk, {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0})[0] == 1950.0
+    assert bench.tensor_peak(pk, {"sm_mhz": 1460.0, "sm_max_mhz": 2070.0})[0] == 1718.0
+    assert bench.tensor_peak(pk, {"sm_mhz": None, "sm_max_mhz": None})[0] == 1718.0
+    r = bench.roofline("tensor", "k", 1500.0, pk, {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0})
+    assert r["peak"] == 1718.0 and r["frac"] == round(1500.0 / 1718.0, 4)
+    assert r["achieved_at_max_clock"] == round(1500.0 * 2070.0 / 1800.0, 1)
+    comp = {"a": bench.pending("hbm", "x", 3400.0), "b": {"c": bench.pending("tensor", "y", 975.0)}}
+    bench.finish_rooflines(comp, pk, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})
+    assert comp["a"]["frac"] == 0.5 and comp["a"]["unit"] == "GB/s"
+    assert comp["b"]["c"]["frac"] == 0.5 and comp["b"]["c"]["unit"] == "TFLOP/s"
+
+
+def test_clock_windows_select_samples_by_time():
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.Clocks(0)
+    c.p = object()          # as if nvidia-smi had run
+    c.samples = [(10.0, 2070.0, 2070.0, set()), (10.1, 2070.0, 2070.0, set()),
+                 (20.0, 1500.0, 2070.0, {"sw_power_cap"}), (20.1, 1400.0, 2070.0, {"sw_power_cap"})]
+    w = c.window(9.9, 10.2)
+    assert w["sm_mhz"] == 2070.0 and w["samples"] == 2 and w["reasons"] == []
+    w = c.window(19.0, 21.0)
+    assert w["sm_mhz"] == 1450.0 and w["reasons"] == ["sw_power_cap"]
+    import os as _os
+    _os.unlink(c.f.name)
