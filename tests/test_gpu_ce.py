@@ -11,6 +11,20 @@ from parity import assert_fp32_close, assert_gemm_close, dev, f32, f64
 pytestmark = pytest.mark.gpu
 
 
+def _assert_sumexp_close(got, ref, Z, name):
+    """Per-token sum-exp s = sum_v exp(z_v - m) against the oracle.  It inherits the logits'
+    error: d(log s) = sum_v softmax_v dz_v (the shift by the max cancels), so |ds / s| <= max_v
+    |dz_v|, which the logits check bounds by 1e-5 * max|z|.  A 4-ulp allowance covers the
+    exponentials' own rounding.  At K = 4096 the tensor cores' fp32 accumulation moves the
+    logits by a few 1e-5, so the plain 1e-5 relative bound is not attainable for s, while the
+    loss (log s + m - z_y) still meets it."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = (1e-5 * np.abs(Z).max() + 4 * 2.0 ** -24) * ref
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), f"{name}: max relative error {(err / ref).max():.3e} > {(bound / ref).max():.3e}"
+
+
 def _run(H, W, target, t, flags=0, fused=True):
     Ws = dev([w.contiguous() for w in W.chunk(t, 0)])
     out = ttl.vocab_parallel_ce(dev(H), Ws, dev(target), flags=flags, fused_stats=fused)
@@ -106,7 +120,7 @@ def test_vocab_parallel_ce_full_size_sampled(fused):
         assert_fp32_close(Z, ref["Z"][i], f"logits[{i}] rows")
         assert_fp32_close(Z[:, tail:], ref["Z"][i][:, tail:], f"logits[{i}] rows, ragged last tile")
         assert_fp32_close(stats[3 * i][rows], ref["stats"][i][0], f"max[{i}] rows")
-        assert_fp32_close(stats[3 * i + 1][rows], ref["stats"][i][1], f"sumexp[{i}] rows")
+        _assert_sumexp_close(stats[3 * i + 1][rows], ref["stats"][i][1], ref["Z"][i], f"sumexp[{i}] rows")
         assert_fp32_close(stats[3 * i + 2][rows], ref["stats"][i][2], f"target logit[{i}] rows")
         assert_gemm_close(f64(out["dlogits"][i][r]), ref["dZ"][i], f"dlogits[{i}] rows")
     assert_fp32_close(stats[3 * cfg.t][rows], ref["lse"], "lse (sampled rows)")
