@@ -484,22 +484,23 @@ def bench_gtp(ttl, torch, dev, pk, args):
     from tensor_transformer_layer_way_gb300 import chain
     runner = chain.GtpChain(ttl, torch, shards, slots)
 
-    def fwd_bwd(folded=False):
+    def fwd_bwd(folded=False, fin_stream=True):
         runner.forward(X, Y, folded=folded)
-        runner.backward(X, dY, dX, staging, main_grad, folded=folded)
+        runner.backward(X, dY, dX, staging, main_grad, folded=folded, finalize_stream=fin_stream)
 
     runner.forward(X, Y, cold=True)           # cold start: every first gather synchronous
     for _ in range(2):
         fwd_bwd()
     torch.cuda.synchronize()
     res = {"workload": "gtp_chain_L8_h8192_tp4_g8_T4096", "gemm_flops_per_pass": 3 * L * 2.0 * M * K * N}
-    for folded in (False, True):
+    for key, folded, fin in (("slot_prefetch", False, True), ("folded", True, True),
+                             ("slot_prefetch_finalize_on_compute_stream", False, False)):
         ttl.trace_enable(True, 1 << 14)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         reps = 3
         e0.record()
         for _ in range(reps):
-            fwd_bwd(folded)
+            fwd_bwd(folded, fin)
         e1.record()
         torch.cuda.synchronize()
         wall = e0.elapsed_time(e1) / reps
@@ -509,7 +510,6 @@ def bench_gtp(ttl, torch, dev, pk, args):
         ga = [r for r in recs if r[0] == "gtp_gather"]
         fi = [r for r in recs if r[0] == "finalize"]
         gemm_ms = sum(r[1] for r in gm) / reps
-        key = "folded" if folded else "slot_prefetch"
         res[key] = {"ms_per_fwd_bwd": round(wall, 3),
                     "gemm_tflops": round(sum(r[2] for r in gm) / (sum(r[1] for r in gm) * 1e-3) / 1e12, 1),
                     "gemm_ms": round(gemm_ms, 3),

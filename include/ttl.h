@@ -255,6 +255,14 @@ int ttl_gtp_gather_gemm(int g, int64_t M, int64_t K, int64_t N, const ttl_bf16* 
                         const ttl_bf16* const* shards, const ttl_bf16* slot, void* slot_ready_event,
                         ttl_bf16* Y, int transpose_w, void* stream);
 
+/* The finalize step alone: main_grad[j] += staging[j] (fp32, g shards of [K/g,N]) on `stream`.
+ * [GTP] concept "Deferred finalize": the merge into main_grad runs one backward layer after
+ * the layer's weight gradient.  A caller that wants it off the compute stream (the chain
+ * helper does) passes staging_prev = NULL to ttl_gtp_wgrad_rs_finalize and issues this on
+ * another stream after an event recorded behind that layer's weight-gradient call. */
+int ttl_gtp_finalize(int g, int64_t K, int64_t N, const float* const* staging, float* const* main_grad,
+                     void* stream);
+
 /* Weight gradient of one layer, reduce-scattered into shards, with deferred finalize.
  *   staging_cur[j] [K/g,N] fp32 <- rows of X^T dY for shard j (the sum over the g token
  *                  groups' partials, folded into the GEMM's token contraction)
@@ -262,7 +270,11 @@ int ttl_gtp_gather_gemm(int g, int64_t M, int64_t K, int64_t N, const ttl_bf16* 
  *                  one backward step earlier, main_grad_prev[j] += staging_prev[j]
  *   sync = 1:      also finalize this layer now, main_grad_cur[j] += staging_cur[j]
  *                  (the last backward layer: nothing follows it)
- *   X [M,K] bf16, dY [M,N] bf16; g divides K. */
+ *   X [M,K] bf16, dY [M,N] bf16; g divides K.
+ * Both finalizes run inside the weight-gradient GEMM's epilogue, element by element beside
+ * the tile it writes (one fp32 addition per element, as a separate pass would do), so they
+ * add no launch to the critical path.  staging_prev may be staging_cur itself (one staging
+ * set reused by every layer): each element of it is read before it is overwritten. */
 int ttl_gtp_wgrad_rs_finalize(int g, int64_t M, int64_t K, int64_t N, const ttl_bf16* X, const ttl_bf16* dY,
                               float* const* staging_cur, const float* const* staging_prev,
                               float* const* main_grad_prev, int sync, float* const* main_grad_cur,
@@ -285,15 +297,18 @@ int ttl_gtp_wgrad_rs_finalize(int g, int64_t M, int64_t K, int64_t N, const ttl_
  *   ws         optional workspace of ttl_vocab_parallel_ce_workspace_size() bytes.  With it,
  *              the LM-head GEMM's epilogue computes each row's max and sum of exponentials
  *              tile by tile while it writes the logits, so the statistics never re-read the
- *              fp32 logits; with ws = NULL a separate pass scans them.  Same results.
+ *              fp32 logits, and one launch merges them, combines the shards and takes the
+ *              mean; with ws = NULL separate passes scan the logits, combine, and average.
+ *              Same results up to fp32 rounding order.
  * t in 1..TTL_MAX_SHARDS divides V; V/t a multiple of 8.  A target outside [0,V) sets
  * TTL_ERR_DEVICE in the status word and that token's loss to NaN. */
 int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, const ttl_bf16* H, const ttl_bf16* const* W,
                           const int64_t* target, float* const* logits, ttl_bf16* const* dlogits, float* stats,
                           float* loss, ttl_bf16* dH, void* ws, size_t ws_bytes, int flags, void* stream);
 
-/* Bytes of the optional ttl_vocab_parallel_ce workspace: per token, 8 bytes for each 256-wide
- * column tile of every vocab shard, plus 4; 0 for invalid arguments. */
+/* Bytes of the optional ttl_vocab_parallel_ce workspace: per token, 8 bytes for each 128-wide
+ * half of a 256-wide column tile of every vocab shard, plus 4, each part rounded up to 256
+ * bytes, plus 256 for a completion counter; 0 for invalid arguments. */
 size_t ttl_vocab_parallel_ce_workspace_size(int t, int64_t T, int64_t h, int64_t V);
 
 /* ------------------------------------------------------------------ vocab-parallel embedding */

@@ -55,6 +55,7 @@ _SIGS = {
     "ttl_gtp_gather": (_int, [_int, _i64, _i64, _vp, _vp, _vp, _vp]),
     "ttl_gtp_gather_gemm": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp]),
     "ttl_gtp_wgrad_rs_finalize": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp, _vp]),
+    "ttl_gtp_finalize": (_int, [_int, _i64, _i64, _vp, _vp, _vp]),
     "ttl_vocab_parallel_ce": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _int, _vp]),
     "ttl_vocab_parallel_ce_workspace_size": (ctypes.c_size_t, [_int, _i64, _i64, _i64]),
@@ -427,6 +428,16 @@ def gtp_wgrad_rs_finalize(X, dY, staging_cur, *, staging_prev=None, main_grad_pr
     _check(lib().ttl_gtp_wgrad_rs_finalize(g, M, K, N, _p(X), _p(dY), _arr(staging_cur), _arr(staging_prev),
                                            _arr(main_grad_prev), int(sync), _arr(main_grad_cur) if sync else None,
                                            _stream(stream)))
+
+
+def gtp_finalize(staging, main_grad, *, stream=None):
+    """main_grad[j] += staging[j] for the g fp32 shards [K/g, N] (on ``stream``, a torch stream)."""
+    g = len(staging)
+    Kg, N = staging[0].shape
+    _need_list(staging, "staging", g, torch.float32, (Kg, N))
+    _need_list(main_grad, "main_grad", g, torch.float32, (Kg, N))
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(lib().ttl_gtp_finalize(g, Kg * g, N, _arr(staging), _arr(main_grad), s.cuda_stream))
 
 
 # ------------------------------------------------------------------ vocab-parallel CE

@@ -23,8 +23,10 @@ class GtpChain:
         self.slots = slots
         self.L = len(shards)
         self.side = torch.cuda.Stream()
+        self.fin = torch.cuda.Stream()                         # deferred finalizes
         self.ready = [torch.cuda.Event() for _ in range(2)]
         self.free = [torch.cuda.Event() for _ in range(2)]
+        self.wgrad_done = [torch.cuda.Event() for _ in range(self.L)]
 
     def _gather_async(self, l, wait_free):
         k = l % 2
@@ -56,17 +58,29 @@ class GtpChain:
             ttl.gtp_gather_gemm(X, self.shards[l], Y[l], slot=self.slots[l % 2])
             self.free[l % 2].record(main)
 
-    def backward(self, X, dY, dX, staging, main_grad, *, folded=False):
+    def backward(self, X, dY, dX, staging, main_grad, *, folded=False, finalize_stream=True):
         """Reverse chain: dX = dY[l] W_l^T with the gather of layer l-1 beside it; the wgrad of
         layer l is reduce-scattered into staging[l] and finalized into main_grad[l] one backward
-        layer later (layer 0 at once).  ``dX`` may be one buffer or a list per layer."""
+        layer later (layer 0 at once).  ``dX`` may be one buffer or a list per layer.
+
+        With ``finalize_stream`` the deferred finalize of layer l+1 is issued at the start of
+        backward step l on a stream of its own (after the event recorded behind layer l+1's
+        weight gradient), so it runs beside step l's GEMMs instead of between them; the
+        compute stream joins it before returning.  Otherwise it runs on the compute stream,
+        inside the weight-gradient call of step l."""
         ttl = self.ttl
         main = self.torch.cuda.current_stream()
         L = self.L
+        if finalize_stream:
+            self.fin.wait_stream(main)
         if not folded:
             self.side.wait_stream(main)
             self._gather_async(L - 1, wait_free=False)          # head of the reverse chain
         for l in range(L - 1, -1, -1):
+            prev = l + 1 if l + 1 < L else None
+            if finalize_stream and prev is not None:
+                self.fin.wait_event(self.wgrad_done[prev])
+                ttl.gtp_finalize(staging[prev], main_grad[prev], stream=self.fin)
             out = dX[l] if isinstance(dX, (list, tuple)) else dX
             if folded:
                 ttl.gtp_gather_gemm(dY[l], self.shards[l], out, transpose_w=True)
@@ -76,8 +90,11 @@ class GtpChain:
                 main.wait_event(self.ready[l % 2])
                 ttl.gtp_gather_gemm(dY[l], self.shards[l], out, slot=self.slots[l % 2], transpose_w=True)
                 self.free[l % 2].record(main)
-            prev = l + 1 if l + 1 < L else None
+            in_stream = prev is not None and not finalize_stream
             ttl.gtp_wgrad_rs_finalize(X, dY[l], staging[l],
-                                      staging_prev=staging[prev] if prev is not None else None,
-                                      main_grad_prev=main_grad[prev] if prev is not None else None,
+                                      staging_prev=staging[prev] if in_stream else None,
+                                      main_grad_prev=main_grad[prev] if in_stream else None,
                                       sync=(l == 0), main_grad_cur=main_grad[0] if l == 0 else None)
+            self.wgrad_done[l].record(main)
+        if finalize_stream:
+            main.wait_stream(self.fin)

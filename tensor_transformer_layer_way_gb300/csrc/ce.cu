@@ -12,6 +12,9 @@
 //   3. combine  per token: M = max m_i, S = sum s_i exp(m_i - M), lse = M + log S,
 //               loss_t = lse - sum y_i
 //   4. mean     loss = mean_t loss_t (one CTA, fixed order, fp64 partials)
+//   With a workspace, step 1's epilogue leaves per-tile (max, sum exp) partials, and steps 2-4
+//   are one launch: a CTA per token merges every shard's partials (a warp per shard), combines
+//   the shards, and the last CTA to finish takes the mean.
 //   5. dlogits  dZ_i = (exp(z - lse) - [v == target]) / T -> bf16 (and fp32 in place if asked)
 //   6. dH       sum_i dZ_i W_i as ONE GEMM whose K loop walks the t shards in order, so the
 //               f-backward reduction of the column-parallel head happens in the accumulator.
@@ -87,32 +90,81 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const __grid_constant__ C
   }
 }
 
-// Fused path, grid (T, t), one warp: shard i's statistics for token `tok` from the per-tile
-// partials the LM-head GEMM epilogue left (tps per shard, ntot per token row), and the
-// target logit the owning tile wrote.
-__global__ void __launch_bounds__(32) ce_stats_from_partials_kernel(const float2* part, const float* ztarget,
-                                                                    const int64_t* target, int64_t T, int64_t Vs,
-                                                                    int64_t V, int tps, int64_t ntot, float* stats) {
+// Fused path, one launch for statistics, combine and mean.  grid T, 32 t threads: warp i merges
+// shard i's per-tile partials for token `tok` and writes its three numbers; warp 0 then combines
+// the shards exactly as ce_combine_kernel does.  Every CTA counts itself done on `ticket` after a
+// fence; the CTA that draws the last ticket sums all T per-token losses in fp64 in a fixed order
+// (independent of which CTA is last) and writes the mean.  `ticket` must be 0 at launch.
+__global__ void __launch_bounds__(32 * kMaxShards) ce_stats_combine_mean_kernel(
+    const float2* part, const float* ztarget, const int64_t* target, int64_t T, int64_t Vs, int64_t V, int tps,
+    int64_t ntot, float* stats, float* loss, unsigned int* ticket, int* status) {
+  const int t = static_cast<int>(blockDim.x >> 5);
   const int64_t tok = blockIdx.x;
-  const int i = blockIdx.y;
-  const float2* p = part + tok * ntot + static_cast<int64_t>(i) * tps;
-  float m = -INFINITY, s = 0.0f;
-  for (int j = threadIdx.x; j < tps; j += 32) {
-    const float2 q = p[j];
-    online_merge(m, s, q.x, q.y);
-  }
+  const int i = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  __shared__ float sm[kMaxShards], ss[kMaxShards];
+  __shared__ double red[32 * kMaxShards];
+  __shared__ bool last;
+  {
+    const float2* p = part + tok * ntot + static_cast<int64_t>(i) * tps;
+    float m = -INFINITY, s = 0.0f;
+    // Every load of a batch is issued before the first merge, so a lane has up to 8
+    // independent 8-byte loads in flight.
+    constexpr int U = 8;
+    for (int j0 = lane; j0 < tps; j0 += 32 * U) {
+      float2 q[U];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    online_merge(m, s, m2, s2);
+      for (int u = 0; u < U; ++u) q[u] = j0 + 32 * u < tps ? __ldcs(p + j0 + 32 * u) : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+      for (int u = 0; u < U; ++u) online_merge(m, s, q[u].x, q[u].y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      online_merge(m, s, m2, s2);
+    }
+    if (lane == 0) {
+      const int64_t tg = target[tok];
+      const bool own = tg >= 0 && tg < V && tg / Vs == i;
+      stats[(3 * i + 0) * T + tok] = m;
+      stats[(3 * i + 1) * T + tok] = s;
+      stats[(3 * i + 2) * T + tok] = own ? ztarget[tok] : 0.0f;
+      sm[i] = m;
+      ss[i] = s;
+    }
   }
+  __syncthreads();
   if (threadIdx.x == 0) {
     const int64_t tg = target[tok];
-    const bool own = tg >= 0 && tg < V && tg / Vs == i;
-    stats[(3 * i + 0) * T + tok] = m;
-    stats[(3 * i + 1) * T + tok] = s;
-    stats[(3 * i + 2) * T + tok] = own ? ztarget[tok] : 0.0f;
+    float M = -INFINITY;
+    for (int k = 0; k < t; ++k) M = fmaxf(M, sm[k]);
+    float Ssum = 0.0f;
+    for (int k = 0; k < t; ++k) Ssum += ss[k] * expf(sm[k] - M);
+    const bool ok = tg >= 0 && tg < V;
+    const float zy = ok ? ztarget[tok] : 0.0f;
+    const float lse = M + logf(Ssum);
+    float lt = lse - zy;
+    if (!ok) {
+      atomicCAS(status, 0, TTL_ERR_DEVICE);
+      lt = __int_as_float(0x7fc00000);
+    }
+    stats[(3 * t) * T + tok] = lse;
+    stats[(3 * t + 1) * T + tok] = lt;
+    __threadfence();
+    last = atomicAdd(ticket, 1u) == static_cast<unsigned int>(gridDim.x) - 1u;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const float* lt = stats + (3 * t + 1) * T;
+  double a = 0.0;
+  for (int64_t k = threadIdx.x; k < T; k += blockDim.x) a += static_cast<double>(__ldcg(lt + k));
+  red[threadIdx.x] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double sum = 0.0;
+    for (int k = 0; k < static_cast<int>(blockDim.x); ++k) sum += red[k];
+    *loss = static_cast<float>(sum / static_cast<double>(T));
   }
 }
 
@@ -206,12 +258,13 @@ int64_t ce_tiles_per_shard(int64_t Vs) { return 2 * ((Vs + kGemmBN - 1) / kGemmB
 size_t ce_part_bytes(int t, int64_t T, int64_t Vs) {
   return (static_cast<size_t>(T) * static_cast<size_t>(t * ce_tiles_per_shard(Vs)) * 8 + 255) & ~size_t(255);
 }
+size_t ce_ztarget_bytes(int64_t T) { return (static_cast<size_t>(T) * 4 + 255) & ~size_t(255); }
 }  // namespace
 
 extern "C" size_t ttl_vocab_parallel_ce_workspace_size(int t, int64_t T, int64_t h, int64_t V) {
   (void)h;
   if (t < 1 || t > kMaxShards || T < 0 || V < 0 || V % t) return 0;
-  return ce_part_bytes(t, T, V / t) + static_cast<size_t>(T) * 4;
+  return ce_part_bytes(t, T, V / t) + ce_ztarget_bytes(T) + 256;   // + the fused launch's ticket
 }
 
 extern "C" int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, const ttl_bf16* H,
@@ -284,30 +337,34 @@ extern "C" int ttl_vocab_parallel_ce(int t, int64_t T, int64_t h, int64_t V, con
     if ((rc = batch.launch(s))) return rc;
   }
 
-  // 2. per-shard statistics.
+  // 2-4. per-shard statistics, combine, mean.
   if (fused) {
-    TraceScope trace(s, TTL_K_CE_STATS, 0.0, static_cast<double>(T) * (ntot * 8.0 + 4.0 + 3.0 * t * 4.0));
-    ce_stats_from_partials_kernel<<<dim3(static_cast<unsigned>(T), t), 32, 0, s>>>(part, ztarget, target, T, Vs, V,
-                                                                                  tps, ntot, stats);
-    if ((rc = cuda_check(cudaGetLastError(), "ce_stats_from_partials_kernel launch"))) return rc;
+    unsigned int* ticket = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + ce_part_bytes(t, T, Vs) +
+                                                           ce_ztarget_bytes(T));
+    if ((rc = cuda_check(cudaMemsetAsync(ticket, 0, sizeof(unsigned int), s), "cudaMemsetAsync(ticket)"))) return rc;
+    TraceScope trace(s, TTL_K_CE_STATS, 0.0,
+                     static_cast<double>(T) * (ntot * 8.0 + 4.0 + 8.0 + 3.0 * t * 4.0 + 2.0 * 4.0 + 4.0));
+    ce_stats_combine_mean_kernel<<<static_cast<unsigned>(T), 32 * t, 0, s>>>(part, ztarget, target, T, Vs, V, tps,
+                                                                             ntot, stats, loss, ticket, status);
+    if ((rc = cuda_check(cudaGetLastError(), "ce_stats_combine_mean_kernel launch"))) return rc;
   } else {
     CeShards cs;
     for (int i = 0; i < kMaxShards; ++i) cs.z[i] = i < t ? logits[i] : nullptr;
-    TraceScope trace(s, TTL_K_CE_STATS, 0.0, static_cast<double>(T) * V * 4.0);
-    ce_stats_kernel<<<dim3(static_cast<unsigned>(T), t), 256, 0, s>>>(cs, target, T, Vs, stats);
-    if ((rc = cuda_check(cudaGetLastError(), "ce_stats_kernel launch"))) return rc;
-  }
-
-  // 3. combine the three numbers across shards; 4. mean.
-  {
-    TraceScope trace(s, TTL_K_CE_SMALL, 0.0, static_cast<double>(T) * (3.0 * t + 2.0) * 4.0);
-    ce_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(t, T, V, target, stats, status);
-    if ((rc = cuda_check(cudaGetLastError(), "ce_combine_kernel launch"))) return rc;
-  }
-  {
-    TraceScope trace(s, TTL_K_CE_SMALL, 0.0, static_cast<double>(T) * 4.0);
-    ce_mean_kernel<<<1, 1024, 0, s>>>(stats + (3 * t + 1) * T, T, loss);
-    if ((rc = cuda_check(cudaGetLastError(), "ce_mean_kernel launch"))) return rc;
+    {
+      TraceScope trace(s, TTL_K_CE_STATS, 0.0, static_cast<double>(T) * V * 4.0);
+      ce_stats_kernel<<<dim3(static_cast<unsigned>(T), t), 256, 0, s>>>(cs, target, T, Vs, stats);
+      if ((rc = cuda_check(cudaGetLastError(), "ce_stats_kernel launch"))) return rc;
+    }
+    {
+      TraceScope trace(s, TTL_K_CE_SMALL, 0.0, static_cast<double>(T) * (3.0 * t + 2.0) * 4.0);
+      ce_combine_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(t, T, V, target, stats, status);
+      if ((rc = cuda_check(cudaGetLastError(), "ce_combine_kernel launch"))) return rc;
+    }
+    {
+      TraceScope trace(s, TTL_K_CE_SMALL, 0.0, static_cast<double>(T) * 4.0);
+      ce_mean_kernel<<<1, 1024, 0, s>>>(stats + (3 * t + 1) * T, T, loss);
+      if ((rc = cuda_check(cudaGetLastError(), "ce_mean_kernel launch"))) return rc;
+    }
   }
   if (fwd_only) return TTL_OK;
 

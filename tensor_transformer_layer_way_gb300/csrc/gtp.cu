@@ -300,3 +300,20 @@ extern "C" int ttl_gtp_wgrad_rs_finalize(int g, int64_t M, int64_t K, int64_t N,
   if (sync) return finalize(g, Kg, N, const_cast<const float* const*>(staging_cur), main_grad_cur, s);
   return TTL_OK;
 }
+
+extern "C" int ttl_gtp_finalize(int g, int64_t K, int64_t N, const float* const* staging, float* const* main_grad,
+                                void* stream) {
+  const char* name = "ttl_gtp_finalize";
+  int rc = check_gkn(g, K, N, name);
+  if (rc) return rc;
+  if ((rc = check_shards(g, reinterpret_cast<const void* const*>(staging), "staging"))) return rc;
+  if ((rc = check_shards(g, reinterpret_cast<const void* const*>(main_grad), "main_grad"))) return rc;
+  for (int j = 0; j < g; ++j)
+    for (int k = 0; k < g; ++k)
+      if (static_cast<const void*>(staging[j]) == static_cast<const void*>(main_grad[k]))
+        return set_error(TTL_ERR_ARG, "%s: staging[%d] and main_grad[%d] alias", name, j, k);
+  const int64_t Kg = K / g;
+  if (Kg == 0 || N == 0) return TTL_OK;
+  if ((rc = require_sm103())) return rc;
+  return finalize(g, Kg, N, staging, main_grad, static_cast<cudaStream_t>(stream));
+}

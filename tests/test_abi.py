@@ -92,6 +92,10 @@ def test_gtp_and_ce_validation(lib):
     assert lib.ttl_gtp_gather(8, 64 * 8, 64, sh, 0x90008, None, None) == 3        # misaligned slot
     assert lib.ttl_gtp_gather_gemm(8, 16, 512, 64, 0x90000, sh, None, None, 0xA0000, 2, None) == 1
     assert lib.ttl_gtp_wgrad_rs_finalize(8, 16, 512, 64, 0x90000, 0xA0000, sh, sh, None, 0, None, None) == 1
+    assert lib.ttl_gtp_finalize(0, 512, 64, sh, sh, None) == 1                    # g < 1
+    assert lib.ttl_gtp_finalize(8, 60, 64, sh, sh, None) == 2                     # g does not divide K
+    assert lib.ttl_gtp_finalize(8, 512, 64, sh, None, None) == 1                  # null main_grad
+    assert lib.ttl_gtp_finalize(8, 512, 64, sh, sh, None) == 1                    # staging aliases main_grad
     W = _arr(0x10000, 0x20000)
     L = _arr(0x30000, 0x40000)
     # t does not divide V
@@ -102,7 +106,8 @@ def test_gtp_and_ce_validation(lib):
                                      None, 0, 8, None) == 1
     # workspace too small for the fused statistics
     need = lib.ttl_vocab_parallel_ce_workspace_size(2, 8, 64, 32)
-    assert need == 256 + 8 * 4        # 8 tokens x 2 shards x 2 half tiles x 8 bytes, + 8 target logits
+    # 8 tokens x 2 shards x 2 half tiles x 8 bytes (256), 8 target logits (32 -> 256), a counter (256)
+    assert need == 256 + 256 + 256
     assert lib.ttl_vocab_parallel_ce(2, 8, 64, 32, 0x90000, W, 0xA0000, L, L, 0xB0000, 0xC0000, 0xD0000,
                                      0xE0000, need - 1, 0, None) == 1
     # embedding: t does not divide V, misaligned ids
@@ -177,3 +182,15 @@ def test_static_scratch_size_matches_the_header():
     m = re.search(r"#define\s+TTL_STATIC_WS_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", hdr)
     assert m, "TTL_STATIC_WS_BYTES not found in include/ttl.h"
     assert ttl.STATIC_WS_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_package_exports_every_binding_of_a_library_call():
+    """Each Python wrapper named after a C entry point (the name minus ``ttl_``) is reachable
+    from the package itself."""
+    import tensor_transformer_layer_way_gb300 as pkg
+    from tensor_transformer_layer_way_gb300 import _binding
+    hdr = open(os.path.join(ROOT, "include", "ttl.h")).read()
+    import re
+    for name in re.findall(r"\bttl_([a-z0-9_]+)\s*\(", hdr):
+        if hasattr(_binding, name) and callable(getattr(_binding, name)):
+            assert hasattr(pkg, name), f"{name} is not exported by the package"
