@@ -933,10 +933,13 @@ struct KvCfg {
   static constexpr int V_BYTES = KB * kBKV * 128;         // the CTA's V tile
   static constexpr int SLOT = KB * kBQ * 128;             // a Q tile or a dO tile
   static constexpr int P_BYTES = kBQ * kBKV * 2;          // a P tile, overwritten in place by dS
+  static constexpr int DO_SLOTS = 2;                      // dO_j: read by dP_j and dV_j
+  static constexpr int P_BUFS = 3;                        // P_j, then dS_j: read until dK_j
   static constexpr int OFF_V = 0;
-  static constexpr int OFF_RING = OFF_V + V_BYTES;
-  static constexpr int OFF_P = OFF_RING + kRing * SLOT;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_DO = OFF_V + V_BYTES;
+  static constexpr int OFF_Q = OFF_DO + DO_SLOTS * SLOT;  // one Q slot: Q_j is read by dK_j alone
+  static constexpr int OFF_P = OFF_Q + SLOT;
+  static constexpr int OFF_BAR = OFF_P + P_BUFS * P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
 };
@@ -948,30 +951,36 @@ struct KvCfg {
 //   dS = P (dP - D) / sqrt(d) (zero above the diagonal, where P is zero); dK += dS^T Q_c.
 // Neither P^T nor dS^T is ever formed: the MMAs read the [queries x keys] tiles as MN-major A
 // operands, and the [queries x d] Q and dO tiles loaded K-major double as MN-major B operands.
-// Roles (352 threads): warp 0 loads V once, then dO_j, Q_j through the 4-slot ring; warp 10 loads
-// P_j into the two P buffers; warp 1 issues dP_j, dV_j, then dK_(j-1); warps 2..9 compute dS
-// (two per TMEM lane quadrant) and at the end store dK and dV.
+// Roles (352 threads): warp 0 loads V once, then dO_(j+1) and Q_j (dO one pair ahead: dP_j needs
+// dO_j at the start of pair j, dK_j needs Q_j only a pair later, so dO takes two slots and Q one);
+// warp 10 loads P_j into three P buffers (a P buffer is busy from its load until dK_j has read
+// dS_j, about two pairs); warp 1 issues dP_j, dV_j, then dK_(j-1); warps 2..9 compute dS (two per
+// TMEM lane quadrant) and at the end store dK and dV.
 template <int D>
 __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __grid_constant__ KvParams P) {
   using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sRing = smem + C::OFF_RING;
+  uint8_t* sDO = smem + C::OFF_DO;
+  uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sP = smem + C::OFF_P;
   uint64_t* v_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* ring_full = v_full + 1;
-  uint64_t* ring_empty = ring_full + kRing;
-  uint64_t* dp_full = ring_empty + kRing;
-  uint64_t* dp_empty = dp_full + 2;
-  uint64_t* pb_full = dp_empty + 2;
-  uint64_t* pb_empty = pb_full + 2;
-  uint64_t* pv_done = pb_empty + 2;
-  uint64_t* ds_full = pv_done + 2;
-  uint64_t* acc_full = ds_full + 2;
+  uint64_t* do_full = v_full + 1;              // [DO_SLOTS]
+  uint64_t* do_empty = do_full + C::DO_SLOTS;  // [DO_SLOTS]
+  uint64_t* q_full = do_empty + C::DO_SLOTS;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* dp_full = q_empty + 1;             // [2] the dP buffers in TMEM
+  uint64_t* dp_empty = dp_full + 2;            // [2]
+  uint64_t* pb_full = dp_empty + 2;            // [P_BUFS]
+  uint64_t* pb_empty = pb_full + C::P_BUFS;    // [P_BUFS]
+  uint64_t* pv_done = pb_empty + C::P_BUFS;    // [P_BUFS]
+  uint64_t* ds_full = pv_done + C::P_BUFS;     // [P_BUFS]
+  uint64_t* acc_full = ds_full + C::P_BUFS;
   uint64_t* done_bar = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  static_assert((1 + 2 * C::DO_SLOTS + 2 + 4 + 4 * C::P_BUFS + 2) * 8 + 8 <= 256, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -989,13 +998,17 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
 
   if (threadIdx.x == 0) {
     mbar_init(v_full, 1);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&ring_full[s], 1);
-      mbar_init(&ring_empty[s], 1);   // one commit after the tile's last MMA (dV for dO, dK for Q)
+    for (int s = 0; s < C::DO_SLOTS; ++s) {
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);   // one commit after dV_j, the tile's last MMA
     }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);          // one commit after dK_j
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dp_full[b], 1);
       mbar_init(&dp_empty[b], 8);
+    }
+    for (int b = 0; b < C::P_BUFS; ++b) {
       mbar_init(&pb_full[b], 1);
       mbar_init(&pb_empty[b], 1);
       mbar_init(&pv_done[b], 1);
@@ -1021,34 +1034,59 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Query-tile row and query head of pair j.
+  auto pair_row = [&](int j) { return (kt + j / P.grp) * kBQ; };
+  auto pair_head = [&](int j) { return g * P.grp + j % P.grp; };
+
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------------------------------------------------------- V, then dO_j / Q_j
+      // ---------------------------------------------------------------- V, then dO_(j+1) / Q_j
       bool ok = true;
       mbar_arrive_expect_tx(v_full, C::V_BYTES);
       for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(sV + kb * 16384, &P.v[shard], v_full, g * D + kb * 64, k0);
-      int issued = 0;
-      for (int pos = 0; ok && pos < 2 * npairs; ++pos) {
-        const int slot = pos % kRing;
-        if (!mbar_wait(&ring_empty[slot], (static_cast<uint32_t>(pos / kRing) & 1u) ^ 1u, abort_flag, status, tmo)) {
-          ok = false;
-          break;
-        }
-        const int j = pos >> 1;
-        const int qrow = (kt + j / P.grp) * kBQ;
-        const int c = g * P.grp + j % P.grp;
-        const CUtensorMap* map = (pos & 1) ? &P.q[shard] : &P.dO[shard];   // dO_j at 2j, Q_j at 2j + 1
-        uint8_t* dst = sRing + slot * C::SLOT;
-        mbar_arrive_expect_tx(&ring_full[slot], C::SLOT);
-        for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(dst + kb * 16384, map, &ring_full[slot], c * D + kb * 64, qrow);
-        ++issued;
+      auto load_do = [&](int j) {
+        const int s = j % C::DO_SLOTS;
+        if (!mbar_wait(&do_empty[s], (static_cast<uint32_t>(j / C::DO_SLOTS) & 1u) ^ 1u, abort_flag, status, tmo))
+          return false;
+        mbar_arrive_expect_tx(&do_full[s], C::SLOT);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_2d(sDO + s * C::SLOT + kb * 16384, &P.dO[shard], &do_full[s], pair_head(j) * D + kb * 64,
+                      pair_row(j));
+        return true;
+      };
+      auto load_q = [&](int j) {
+        if (!mbar_wait(q_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag, status, tmo)) return false;
+        mbar_arrive_expect_tx(q_full, C::SLOT);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_2d(sQ + kb * 16384, &P.q[shard], q_full, pair_head(j) * D + kb * 64, pair_row(j));
+        return true;
+      };
+      // Order: dO_0, then for every j: dO_(j+1), Q_j -- Q_j's slot frees only once dK_(j-1) is done.
+      int n_do = 0, n_q = 0;
+      if (npairs > 0) {
+        ok = load_do(0);
+        if (ok) n_do = 1;
       }
+      for (int j = 0; ok && j < npairs; ++j) {
+        if (j + 1 < npairs) {
+          ok = load_do(j + 1);
+          if (!ok) break;
+          ++n_do;
+        }
+        ok = load_q(j);
+        if (!ok) break;
+        ++n_q;
+      }
+      // No copy may still be landing when the CTA leaves: wait (bounded) for the latest phase of
+      // every buffer (an earlier load on a buffer completed before the buffer could be reused).
       int dummy_abort = 0;
-      mbar_wait(v_full, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
-      const int pending = issued < kRing ? issued : kRing;
-      for (int i = issued - pending; i < issued; ++i)
-        mbar_wait(&ring_full[i % kRing], static_cast<uint32_t>(i / kRing) & 1u,
-                  reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
+      volatile int* da = reinterpret_cast<volatile int*>(&dummy_abort);
+      mbar_wait(v_full, 0, da, status, tmo);
+      for (int s = 0; s < C::DO_SLOTS; ++s) {
+        const int jl = n_do - 1 - ((n_do - 1 - s) % C::DO_SLOTS + C::DO_SLOTS) % C::DO_SLOTS;
+        if (jl >= 0) mbar_wait(&do_full[s], static_cast<uint32_t>(jl / C::DO_SLOTS) & 1u, da, status, tmo);
+      }
+      if (n_q > 0) mbar_wait(q_full, static_cast<uint32_t>(n_q - 1) & 1u, da, status, tmo);
     }
     __syncwarp();
   } else if (warp == kThreads / 32) {
@@ -1057,32 +1095,28 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
       bool ok = true;
       int started = 0;
       auto prefetch_pair = [&](int j) {
-        const int qrow = (kt + j / P.grp) * kBQ;
-        const int c = g * P.grp + j % P.grp;
-        tma_prefetch_3d(&P.p[shard], k0, qrow, c);
-        tma_prefetch_3d(&P.p[shard], k0 + 64, qrow, c);
+        tma_prefetch_3d(&P.p[shard], k0, pair_row(j), pair_head(j));
+        tma_prefetch_3d(&P.p[shard], k0 + 64, pair_row(j), pair_head(j));
       };
-      for (int j = 0; j < 2 && j < npairs; ++j) prefetch_pair(j);
+      for (int j = 0; j < 3 && j < npairs; ++j) prefetch_pair(j);
       for (int j = 0; ok && j < npairs; ++j) {
-        const int b = j & 1;
-        if (j + 2 < npairs) prefetch_pair(j + 2);   // two pairs ahead into L2
-        if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
+        const int b = j % C::P_BUFS;
+        if (j + 3 < npairs) prefetch_pair(j + 3);   // three pairs ahead into L2
+        if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j / C::P_BUFS) & 1u) ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
-        const int qrow = (kt + j / P.grp) * kBQ;
-        const int c = g * P.grp + j % P.grp;
         mbar_arrive_expect_tx(&pb_full[b], C::P_BYTES);
-        tma_load_3d(sP + b * C::P_BYTES, &P.p[shard], &pb_full[b], k0, qrow, c);
-        tma_load_3d(sP + b * C::P_BYTES + 16384, &P.p[shard], &pb_full[b], k0 + 64, qrow, c);
+        tma_load_3d(sP + b * C::P_BYTES, &P.p[shard], &pb_full[b], k0, pair_row(j), pair_head(j));
+        tma_load_3d(sP + b * C::P_BYTES + 16384, &P.p[shard], &pb_full[b], k0 + 64, pair_row(j), pair_head(j));
         ++started;
       }
       int dummy_abort = 0;
-      for (int b = 0; b < 2; ++b) {
-        const int jl = started - 1 - ((started - 1 - b) & 1);   // last started tile on buffer b
+      for (int b = 0; b < C::P_BUFS; ++b) {
+        const int jl = started - 1 - ((started - 1 - b) % C::P_BUFS + C::P_BUFS) % C::P_BUFS;   // last on b
         if (jl >= 0)
-          mbar_wait(&pb_full[b], static_cast<uint32_t>(jl >> 1) & 1u, reinterpret_cast<volatile int*>(&dummy_abort),
-                    status, tmo);
+          mbar_wait(&pb_full[b], static_cast<uint32_t>(jl / C::P_BUFS) & 1u,
+                    reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
       }
     }
     __syncwarp();
@@ -1092,32 +1126,26 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
       bool ok = mbar_wait(v_full, 0, abort_flag, status, tmo);
       tc_fence_after_sync();
       const uint64_t vkd = smem_desc_sw128(smem_u32(sV), 16, 1024);   // V, K-major B of dP
-      const uint32_t ring0 = smem_u32(sRing);
+      const uint32_t do0 = smem_u32(sDO);
+      const uint32_t qaddr = smem_u32(sQ);
       const uint32_t paddr = smem_u32(sP);
       const uint32_t idesc_dp = idesc_bf16_f32(kBQ, kBKV, false, false);   // [queries x keys]
       const uint32_t idesc_acc = idesc_bf16_f32(kBKV, D, true, true);      // [keys x d], A and B MN-major
       const uint32_t t_dk = tmem_base + 2 * kBKV;
       const uint32_t t_dv = tmem_base + 2 * kBKV + D;
-      auto wait_pos = [&](int pos) {
-        const int slot = pos % kRing;
-        if (!mbar_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u, abort_flag, status, tmo))
-          return -1;
-        tc_fence_after_sync();
-        return slot;
-      };
-      int qslot_prev = -1;
       for (int j = 0; ok && j <= npairs; ++j) {
         if (j < npairs) {
           const int b = j & 1;
+          const int ds = j % C::DO_SLOTS;
+          const int pbuf = j % C::P_BUFS;
           // dP_j = dO_j V^T  [queries x keys]
-          const int dslot = wait_pos(2 * j);
-          if (dslot < 0 ||
+          if (!mbar_wait(&do_full[ds], static_cast<uint32_t>(j / C::DO_SLOTS) & 1u, abort_flag, status, tmo) ||
               !mbar_wait(&dp_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t daddr = ring0 + dslot * C::SLOT;
+          const uint32_t daddr = do0 + ds * C::SLOT;
           const uint64_t dd = smem_desc_sw128(daddr, 16, 1024);
           for (int kb = 0; kb < C::KB; ++kb) {
 #pragma unroll
@@ -1129,12 +1157,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
           }
           umma_commit(&dp_full[b]);
           // dV += P_j^T dO_j: A = P tile read MN-major (keys contiguous), B = dO tile read MN-major
-          if (!mbar_wait(&pb_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo)) {
+          if (!mbar_wait(&pb_full[pbuf], static_cast<uint32_t>(j / C::P_BUFS) & 1u, abort_flag, status, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint64_t pmd = smem_desc_sw128(paddr + b * C::P_BYTES, 16384, 1024);
+          const uint64_t pmd = smem_desc_sw128(paddr + pbuf * C::P_BYTES, 16384, 1024);
           const uint64_t dmd = smem_desc_sw128(daddr, 16384, 1024);
 #pragma unroll
           for (int kq = 0; kq < kBQ / 16; ++kq) {   // K = the 128 queries, 16 per MMA
@@ -1142,33 +1170,31 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
             const uint64_t bd = desc_advance(dmd, kq * 2048);
             umma_bf16(t_dv, ad, bd, idesc_acc, (j | kq) ? 1u : 0u);
           }
-          umma_commit(&pv_done[b]);
-          umma_commit(&ring_empty[dslot]);          // the dO tile's last MMA (dP's are earlier)
+          umma_commit(&pv_done[pbuf]);
+          umma_commit(&do_empty[ds]);               // the dO tile's last MMA (dP's are earlier)
         }
         if (ok && j > 0) {
           // dK += dS_(j-1)^T Q_(j-1): A = dS (in the P buffer) MN-major, B = Q tile MN-major
           const int jp = j - 1;
-          const int b = jp & 1;
-          const int qslot = wait_pos(2 * jp + 1);
-          if (qslot < 0 || !mbar_wait(&ds_full[b], static_cast<uint32_t>(jp >> 1) & 1u, abort_flag, status, tmo)) {
+          const int pbuf = jp % C::P_BUFS;
+          if (!mbar_wait(q_full, static_cast<uint32_t>(jp) & 1u, abort_flag, status, tmo) ||
+              !mbar_wait(&ds_full[pbuf], static_cast<uint32_t>(jp / C::P_BUFS) & 1u, abort_flag, status, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint64_t smd = smem_desc_sw128(paddr + b * C::P_BYTES, 16384, 1024);
-          const uint64_t qmd = smem_desc_sw128(ring0 + qslot * C::SLOT, 16384, 1024);
+          const uint64_t smd = smem_desc_sw128(paddr + pbuf * C::P_BYTES, 16384, 1024);
+          const uint64_t qmd = smem_desc_sw128(qaddr, 16384, 1024);
 #pragma unroll
           for (int kq = 0; kq < kBQ / 16; ++kq) {
             const uint64_t ad = desc_advance(smd, kq * 2048);
             const uint64_t bd = desc_advance(qmd, kq * 2048);
             umma_bf16(t_dk, ad, bd, idesc_acc, (jp | kq) ? 1u : 0u);
           }
-          umma_commit(&pb_empty[b]);
-          umma_commit(&ring_empty[qslot]);
-          qslot_prev = qslot;
+          umma_commit(&pb_empty[pbuf]);
+          umma_commit(q_empty);
         }
       }
-      (void)qslot_prev;
       if (ok) umma_commit(acc_full);
       umma_commit(done_bar);
       int dummy_abort = 0;
@@ -1186,8 +1212,9 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
     bool ok = true;
     for (int j = 0; ok && j < npairs; ++j) {
       const int b = j & 1;
-      const int q = (kt + j / P.grp) * kBQ + r;
-      const int c = g * P.grp + j % P.grp;
+      const int pbuf = j % C::P_BUFS;
+      const int q = pair_row(j) + r;
+      const int c = pair_head(j);
       const float Dq = q < P.T ? P.D[(static_cast<int64_t>(shard) * P.nql + c) * P.T + q] : 0.0f;
       ok = mbar_wait(&dp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -1203,13 +1230,13 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
       __syncwarp();
       if (lane == 0) mbar_arrive(&dp_empty[b]);
       // dV's MMA has read P_j: it may now be overwritten by dS_j
-      ok = mbar_wait(&pv_done[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
+      ok = mbar_wait(&pv_done[pbuf], static_cast<uint32_t>(j / C::P_BUFS) & 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      uint8_t* row = my_row + b * C::P_BYTES;
+      uint8_t* row = my_row + pbuf * C::P_BYTES;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
@@ -1228,7 +1255,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ds_full[b]);
+      if (lane == 0) mbar_arrive(&ds_full[pbuf]);
     }
     // dK and dV rows (keys): this warp stores half of the d columns of each
     if (ok) ok = mbar_wait(acc_full, 0, abort_flag, status, tmo);
