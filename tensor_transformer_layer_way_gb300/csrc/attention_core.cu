@@ -16,8 +16,8 @@
 // The probabilities the backward reads are therefore written once; nothing re-reads them here.
 //
 // Roles (352 threads): warp 0 issues TMA loads (Q once; then the pairs (K_0, K_1), (K_2, K_3), ...
-// for pass 1, each filling two adjacent slots, and K_0, V_0, K_1, V_1, ... for pass 2 through a
-// 4-slot ring); warp 1 issues the MMAs; warp 10 issues the TMA stores of P; warps 2..9 run the
+// for pass 1, each filling two adjacent slots, and K_0, K_1, V_0, K_2, V_1, ... -- K a tile ahead
+// of V -- for pass 2 through a 4-slot ring); warp 1 issues the MMAs; warp 10 issues the TMA stores of P; warps 2..9 run the
 // softmax: two warps per TMEM lane quadrant, each on half of a score group's keys (and, at the
 // end, half of O's d columns).  In pass 2 the MMA warp
 // issues whichever is ready first, the next S or the next P V, so the softmax of tile j
@@ -189,6 +189,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
   const int ntiles = qt + 1;   // key tiles 0..qt (qt * 128 < T)
   const int npairs = (ntiles + 1) >> 1;   // pass-1 score groups of two key tiles
   const int p1_pos = 2 * npairs;          // ring positions of pass 1
+  // Pass-2 ring positions: K_0, K_1, V_0, K_2, V_1, ..., K_(n-1), V_(n-2), V_(n-1).  V_j's slot
+  // frees only when P_(j-2) V_(j-2) is done, and the producer fills positions in order, so with
+  // K_(j+1) behind V_j the score tile S_(j+1) would wait for that P V; K one tile ahead of V
+  // breaks the chain.  Each slot still fills and frees in position order.
+  auto p2_k_pos = [&](int j) { return p1_pos + (j == 0 ? 0 : 2 * j - 1); };
+  auto p2_v_pos = [&](int j) { return p1_pos + (j == ntiles - 1 ? 2 * ntiles - 1 : 2 * j + 2); };
   int* status = P.status;
   const uint64_t tmo = P.timeout_ns;
 
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(sQ + kb * 16384, &P.q[shard], q_full, c * D + kb * 64, q0);
       // ring sequence: pass 1 the pairs (K_0, K_1), (K_2, K_3), ... two positions each; pass 2
-      // K_0, V_0, K_1, V_1, ...
+      // K_0, K_1, V_0, K_2, V_1, ..., K_(n-1), V_(n-2), V_(n-1)
       const int nseq = p1_pos + 2 * ntiles;
       int issued = 0;
       for (int seq = 0; ok && seq < nseq; ++seq) {
@@ -260,8 +266,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
           ++issued;
           continue;
         }
-        const bool is_v = (seq - p1_pos) & 1;
-        const int j = (seq - p1_pos) >> 1;
+        // Pass 2 order: K_0, then K_(j+1) before V_j (K runs a tile ahead, see p2_k_pos).
+        const int k2 = seq - p1_pos;
+        const bool is_v = k2 != 0 && (k2 == 2 * ntiles - 1 || (k2 & 1) == 0);
+        const int j = k2 == 0 ? 0 : (k2 == 2 * ntiles - 1 ? ntiles - 1 : (is_v ? k2 / 2 - 1 : (k2 + 1) / 2));
         if (!is_v) {
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_2d(dst + kb * 16384, &P.k[shard], &ring_full[slot], g * D + kb * 64, j * kBKV);
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
       while (ok && np < ntiles) {
         bool progress = false;
         if (ns < ntiles) {
-          const int pos = p1_pos + 2 * ns;
+          const int pos = p2_k_pos(ns);
           const int slot = pos % kRing;
           const int b = sj & 1;
           if (mbar_test_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u) &&
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
           }
         }
         if (ok && np < ns) {
-          const int pos = p1_pos + 2 * np + 1;
+          const int pos = p2_v_pos(np);
           const int vslot = pos % kRing;
           const int b = np & 1;
           if (mbar_test_wait(&ring_full[vslot], static_cast<uint32_t>(pos / kRing) & 1u) &&
