@@ -321,11 +321,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
       const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKV, false, false);
       const uint32_t idesc_o = idesc_bf16_f32(kBQ, D, false, true);
       int sj = 0;            // S tiles issued (both passes), selects the score buffer
+      // Pass 2's S_ns, issued once the caller has seen its K tile loaded and its score buffer free.
+      // The K slot is released by a softmax thread once S_ns is complete (one commit fewer here).
       auto issue_s = [&](int slot) {
         const int b = sj & 1;
-        const uint32_t sph = static_cast<uint32_t>(sj >> 1) & 1u;
-        if (!mbar_wait(&s_empty[b], sph ^ 1u, abort_flag, status, tmo)) return false;
-        tc_fence_after_sync();
         const uint64_t kd = smem_desc_sw128(ring0 + slot * C::SLOT, 16, 1024);
         for (int kb = 0; kb < C::KB; ++kb) {
 #pragma unroll
@@ -335,7 +334,6 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
             umma_bf16(tmem_base + b * kBKV, ad, bd, idesc_s, (kb | kk) ? 1u : 0u);
           }
         }
-        umma_commit(&ring_empty[slot]);
         umma_commit(&s_full[b]);
         ++sj;
         return true;
@@ -369,9 +367,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
             umma_bf16(tmem_base + b * 2 * kBKV, ad, bd, idesc_w, (kb | kk) ? 1u : 0u);
           }
         }
-        umma_commit(&ring_empty[s0]);
-        umma_commit(&ring_empty[s1]);
-        umma_commit(&s_full[b]);
+        umma_commit(&s_full[b]);   // a softmax thread releases both K slots once this completes
         ++sj;
       }
       // Pass 2's score buffers (columns [0, 256)) overlap pass 1's buffer 0, whose last group may
@@ -381,7 +377,11 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
       // p1 + 2 ns, a free score buffer) or the next P_np V_np (V_np at p1 + 2 np + 1, P_np
       // written) -- so that a P V never waits behind a late K tile, nor an S behind a late softmax.
       int ns = 0, np = 0;
-      uint64_t t_idle = globaltimer_ns();
+      // The wall-clock timeout is measured from the start of an idle stretch: the timer is read
+      // when polling first finds nothing to issue, never on the path between two MMA groups
+      // (a read costs about 200 cycles, during which the tensor pipe would run dry).
+      uint64_t t_idle = 0;
+      bool idle = false;
       while (ok && np < ntiles) {
         bool progress = false;
         if (ns < ntiles) {
@@ -420,9 +420,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
           }
         }
         if (progress) {
-          t_idle = globaltimer_ns();
+          idle = false;
         } else if (*abort_flag) {
           ok = false;
+        } else if (!idle) {
+          idle = true;
+          t_idle = globaltimer_ns();
         } else if (globaltimer_ns() - t_idle > tmo) {
           if (status) atomicCAS(status, 0, TTL_ERR_TIMEOUT);
           *abort_flag = 1;
@@ -456,6 +459,11 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
+      }
+      // The group's MMAs are complete, so its two K tiles (ring positions 2 pg, 2 pg + 1) are free.
+      if (warp == 2 && lane == 0) {
+        mbar_arrive(&ring_empty[(2 * pg) % kRing]);
+        mbar_arrive(&ring_empty[(2 * pg + 1) % kRing]);
       }
       tc_fence_after_sync();
       uint32_t ra[32], rb[32], rc[32], rd[32];
@@ -498,6 +506,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
         ok = false;
         break;
       }
+      // S_j is complete: its K tile's ring slot is free.
+      if (warp == 2 && lane == 0) mbar_arrive(&ring_empty[p2_k_pos(j) % kRing]);
       tc_fence_after_sync();
       uint32_t r0[32], r1[32];
       tmem_ld_32x32b_x32(lane_base + b * kBKV + half * 64, r0);
