@@ -83,9 +83,6 @@ struct CoreCfg {
   static_assert(T_P + 2 * (kBKV / 2) <= kTmemCols, "tensor memory layout");
 };
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -99,16 +96,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// All but the newest N committed store groups have finished reading shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// All committed store groups have completed.
-__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Folds 64 scores of one row (r0: keys 0..31, r1: keys 32..63 of the chunk, fp32 bits) into
 // the row's running max m and sum l of 2^(s k - m); only the first nv keys count (nv <= 0: none).

@@ -11,7 +11,7 @@
 //   warps 2..5  epilogue: tcgen05.ld the accumulator rows, apply the fused op (bias,
 //               GeLU, SwiGLU, their derivatives) and store bf16/fp32 to global memory.
 //
-// Two variants share the code:
+// Three variants share the code:
 //   single CTA  (PAIR = false): TILE_M = 128, MMA M=128 N=256, 4 stages of 48 KiB.
 //   CTA pair    (PAIR = true) : a cluster of two CTAs on two SMs computes a 256 x 256 tile
 //               with tcgen05.mma.cta_group::2 (M=256 N=256).  Each CTA holds its own 128 A
@@ -19,6 +19,13 @@
 //               shared memory once per pair; each stage is 32 KiB and 6 stages fit.  Both
 //               CTAs' TMA loads complete on the leader CTA's full barrier, the leader alone
 //               issues MMAs, and its commits arrive on both CTAs' barriers (multicast).
+//   wide pair   (WIDE = true) : 256 x 512 tiles for plain bf16 outputs.  Each K step issues two
+//               independent N=256 MMAs into the halves of one 512-column accumulator: MMAs
+//               into one accumulator wait for each other, two chains overlap, and the operand
+//               bytes per MMA drop by a quarter (each stage: 16 KiB of A, 32 KiB of B per CTA,
+//               4 stages).  With TMEM full the epilogue cannot overlap the next tile's MMAs, so
+//               8 epilogue warps empty the accumulator into shared-memory staging (partly the
+//               ring slots of the next tile's k-blocks 2 and 3) and write it with TMA stores.
 //
 // Every mbarrier wait is bounded in wall time; a timeout records TTL_ERR_TIMEOUT, all roles
 // leave their loops, in-flight copies and MMAs are waited for (again bounded), TMEM is
@@ -45,20 +52,33 @@ constexpr int BN = kGemmBN;        // accumulator columns per tile
 constexpr int BK = 64;             // K per stage
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int GROUP_M = 16;
-constexpr int NUM_THREADS = 192;   // producer warp, MMA warp, 4 epilogue warps (one per TMEM lane quadrant)
+constexpr int STG_BOX = 4096;      // wide epilogue: one TMA store box, 32 rows x 64 bf16 columns
 
-template <bool PAIR>
+// WIDE (a CTA pair only): 256 x 512 output tiles, two N = 256 MMAs per K step into the two
+// halves of a single 512-column accumulator, plain bf16 epilogue through TMA stores.
+template <bool PAIR, bool WIDE = false>
 struct Cfg {
+  static_assert(!WIDE || PAIR, "the wide tile is a CTA-pair tile");
   static constexpr int TILE_M = PAIR ? 256 : 128;     // rows per tile (both CTAs of a pair)
-  static constexpr int B_COLS = PAIR ? 128 : 256;     // B columns held by one CTA
+  static constexpr int TILE_N = WIDE ? 2 * BN : BN;   // output columns per (unpaired) tile
+  static constexpr int B_COLS = WIDE ? 256 : PAIR ? 128 : 256;   // B columns held by one CTA
   static constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
   static constexpr int B_BYTES = B_COLS * BK * 2;     // 16 or 32 KiB
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = PAIR ? 7 : 4;
+  static constexpr int STAGES = WIDE ? 4 : PAIR ? 7 : 4;
   static constexpr int TX_BYTES = PAIR ? 2 * STAGE : STAGE;   // counted on the (leader's) full barrier
+  // producer warp, MMA warp, then the epilogue warps: one per TMEM lane quadrant, two in the
+  // wide kernel (one per 256-column half of the accumulator)
+  static constexpr int THREADS = WIDE ? 320 : 192;
+  static constexpr int EPI_WARPS = THREADS / 32 - 2;
   static constexpr int SCHED_BYTES = 1280;   // the shared copy of the tile schedule
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + SCHED_BYTES;
+  // Wide epilogue staging: 32 boxes, 12 in each of the two ring slots it borrows at a tile's
+  // end and 8 in a region of their own after the barriers and the schedule.
+  static constexpr int STG_OFF = STAGES * STAGE + 2048;
+  static constexpr int SMEM = WIDE ? STG_OFF + 8 * STG_BOX + 1024 /*align slack*/
+                                   : STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + SCHED_BYTES;
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+  static_assert(!WIDE || (STAGE % STG_BOX == 0 && STAGE / STG_BOX == 12), "wide staging layout");
 };
 
 struct TileCoord {
@@ -74,9 +94,14 @@ struct SchedTable {
   int32_t p_tn0[kMaxProblems];
   int32_t p_kb[kMaxProblems];      // k-blocks of each of the problem's tiles (all segments)
   uint32_t p_flags[kMaxProblems];  // bit 0: A MN-major, bit 1: B MN-major, bit 2: 128-column MMAs
+  // Per group, what the MMA thread needs when every problem of the group has the same k-block
+  // count and flags: bit 31 set, flags in bits 0..2, k-blocks from bit 3.  The MMA thread then
+  // skips the full tile decode, which at a tile change leaves the tensor pipe waiting.
+  uint32_t g_mma[kMaxProblems];
   int32_t ngroups;
 };
 static_assert(sizeof(SchedTable) <= Cfg<true>::SCHED_BYTES, "schedule table beyond its space");
+static_assert(256 + Cfg<true>::SCHED_BYTES <= 2048, "barriers and schedule overlap the wide staging");
 
 // Linear tile index -> (problem, m-tile, n-tile).  Inside a tile group the order is: bands
 // of GROUP_M m-tiles; within a band, n-tiles across all of the group's problems; within
@@ -334,9 +359,9 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
 
 // ------------------------------------------------------------------ the kernel
 
-template <bool PAIR>
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams P) {
-  using C = Cfg<PAIR>;
+template <bool PAIR, bool WIDE = false>
+__global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams P) {
+  using C = Cfg<PAIR, WIDE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Stages must sit on 1024-byte boundaries for the 128-byte swizzle atoms.  The offset is
   // the same in both CTAs of a pair, which the pair MMA's shared descriptors rely on.
@@ -346,7 +371,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
   uint64_t* tfull_bar = empty_bar + C::STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* done_bar = tempty_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* stg_bar = done_bar + 1;   // wide: the epilogue has handed its borrowed ring slots back
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   SchedTable* sched = reinterpret_cast<SchedTable*>(smem + C::STAGES * C::STAGE + 256);
 
@@ -364,9 +390,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], PAIR ? 8 : 4);   // every epilogue warp of the pair arrives
+      mbar_init(&tempty_bar[a], (PAIR ? 2 : 1) * C::EPI_WARPS);   // every epilogue warp of the pair arrives
     }
     mbar_init(done_bar, 1);
+    mbar_init(stg_bar, C::EPI_WARPS);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -390,6 +417,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       sched->p_kb[i] = kb;
       sched->p_flags[i] = (pr.a_mn ? 1u : 0u) | (pr.b_mn ? 2u : 0u) | (pr.half_n ? 4u : 0u);
     }
+  }
+  if (threadIdx.x < P.ngroups) {
+    const TileGroup& g = P.groups[threadIdx.x];
+    uint32_t word = 0;
+    bool uniform = true;
+    for (int j = g.first; j < g.first + g.count; ++j) {
+      const Problem& pr = P.probs[j];
+      int kb = 0;
+      for (int s = 0; s < pr.nseg; ++s) kb += pr.seg[s].kblocks;
+      const uint32_t w = (pr.a_mn ? 1u : 0u) | (pr.b_mn ? 2u : 0u) | (pr.half_n ? 4u : 0u) |
+                         (static_cast<uint32_t>(kb) << 3);
+      if (j == g.first) word = w;
+      else if (w != word) uniform = false;
+    }
+    sched->g_mma[threadIdx.x] = (uniform && g.count > 0 && (word >> 3) < (1u << 28)) ? (word | 0x80000000u) : 0u;
   }
   if (threadIdx.x == 0) sched->ngroups = P.ngroups;
   if (warp == 1) {
@@ -418,8 +460,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       int issued = 0;
       bool ok = true;
       int gi = 0;
-      for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
+      int tile_seq = 0;   // tiles this worker has loaded so far
+      for (int tile = unit; ok && tile < P.total_tiles; tile += nunits, ++tile_seq) {
         const TileCoord c = decode_tile_s(*sched, tile, gi);
+        int lkb = 0;      // k-block index within the tile, over its segments
         const Problem& pr = P.probs[c.p];
         int am = pr.a_m0 + c.tm * C::TILE_M + static_cast<int>(rank) * 128;
         int slab = 0;
@@ -433,12 +477,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
           const CUtensorMap* mb0 = &P.maps[sg.map_b];
           const CUtensorMap* mb1 = pr.paired ? &P.maps[sg.map_b2] : mb0;
           const int bnb = pr.b_n0 + sg.b_n1;
-          const int bn0 = pr.paired ? bnb + c.tn * (BN / 2) : bnb + c.tn * BN;
+          const int bn0 = pr.paired ? bnb + c.tn * (BN / 2) : bnb + c.tn * C::TILE_N;
           // The second half of the B columns: a pair's second CTA supplies columns
           // [N/2, N) of the MMA (64 of a 128-column one); paired tiles share coordinates.
           const int bn1 = pr.paired ? bn0 : bn0 + (pr.half_n ? BN / 4 : BN / 2);
           const bool b_half = !PAIR && pr.half_n;   // one CTA, 128 columns: no second B box
-          for (int kb = 0; kb < sg.kblocks; ++kb) {
+          for (int kb = 0; kb < sg.kblocks; ++kb, ++lkb) {
+            // Wide: the previous tile's epilogue borrowed the ring slots of this tile's k-blocks
+            // 2 and 3 (every tile has at least 3) as staging; wait until it hands them back.
+            if (WIDE && lkb == 2 && tile_seq > 0 &&
+                !mbar_wait(stg_bar, static_cast<uint32_t>(tile_seq - 1) & 1u, abort_flag, status, tmo)) {
+              ok = false;
+              break;
+            }
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, status, tmo)) {
               ok = false;
               break;
@@ -458,13 +509,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
                 tma_load_2d_pair(sa, ma, fb, am, ka);
                 tma_load_2d_pair(sa + 8192, ma, fb, am + 64, ka);
               }
-              const CUtensorMap* mb = rank ? mb1 : mb0;
-              const int bn = rank ? bn1 : bn0;
-              if (!pr.b_mn) {
-                tma_load_2d_pair(sb, mb, fb, kbb, bn);
+              if (WIDE) {
+                // This CTA's 128 columns of each 256-column half: [r 128, r 128 + 128) of the
+                // first half, the same of the second half 16 KiB further on.
+                const int bw = bn0 + static_cast<int>(rank) * (BN / 2);
+                if (!pr.b_mn) {
+                  tma_load_2d_pair(sb, mb0, fb, kbb, bw);
+                  tma_load_2d_pair(sb + 16384, mb0, fb, kbb, bw + BN);
+                } else {
+                  tma_load_2d_pair(sb, mb0, fb, bw, kbb);
+                  tma_load_2d_pair(sb + 8192, mb0, fb, bw + 64, kbb);
+                  tma_load_2d_pair(sb + 16384, mb0, fb, bw + BN, kbb);
+                  tma_load_2d_pair(sb + 24576, mb0, fb, bw + BN + 64, kbb);
+                }
               } else {
-                tma_load_2d_pair(sb, mb, fb, bn, kbb);
-                tma_load_2d_pair(sb + 8192, mb, fb, bn + 64, kbb);
+                const CUtensorMap* mb = rank ? mb1 : mb0;
+                const int bn = rank ? bn1 : bn0;
+                if (!pr.b_mn) {
+                  tma_load_2d_pair(sb, mb, fb, kbb, bn);
+                } else {
+                  tma_load_2d_pair(sb, mb, fb, bn, kbb);
+                  tma_load_2d_pair(sb + 8192, mb, fb, bn + 64, kbb);
+                }
               }
             } else {
               mbar_arrive_expect_tx(&full_bar[stage], b_half ? C::TX_BYTES - 16384 : C::TX_BYTES);
@@ -524,16 +590,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       const uint32_t sbase = smem_u32(smem);
       int gi = 0;
       for (int tile = unit; ok && tile < P.total_tiles; tile += nunits) {
-        const int pi = decode_tile_s(*sched, tile, gi).p;
-        const uint32_t fl = sched->p_flags[pi];
-        const int nkb = sched->p_kb[pi];
+#pragma unroll 1
+        while (gi + 1 < sched->ngroups && tile >= sched->g_start[gi + 1]) ++gi;
+        uint32_t fl;
+        int nkb;
+        const uint32_t gw = sched->g_mma[gi];
+        if (gw & 0x80000000u) {
+          fl = gw & 7u;
+          nkb = static_cast<int>((gw >> 3) & 0x0FFFFFFFu);
+        } else {
+          const int pi = decode_tile_s(*sched, tile, gi).p;
+          fl = sched->p_flags[pi];
+          nkb = sched->p_kb[pi];
+        }
         const bool a_mn = fl & 1u, b_mn = fl & 2u;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + (WIDE ? 0u : static_cast<uint32_t>(acc * BN));
         const uint32_t idesc = idesc_bf16_f32(C::TILE_M, (fl & 4u) ? BN / 2 : BN, a_mn, b_mn);
         const uint32_t a_step = a_mn ? 2048u : 32u;
         const uint32_t b_step = b_mn ? 2048u : 32u;
@@ -554,8 +630,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t adesc = desc_advance(ad0, kk * a_step);
               const uint64_t bdesc = desc_advance(bd0, kk * b_step);
-              if (PAIR) umma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
-              else umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+              if (PAIR) {
+                umma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+                // Wide: the second half into accumulator columns [256, 512); the two chains
+                // are independent, so neither MMA waits for the other's accumulator.
+                if (WIDE) umma_bf16_pair(d_tmem + BN, adesc, desc_advance(bdesc, 16384), idesc, accumulate);
+              } else {
+                umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+              }
               accumulate = 1;
             }
             // Frees this stage in both CTAs once the MMAs reading it are done.
@@ -570,7 +652,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
         if (!ok) break;
         if (PAIR) umma_commit_pair(&tfull_bar[acc], 0x3);
         else umma_commit(&tfull_bar[acc]);
-        if (++acc == 2) {
+        if (WIDE) {
+          acc_phase ^= 1u;   // one accumulator: the next tile waits for this tile's epilogue
+        } else if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -582,6 +666,86 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tcgen05_kernel(const __gr
       mbar_wait(done_bar, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
     }
     __syncwarp();
+  } else if (WIDE) {
+    // ---------------------------------------------------------------- wide epilogue warps
+    // Two warps per TMEM lane quadrant, one per 256-column half.  A warp moves its 32 rows x
+    // 256 columns from TMEM through registers (rounded to bf16) into four swizzled 32 x 64 staging
+    // boxes, hands the accumulator back, then writes the boxes with TMA stores.  The staging
+    // lives in the two ring slots that the next tile's k-blocks 2 and 3 will use (both free once
+    // this tile's MMAs are done; the producer waits for stg_bar before refilling them) and in a
+    // region of its own, so the accumulator is free again after the TMEM reads alone.
+    const int ew = warp - 2;                // 0 .. EPI_WARPS - 1
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int h2 = ew >> 2;                 // accumulator half
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty_bar[0]), 0);
+    uint32_t acc_phase = 0;
+    int gi = 0;
+    int64_t kb_end = 0;                     // k-blocks loaded through the current tile
+    for (int tile = unit; tile < P.total_tiles; tile += nunits) {
+      const TileCoord c = decode_tile_s(*sched, tile, gi);
+      const Problem& pr = P.probs[c.p];
+      kb_end += sched->p_kb[c.p];
+      const bool ready = mbar_wait(&tfull_bar[0], acc_phase, abort_flag, status, tmo);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after_sync();
+      uint8_t* const slot_a = smem + static_cast<int>((kb_end + 2) % C::STAGES) * C::STAGE;
+      uint8_t* const slot_b = smem + static_cast<int>((kb_end + 3) % C::STAGES) * C::STAGE;
+      const int col0 = c.tn * C::TILE_N + h2 * BN;   // output column of this warp's first box
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h2 * BN);
+      // Staging box j of this warp: boxes 0..11 in slot_a, 12..23 in slot_b, 24..31 in the own region.
+      auto box = [&](int j) -> uint8_t* {
+        const int b = 4 * ew + j;
+        return b < 12 ? slot_a + b * STG_BOX : b < 24 ? slot_b + (b - 12) * STG_BOX : smem + C::STG_OFF + (b - 24) * STG_BOX;
+      };
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        uint32_t r0[32], r1[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tb + j * 64, r0);
+        tmem_ld_32x32b_x32(tb + j * 64 + 32, r1);
+        tmem_ld_wait();
+        float v[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = __uint_as_float(r0[i]);
+          v[32 + i] = __uint_as_float(r1[i]);
+        }
+        // Row `lane` of the box: 128 bytes, 16-byte chunk k at position k ^ (row mod 8) (the
+        // 128-byte swizzle of the output tensor map).
+        uint8_t* rowp = box(j) + lane * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 w = make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                                     pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+          *reinterpret_cast<uint4*>(rowp + ((k ^ (lane & 7)) << 4)) = w;
+        }
+      }
+      // Every TMEM read of this warp is complete (tcgen05.wait::ld): the MMA may start the next tile.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+      // The generic-proxy staging writes must be visible to the TMA engine's reads.
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int y = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + q * 32;
+        if (y < pr.M) {
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            if (col0 + j * 64 >= pr.N) break;
+            tma_store_2d(&P.maps[pr.omap], box(j), col0 + j * 64, y);
+          }
+        }
+        bulk_commit_group();
+        bulk_wait_group_read<0>();   // the boxes may be overwritten: hand the borrowed slots back
+        mbar_arrive(stg_bar);
+      }
+      __syncwarp();
+      acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group_all();   // every store complete before shared memory goes away
+    __syncwarp();
+    tc_fence_before_sync();
   } else {
     // ---------------------------------------------------------------- epilogue warps
     // One warp per TMEM lane quadrant, storing both halves of the accumulator columns in turn.
@@ -666,6 +830,7 @@ EncodeTiledFn encode_tiled_fn() {
 struct DevState {
   bool attrs = false;
   int pair_clusters = 0;   // co-resident CTA pairs (0 = not queried / none)
+  int wide_clusters = 0;   // the same for the wide kernel
 };
 
 int device_setup(int device, DevState** out) {
@@ -683,6 +848,10 @@ int device_setup(int device, DevState** out) {
                                          Cfg<true>::SMEM),
                     "cudaFuncSetAttribute(gemm pair smem)");
     if (rc) return rc;
+    rc = cuda_check(cudaFuncSetAttribute(gemm_tcgen05_kernel<true, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true, true>::SMEM),
+                    "cudaFuncSetAttribute(gemm wide smem)");
+    if (rc) return rc;
     // How many CTA pairs can be resident at once (one CTA per SM).
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -691,7 +860,7 @@ int device_setup(int device, DevState** out) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * 512, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(Cfg<true>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg<true>::SMEM;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -701,6 +870,14 @@ int device_setup(int device, DevState** out) {
       n = 0;
     }
     s.pair_clusters = n;
+    cfg.blockDim = dim3(Cfg<true, true>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<true, true>::SMEM;
+    n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<true, true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    s.wide_clusters = n;
     s.attrs = true;
   }
   *out = &s;
@@ -712,6 +889,16 @@ bool pair_allowed() {
   static int v = -1;
   if (v < 0) {
     const char* e = std::getenv("TTL_GEMM_CTA_PAIR");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
+// TTL_GEMM_WIDE=0 keeps every launch on the 256-column tiles (for comparisons).
+bool wide_allowed() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("TTL_GEMM_WIDE");
     v = (e && e[0] == '0') ? 0 : 1;
   }
   return v == 1;
@@ -911,12 +1098,25 @@ int GemmBatch::launch(cudaStream_t stream) {
                        p.a_slab_rows);
     if (p.a_slab_rows % 256) pair = false;
   }
+  // The wide kernel (256 x 512 tiles, TMA-store epilogue) takes launches whose problems all
+  // have the plain bf16 epilogue without bias, more than 256 columns and at least 3 k-blocks (its epilogue
+  // borrows the ring slots of the next tile's k-blocks 2 and 3), and whose outputs a tensor
+  // map can address.
+  bool wide = pair && wide_allowed() && ds->wide_clusters > 0 && nmaps_ + p_->nprob <= kMaxMaps;
+  for (int i = 0; wide && i < p_->nprob; ++i) {
+    const Problem& p = p_->probs[i];
+    int kb = 0;
+    for (int k = 0; k < p.nseg; ++k) kb += p.seg[k].kblocks;
+    wide = p.epi == EPI_BF16 && !p.bias0 && !p.paired && p.N > BN && p.N % 8 == 0 && kb >= 3 && aligned16(p.out0) &&
+           (p.ld_out * 2) % 16 == 0 && p.ld_out >= p.N;
+  }
   const int tile_m = pair ? Cfg<true>::TILE_M : Cfg<false>::TILE_M;
+  const int tile_n = wide ? Cfg<true, true>::TILE_N : BN;
   int total = 0;
   p_->ngroups = 0;
   for (int i = 0; i < p_->nprob; ++i) {
     Problem& p = p_->probs[i];
-    const int tn = p.paired ? BN / 2 : BN;
+    const int tn = p.paired ? BN / 2 : tile_n;
     p.tiles_m = (p.M + tile_m - 1) / tile_m;
     p.tiles_n = (p.N + tn - 1) / tn;
     p.half_n = !p.paired && p.N <= BN / 2;
@@ -935,6 +1135,14 @@ int GemmBatch::launch(cudaStream_t stream) {
     total += p.tiles_m * p.tiles_n;
   }
   p_->total_tiles = total;
+  if (wide) {
+    for (int i = 0; i < p_->nprob; ++i) {
+      Problem& p = p_->probs[i];
+      // 32-row x 64-column boxes, the staging layout of the wide epilogue.
+      if ((rc = encode_map_bf16(&p_->maps[nmaps_], p.out0, p.M, p.N, p.ld_out, 64, 32))) return rc;
+      p.omap = static_cast<uint8_t>(nmaps_++);
+    }
+  }
   p_->nmaps = nmaps_;
   if (total == 0) return TTL_OK;
   p_->status = device_status_ptr();
@@ -943,10 +1151,11 @@ int GemmBatch::launch(cudaStream_t stream) {
   TraceScope trace(stream, TTL_K_GEMM, flops_, bytes_);
   if (!pair) {
     const int grid = total < num_sms() ? total : num_sms();
-    gemm_tcgen05_kernel<false><<<grid, NUM_THREADS, Cfg<false>::SMEM, stream>>>(*p_);
+    gemm_tcgen05_kernel<false><<<grid, Cfg<false>::THREADS, Cfg<false>::SMEM, stream>>>(*p_);
     return cuda_check(cudaGetLastError(), "gemm_tcgen05_kernel launch");
   }
-  const int pairs = total < ds->pair_clusters ? total : ds->pair_clusters;
+  const int max_pairs = wide ? ds->wide_clusters : ds->pair_clusters;
+  const int pairs = total < max_pairs ? total : max_pairs;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -954,11 +1163,13 @@ int GemmBatch::launch(cudaStream_t stream) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<true>::SMEM;
+  cfg.blockDim = dim3(wide ? Cfg<true, true>::THREADS : Cfg<true>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = wide ? Cfg<true, true>::SMEM : Cfg<true>::SMEM;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (wide)
+    return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<true, true>, *p_), "gemm_tcgen05_kernel<wide> launch");
   return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<true>, *p_), "gemm_tcgen05_kernel<pair> launch");
 }
 

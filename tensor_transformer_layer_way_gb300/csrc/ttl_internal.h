@@ -91,7 +91,7 @@ struct Problem {
   uint8_t epi, nseg;
   uint8_t paired;
   uint8_t join;           // 1 = same tile group as the previous problem (shares its A rows)
-  uint8_t pad0;
+  uint8_t omap;           // set by launch() for the wide kernel: the map of out0 its TMA stores use
   uint8_t half_n;         // set by launch() when N <= 128 (unpaired): the MMAs are 128 columns wide
   Seg seg[kMaxSegs];
   void* out0;

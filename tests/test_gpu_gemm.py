@@ -6,6 +6,7 @@ import torch
 import synth_inputs as si
 import tensor_transformer_layer_way_gb300 as ttl
 from oracle import tp_mlp
+from oracle.numerics import round_to_bf16
 from parity import assert_gemm_close, f64
 
 pytestmark = pytest.mark.gpu
@@ -70,3 +71,17 @@ def test_gemm_deterministic():
     ttl.gemm(Ad, Bd, D1, b_kmajor=False)
     ttl.gemm(Ad, Bd, D2, b_kmajor=False)
     assert torch.equal(D1, D2)
+
+
+@pytest.mark.parametrize("a_kmajor,b_kmajor", [(True, True), (True, False), (False, True), (False, False)])
+@pytest.mark.parametrize("M,N,K", [(520, 776, 1000), (256, 512, 4096), (296, 1032, 192), (1024, 264, 512)])
+def test_gemm_integer_inputs_bf16_output_exact(M, N, K, a_kmajor, b_kmajor):
+    """bf16 outputs (the 256 x 512 tiles with the TMA-store epilogue take these launches when
+    N > 256) of small-integer products: every fp32 sum is exact, so D must equal the exact
+    product rounded once to bf16, element for element, ragged rows and columns included."""
+    A, B, Ad, Bd = _operands(M, N, K, a_kmajor, b_kmajor, True, 3 * M + N + K)
+    D = torch.full((M, N), float("nan"), device="cuda", dtype=torch.bfloat16)
+    ttl.gemm(Ad, Bd, D, a_kmajor=a_kmajor, b_kmajor=b_kmajor)
+    assert ttl.device_status() == 0
+    ref = tp_mlp.column_parallel_forward(f64(A), [f64(B)])[0]
+    np.testing.assert_array_equal(f64(D), round_to_bf16(ref).astype(np.float64))
