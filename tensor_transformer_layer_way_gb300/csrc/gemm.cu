@@ -61,6 +61,7 @@ struct Cfg {
   static_assert(!WIDE || PAIR, "the wide tile is a CTA-pair tile");
   static constexpr int TILE_M = PAIR ? 256 : 128;     // rows per tile (both CTAs of a pair)
   static constexpr int TILE_N = WIDE ? 2 * BN : BN;   // output columns per (unpaired) tile
+  static constexpr int TILE_NP = WIDE ? BN : BN / 2;  // output columns per paired tile
   static constexpr int B_COLS = WIDE ? 256 : PAIR ? 128 : 256;   // B columns held by one CTA
   static constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
   static constexpr int B_BYTES = B_COLS * BK * 2;     // 16 or 32 KiB
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
           const CUtensorMap* mb0 = &P.maps[sg.map_b];
           const CUtensorMap* mb1 = pr.paired ? &P.maps[sg.map_b2] : mb0;
           const int bnb = pr.b_n0 + sg.b_n1;
-          const int bn0 = pr.paired ? bnb + c.tn * (BN / 2) : bnb + c.tn * C::TILE_N;
+          const int bn0 = pr.paired ? bnb + c.tn * C::TILE_NP : bnb + c.tn * C::TILE_N;
           // The second half of the B columns: a pair's second CTA supplies columns
           // [N/2, N) of the MMA (64 of a 128-column one); paired tiles share coordinates.
           const int bn1 = pr.paired ? bn0 : bn0 + (pr.half_n ? BN / 4 : BN / 2);
@@ -510,17 +511,19 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
                 tma_load_2d_pair(sa + 8192, ma, fb, am + 64, ka);
               }
               if (WIDE) {
-                // This CTA's 128 columns of each 256-column half: [r 128, r 128 + 128) of the
-                // first half, the same of the second half 16 KiB further on.
+                // This CTA's 128 columns of each 256-column accumulator half: [r 128, r 128 + 128)
+                // of the first half, then the same of the second half 16 KiB further on (a paired
+                // tile: the same columns of map_b2).
                 const int bw = bn0 + static_cast<int>(rank) * (BN / 2);
+                const int bw2 = pr.paired ? bw : bw + BN;
                 if (!pr.b_mn) {
                   tma_load_2d_pair(sb, mb0, fb, kbb, bw);
-                  tma_load_2d_pair(sb + 16384, mb0, fb, kbb, bw + BN);
+                  tma_load_2d_pair(sb + 16384, mb1, fb, kbb, bw2);
                 } else {
                   tma_load_2d_pair(sb, mb0, fb, bw, kbb);
                   tma_load_2d_pair(sb + 8192, mb0, fb, bw + 64, kbb);
-                  tma_load_2d_pair(sb + 16384, mb0, fb, bw + BN, kbb);
-                  tma_load_2d_pair(sb + 24576, mb0, fb, bw + BN + 64, kbb);
+                  tma_load_2d_pair(sb + 16384, mb1, fb, bw2, kbb);
+                  tma_load_2d_pair(sb + 24576, mb1, fb, bw2 + 64, kbb);
                 }
               } else {
                 const CUtensorMap* mb = rank ? mb1 : mb0;
@@ -690,13 +693,99 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
       tc_fence_after_sync();
       uint8_t* const slot_a = smem + static_cast<int>((kb_end + 2) % C::STAGES) * C::STAGE;
       uint8_t* const slot_b = smem + static_cast<int>((kb_end + 3) % C::STAGES) * C::STAGE;
-      const int col0 = c.tn * C::TILE_N + h2 * BN;   // output column of this warp's first box
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h2 * BN);
       // Staging box j of this warp: boxes 0..11 in slot_a, 12..23 in slot_b, 24..31 in the own region.
       auto box = [&](int j) -> uint8_t* {
         const int b = 4 * ew + j;
         return b < 12 ? slot_a + b * STG_BOX : b < 24 ? slot_b + (b - 12) * STG_BOX : smem + C::STG_OFF + (b - 24) * STG_BOX;
       };
+      const int y = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + q * 32;   // first row of this warp
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      if (pr.paired) {
+        // SwiGLU forward: accumulator columns [0, 256) hold G and [256, 512) hold V of the tile's
+        // 256 output columns; this warp takes output columns [h2 128, h2 128 + 128).  G and V go
+        // to boxes 0, 1 and 2, 3; H = SiLU(G) V (from the fp32 values) waits in registers and
+        // takes G's boxes once their stores have read them.
+        const int col0 = c.tn * C::TILE_NP + h2 * 128;
+        uint32_t hq[64];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub) {
+            uint32_t g[32], u[32];
+            __syncwarp();
+            const uint32_t cg = tq + static_cast<uint32_t>(h2 * 128 + j * 64 + sub * 32);
+            tmem_ld_32x32b_x32(cg, g);
+            tmem_ld_32x32b_x32(cg + BN, u);
+            tmem_ld_wait();
+            uint8_t* rg = box(j) + lane * 128;
+            uint8_t* rv = box(2 + j) + lane * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float gv[8], uv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                gv[e] = __uint_as_float(g[8 * k + e]);
+                uv[e] = __uint_as_float(u[8 * k + e]);
+              }
+              const int pos = ((sub * 4 + k) ^ (lane & 7)) << 4;
+              *reinterpret_cast<uint4*>(rg + pos) = make_uint4(pack_bf16x2(gv[0], gv[1]), pack_bf16x2(gv[2], gv[3]),
+                                                               pack_bf16x2(gv[4], gv[5]), pack_bf16x2(gv[6], gv[7]));
+              *reinterpret_cast<uint4*>(rv + pos) = make_uint4(pack_bf16x2(uv[0], uv[1]), pack_bf16x2(uv[2], uv[3]),
+                                                               pack_bf16x2(uv[4], uv[5]), pack_bf16x2(uv[6], uv[7]));
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                hq[j * 32 + sub * 16 + k * 4 + e] =
+                    pack_bf16x2(gv[2 * e] * sigmoid_f(gv[2 * e]) * uv[2 * e],
+                                gv[2 * e + 1] * sigmoid_f(gv[2 * e + 1]) * uv[2 * e + 1]);
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (y < pr.M) {
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j) {
+              if (col0 + j * 64 >= pr.N) break;
+              tma_store_2d(&P.maps[pr.omap], box(j), col0 + j * 64, y);
+              tma_store_2d(&P.maps[pr.omap + 1], box(2 + j), col0 + j * 64, y);
+            }
+          }
+          bulk_commit_group();
+          bulk_wait_group_read<0>();
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint8_t* rowp = box(j) + lane * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(rowp + ((k ^ (lane & 7)) << 4)) =
+                make_uint4(hq[j * 32 + 4 * k], hq[j * 32 + 4 * k + 1], hq[j * 32 + 4 * k + 2], hq[j * 32 + 4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (y < pr.M) {
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j) {
+              if (col0 + j * 64 >= pr.N) break;
+              tma_store_2d(&P.maps[pr.omap + 2], box(j), col0 + j * 64, y);
+            }
+          }
+          bulk_commit_group();
+          bulk_wait_group_read<0>();   // the boxes may be overwritten: hand the borrowed slots back
+          mbar_arrive(stg_bar);
+        }
+        __syncwarp();
+        acc_phase ^= 1u;
+        continue;
+      }
+      const int col0 = c.tn * C::TILE_N + h2 * BN;   // output column of this warp's first box
+      const uint32_t tb = tq + static_cast<uint32_t>(h2 * BN);
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t r0[32], r1[32];
@@ -728,7 +817,6 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        const int y = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + q * 32;
         if (y < pr.M) {
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
@@ -1102,12 +1190,16 @@ int GemmBatch::launch(cudaStream_t stream) {
   // have the plain bf16 epilogue without bias, more than 256 columns and at least 3 k-blocks (its epilogue
   // borrows the ring slots of the next tile's k-blocks 2 and 3), and whose outputs a tensor
   // map can address.
-  bool wide = pair && wide_allowed() && ds->wide_clusters > 0 && nmaps_ + p_->nprob <= kMaxMaps;
+  int out_maps = 0;   // the wide epilogue's output tensor maps: one per problem, three for SwiGLU
+  for (int i = 0; i < p_->nprob; ++i) out_maps += p_->probs[i].paired ? 3 : 1;
+  bool wide = pair && wide_allowed() && ds->wide_clusters > 0 && nmaps_ + out_maps <= kMaxMaps;
   for (int i = 0; wide && i < p_->nprob; ++i) {
     const Problem& p = p_->probs[i];
     int kb = 0;
     for (int k = 0; k < p.nseg; ++k) kb += p.seg[k].kblocks;
-    wide = p.epi == EPI_BF16 && !p.bias0 && !p.paired && p.N > BN && p.N % 8 == 0 && kb >= 3 && aligned16(p.out0) &&
+    const bool plain = p.epi == EPI_BF16 && !p.paired && p.N > BN;
+    const bool swiglu = p.epi == EPI_SWIGLU_FWD && p.paired && p.N > BN / 2 && aligned16(p.out1) && aligned16(p.out2);
+    wide = (plain || swiglu) && !p.bias0 && p.N % 8 == 0 && kb >= 3 && aligned16(p.out0) &&
            (p.ld_out * 2) % 16 == 0 && p.ld_out >= p.N;
   }
   const int tile_m = pair ? Cfg<true>::TILE_M : Cfg<false>::TILE_M;
@@ -1116,7 +1208,7 @@ int GemmBatch::launch(cudaStream_t stream) {
   p_->ngroups = 0;
   for (int i = 0; i < p_->nprob; ++i) {
     Problem& p = p_->probs[i];
-    const int tn = p.paired ? BN / 2 : tile_n;
+    const int tn = p.paired ? (wide ? Cfg<true, true>::TILE_NP : BN / 2) : tile_n;
     p.tiles_m = (p.M + tile_m - 1) / tile_m;
     p.tiles_n = (p.N + tn - 1) / tn;
     p.half_n = !p.paired && p.N <= BN / 2;
@@ -1138,9 +1230,12 @@ int GemmBatch::launch(cudaStream_t stream) {
   if (wide) {
     for (int i = 0; i < p_->nprob; ++i) {
       Problem& p = p_->probs[i];
-      // 32-row x 64-column boxes, the staging layout of the wide epilogue.
-      if ((rc = encode_map_bf16(&p_->maps[nmaps_], p.out0, p.M, p.N, p.ld_out, 64, 32))) return rc;
-      p.omap = static_cast<uint8_t>(nmaps_++);
+      // 32-row x 64-column boxes, the staging layout of the wide epilogue; a SwiGLU tile writes
+      // G, V and H through three consecutive maps.
+      p.omap = static_cast<uint8_t>(nmaps_);
+      void* const outs[3] = {p.out0, p.out1, p.out2};
+      for (int k = 0; k < (p.paired ? 3 : 1); ++k)
+        if ((rc = encode_map_bf16(&p_->maps[nmaps_++], outs[k], p.M, p.N, p.ld_out, 64, 32))) return rc;
     }
   }
   p_->nmaps = nmaps_;
