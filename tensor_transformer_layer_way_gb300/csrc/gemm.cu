@@ -353,8 +353,8 @@ __device__ __forceinline__ void epilogue_tile(const Problem& pr, uint32_t tbase,
   }
   // One (max, sum) partial per row and half tile (BN / 2 columns): index 2 tile + half.
   if (epi == EPI_F32_CE && row_ok) {
-    const int64_t gt = pr.tn0 + n_base / BN;   // this tile's index among the group's n-tiles
-    reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + 2 * gt + half] = make_float2(st.m, st.s);
+    const int64_t chunk = pr.cbase + 2 * (n_base / BN) + half;   // 128-column chunk of this half tile
+    reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + chunk] = make_float2(st.m, st.s);
   }
 }
 
@@ -786,6 +786,99 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
       }
       const int col0 = c.tn * C::TILE_N + h2 * BN;   // output column of this warp's first box
       const uint32_t tb = tq + static_cast<uint32_t>(h2 * BN);
+      if (pr.epi == EPI_F32 || pr.epi == EPI_F32_CE) {
+        // fp32: 256 columns are 8 boxes of 32 rows x 32 columns, staged in two rounds of 128
+        // columns through this warp's four boxes; round 1 reuses them once round 0's stores
+        // have read them, and TMEM is released after round 1's last read.  The cross-entropy
+        // variant folds each round's 128 columns into one (max, sum exp) partial per row.
+        const bool ce = pr.epi == EPI_F32_CE;
+        const int row = y + lane;
+        const bool row_ok = row < pr.M;
+        const int64_t tgt = (ce && row_ok) ? reinterpret_cast<const int64_t*>(pr.aux0)[row] - pr.ext0 : -1;
+        const int nchunks = 2 * ((pr.N + BN - 1) / BN);   // partials this problem owns per row
+#pragma unroll 1
+        for (int r = 0; r < 2; ++r) {
+          float m = -INFINITY, sum = 0.0f;
+#pragma unroll 1
+          for (int sub = 0; sub < 2; ++sub) {
+            uint32_t r0[32], r1[32];
+            __syncwarp();
+            tmem_ld_32x32b_x32(tb + r * 128 + sub * 64, r0);
+            tmem_ld_32x32b_x32(tb + r * 128 + sub * 64 + 32, r1);
+            tmem_ld_wait();
+            if (r == 1 && sub == 1) {
+              // The last TMEM read of this warp: the MMA may start the next tile.
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+            }
+            if (r == 1 && sub == 0) {   // round 0's boxes must have been read by their stores
+              if (lane == 0) bulk_wait_group_read<0>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t* w = hh ? r1 : r0;
+              const int colc = col0 + r * 128 + sub * 64 + hh * 32;   // problem column of w[0]
+              if (ce) {
+                const int nv = min(32, pr.N - colc);
+                if (nv > 0) {
+                  float mx = -INFINITY;
+#pragma unroll
+                  for (int e = 0; e < 32; ++e)
+                    if (e < nv) mx = fmaxf(mx, __uint_as_float(w[e]));
+                  if (mx > m) {
+                    sum *= __expf(m - mx);
+                    m = mx;
+                  }
+                  float se = 0.0f;
+#pragma unroll
+                  for (int e = 0; e < 32; ++e)
+                    if (e < nv) se += __expf(__uint_as_float(w[e]) - m);
+                  sum += se;
+                  if (tgt >= colc && tgt < colc + nv) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                      if (tgt == colc + e) reinterpret_cast<float*>(pr.out2)[row] = __uint_as_float(w[e]);
+                  }
+                }
+              }
+              uint8_t* rowp = box(2 * sub + hh) + lane * 128;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4*>(rowp + ((k ^ (lane & 7)) << 4)) =
+                    make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            }
+          }
+          if (ce && row_ok) {
+            const int chunk = 4 * c.tn + 2 * h2 + r;   // 128-column chunk of the problem
+            if (chunk < nchunks)
+              reinterpret_cast<float2*>(pr.out1)[static_cast<int64_t>(row) * pr.ext1 + pr.cbase + chunk] =
+                  make_float2(m, sum);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (y < pr.M) {
+#pragma unroll 1
+              for (int b = 0; b < 4; ++b) {
+                const int x = col0 + r * 128 + b * 32;
+                if (x >= pr.N) break;
+                tma_store_2d(&P.maps[pr.omap], box(b), x, y);
+              }
+            }
+            bulk_commit_group();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          bulk_wait_group_read<0>();   // the boxes may be overwritten: hand the borrowed slots back
+          mbar_arrive(stg_bar);
+        }
+        __syncwarp();
+        acc_phase ^= 1u;
+        continue;
+      }
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t r0[32], r1[32];
@@ -1011,6 +1104,23 @@ int encode_map_bf16(CUtensorMap* out, const void* ptr, int64_t rows, int64_t col
                   "cuTensorMapEncodeTiled");
 }
 
+int encode_map_f32(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                   int box_rows) {
+  if (!aligned16(ptr) || (ld * 4) % 16 != 0 || cols % 4 != 0 || rows <= 0 || cols <= 0)
+    return set_error(TTL_ERR_ALIGN, "tensor map %p: pointer, row stride (%lld) and width (%lld) must be 16-byte aligned",
+                     ptr, (long long)ld, (long long)cols);
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return set_error(TTL_ERR_CUDA, "cuTensorMapEncodeTiled not available from the CUDA driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return cu_check(enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                  "cuTensorMapEncodeTiled(f32)");
+}
+
 int encode_map_bf16_3d(CUtensorMap* out, const void* ptr, int64_t d0, int64_t d1, int64_t d2, int64_t ld1,
                        int64_t ld2, int box0, int box1) {
   if (!aligned16(ptr) || (ld1 * 2) % 16 != 0 || (ld2 * 2) % 16 != 0 || d0 % 8 != 0 || d0 <= 0 || d1 <= 0 || d2 <= 0)
@@ -1187,9 +1297,10 @@ int GemmBatch::launch(cudaStream_t stream) {
     if (p.a_slab_rows % 256) pair = false;
   }
   // The wide kernel (256 x 512 tiles, TMA-store epilogue) takes launches whose problems all
-  // have the plain bf16 epilogue without bias, more than 256 columns and at least 3 k-blocks (its epilogue
-  // borrows the ring slots of the next tile's k-blocks 2 and 3), and whose outputs a tensor
-  // map can address.
+  // have one of its epilogues (plain bf16 without bias, the SwiGLU forward, fp32, fp32 with the
+  // cross-entropy partials), more than 256 columns (SwiGLU: 128) and at least 3 k-blocks (its
+  // epilogue borrows the ring slots of the next tile's k-blocks 2 and 3), and whose outputs a
+  // tensor map can address.
   int out_maps = 0;   // the wide epilogue's output tensor maps: one per problem, three for SwiGLU
   for (int i = 0; i < p_->nprob; ++i) out_maps += p_->probs[i].paired ? 3 : 1;
   bool wide = pair && wide_allowed() && ds->wide_clusters > 0 && nmaps_ + out_maps <= kMaxMaps;
@@ -1197,10 +1308,11 @@ int GemmBatch::launch(cudaStream_t stream) {
     const Problem& p = p_->probs[i];
     int kb = 0;
     for (int k = 0; k < p.nseg; ++k) kb += p.seg[k].kblocks;
-    const bool plain = p.epi == EPI_BF16 && !p.paired && p.N > BN;
-    const bool swiglu = p.epi == EPI_SWIGLU_FWD && p.paired && p.N > BN / 2 && aligned16(p.out1) && aligned16(p.out2);
-    wide = (plain || swiglu) && !p.bias0 && p.N % 8 == 0 && kb >= 3 && aligned16(p.out0) &&
-           (p.ld_out * 2) % 16 == 0 && p.ld_out >= p.N;
+    const bool plain = p.epi == EPI_BF16 && !p.paired && p.N > BN && (p.ld_out * 2) % 16 == 0;
+    const bool swiglu = p.epi == EPI_SWIGLU_FWD && p.paired && p.N > BN / 2 && aligned16(p.out1) &&
+                        aligned16(p.out2) && (p.ld_out * 2) % 16 == 0;
+    const bool f32 = (p.epi == EPI_F32 || p.epi == EPI_F32_CE) && !p.paired && p.N > BN && (p.ld_out * 4) % 16 == 0;
+    wide = (plain || swiglu || f32) && !p.bias0 && p.N % 8 == 0 && kb >= 3 && aligned16(p.out0) && p.ld_out >= p.N;
   }
   const int tile_m = pair ? Cfg<true>::TILE_M : Cfg<false>::TILE_M;
   const int tile_n = wide ? Cfg<true, true>::TILE_N : BN;
@@ -1221,6 +1333,9 @@ int GemmBatch::launch(cudaStream_t stream) {
       g.count = 0;
     }
     TileGroup& g = p_->groups[p_->ngroups - 1];
+    // Cross-entropy partials: two per 256-column tile of every earlier problem of the group,
+    // whichever tile width the launch uses.
+    p.cbase = g.count == 0 ? 0 : p_->probs[i - 1].cbase + 2 * ((p_->probs[i - 1].N + BN - 1) / BN);
     p.tn0 = g.tiles_n;
     g.tiles_n += p.tiles_n;
     g.count += 1;
@@ -1230,9 +1345,13 @@ int GemmBatch::launch(cudaStream_t stream) {
   if (wide) {
     for (int i = 0; i < p_->nprob; ++i) {
       Problem& p = p_->probs[i];
-      // 32-row x 64-column boxes, the staging layout of the wide epilogue; a SwiGLU tile writes
-      // G, V and H through three consecutive maps.
+      // 32-row x 128-byte boxes (64 bf16 or 32 fp32 columns), the staging layout of the wide
+      // epilogue; a SwiGLU tile writes G, V and H through three consecutive maps.
       p.omap = static_cast<uint8_t>(nmaps_);
+      if (p.epi == EPI_F32 || p.epi == EPI_F32_CE) {
+        if ((rc = encode_map_f32(&p_->maps[nmaps_++], p.out0, p.M, p.N, p.ld_out, 32, 32))) return rc;
+        continue;
+      }
       void* const outs[3] = {p.out0, p.out1, p.out2};
       for (int k = 0; k < (p.paired ? 3 : 1); ++k)
         if ((rc = encode_map_bf16(&p_->maps[nmaps_++], outs[k], p.M, p.N, p.ld_out, 64, 32))) return rc;

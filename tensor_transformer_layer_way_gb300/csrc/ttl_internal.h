@@ -60,10 +60,11 @@ enum Epilogue : int {
   EPI_SWIGLU_FWD = 3,  // paired tile: out0 = G, out1 = V, out2 = SiLU(G) * V
   EPI_GELU_BWD = 4,    // out0 = bf16(acc * GeLU'(aux0))                          (dU)
   EPI_SWIGLU_BWD = 5,  // out0 = bf16(acc * aux1 * SiLU'(aux0)), out1 = bf16(acc * SiLU(aux0))
-  EPI_F32_CE = 6,      // out0 = acc (fp32 logits) and, per row and half tile (BN / 2 columns),
-                       // the cross-entropy partials: out1[row * ext1 + 2 (tn0 + tn) + half] =
-                       // (max, sum exp(z - max)) over those columns; out2[row] = the logit at
-                       // target aux0[row] - ext0 when that column is in the tile
+  EPI_F32_CE = 6,      // out0 = acc (fp32 logits) and, per row and 128-column chunk c of the
+                       // problem, the cross-entropy partials: out1[row * ext1 + cbase + c] =
+                       // (max, sum exp(z - max)) over the chunk's columns (chunks counted 2 per
+                       // 256-column tile, so every chunk below 2 ceil(N / 256) is written);
+                       // out2[row] = the logit at target aux0[row] - ext0 when that column exists
   EPI_PAIR_BF16 = 7,   // paired tile: out0 = bf16(accumulator columns [0,128)) from map_b,
                        // out1 = bf16(columns [128,256)) from map_b2 (two narrow products as one
                        // full-width MMA, e.g. the K and V projections of a shard)
@@ -84,6 +85,7 @@ struct Problem {
   int32_t M, N;
   int32_t tiles_m, tiles_n;
   int32_t tn0;            // first n-tile of this problem within its group's n-tile range
+  int32_t cbase;          // EPI_F32_CE: first partial of this problem in a row of out1 (set by launch())
   int32_t a_m0, b_n0;     // offsets added to the M coordinate of A and N coordinate of B
   int32_t a_slab_rows;    // > 0: A's rows live in consecutive maps seg.map_a + r, r = row / a_slab_rows
                           // (token slabs, e.g. an all-gather folded into the operand loads)
@@ -176,6 +178,10 @@ class GemmBatch {
 // with a box of box_cols x box_rows elements and 128-byte swizzle.  TTL_OK or an error code.
 int encode_map_bf16(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
                     int box_rows);
+
+// The same for an fp32 matrix (row stride ld elements, a multiple of 4).
+int encode_map_f32(CUtensorMap* out, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                   int box_rows);
 
 // The same for a 3-D bf16 tensor [d2][d1][d0] (d0 contiguous; ld1, ld2 the strides of dims 1
 // and 2 in elements) with a box of box0 x box1 x 1.
