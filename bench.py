@@ -484,23 +484,28 @@ def bench_gtp(ttl, torch, dev, pk, args):
     from tensor_transformer_layer_way_gb300 import chain
     runner = chain.GtpChain(ttl, torch, shards, slots)
 
-    def fwd_bwd(folded=False, fin_stream=True):
+    def fwd_bwd(folded=False, fin_stream=True, wg_stream=True):
         runner.forward(X, Y, folded=folded)
-        runner.backward(X, dY, dX, staging, main_grad, folded=folded, finalize_stream=fin_stream)
+        runner.backward(X, dY, dX, staging, main_grad, folded=folded, finalize_stream=fin_stream,
+                        wgrad_stream=wg_stream)
 
     runner.forward(X, Y, cold=True)           # cold start: every first gather synchronous
     for _ in range(2):
         fwd_bwd()
     torch.cuda.synchronize()
     res = {"workload": "gtp_chain_L8_h8192_tp4_g8_T4096", "gemm_flops_per_pass": 3 * L * 2.0 * M * K * N}
-    for key, folded, fin in (("slot_prefetch", False, True), ("folded", True, True),
-                             ("slot_prefetch_finalize_on_compute_stream", False, False)):
+    # slot_prefetch: the chain's defaults (finalizes and weight gradients on streams of their
+    # own); the last variant keeps every launch on the compute stream, so its GEMM launches
+    # run undisturbed and their CUDA-event durations give the kernel's own rate.
+    for key, folded, fin, wgs in (("slot_prefetch", False, True, True), ("folded", True, True, True),
+                                  ("slot_prefetch_wgrad_on_compute_stream", False, True, False),
+                                  ("slot_prefetch_all_on_compute_stream", False, False, False)):
         ttl.trace_enable(True, 1 << 14)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         reps = 3
         e0.record()
         for _ in range(reps):
-            fwd_bwd(folded, fin)
+            fwd_bwd(folded, fin, wgs)
         e1.record()
         torch.cuda.synchronize()
         wall = e0.elapsed_time(e1) / reps
@@ -516,6 +521,9 @@ def bench_gtp(ttl, torch, dev, pk, args):
                     # everything the chain's wall time spends outside the GEMMs: exposed gathers,
                     # finalize work that is not hidden, launch gaps
                     "exposed_ms": round(wall - gemm_ms, 3),
+                    # every GEMM FLOP of the pass over the wall time (with GEMMs on two streams
+                    # their launch durations overlap, so only this rate is comparable)
+                    "chain_tflops": round(res["gemm_flops_per_pass"] / (wall * 1e-3) / 1e12, 1),
                     "finalize_ms": round(sum(r[1] for r in fi) / reps, 3),
                     "finalize_gbs": round(sum(r[3] for r in fi) / (sum(r[1] for r in fi) * 1e-3) / 1e9, 1) if fi else None}
         if ga:
@@ -557,8 +565,12 @@ def bench_gtp(ttl, torch, dev, pk, args):
                               "torch_copy_same_bytes_gbs": round(gather_bytes / (cms * 1e-3) / 1e9, 1),
                               "bytes": gather_bytes, "l2": "flushed before each repetition of the 8 launches"}
     del flush, dst, src
-    res["roofline"] = pending("tensor", "gemm_tcgen05_kernel", res["slot_prefetch"]["gemm_tflops"],
-                              path="slot_prefetch chain (gathered slot, side-stream prefetch)")
+    res["roofline"] = pending("tensor", "gemm_tcgen05_kernel", res["slot_prefetch_all_on_compute_stream"]["gemm_tflops"],
+                              path="GEMM launches of the slot_prefetch chain with every launch on the compute "
+                                   "stream (the default chain overlaps them, see chain_roofline)")
+    res["chain_roofline"] = pending("tensor", "whole chain (all GEMM FLOPs over the fwd+bwd wall time)",
+                                    res["slot_prefetch"]["chain_tflops"],
+                                    path="slot_prefetch chain, finalizes and weight gradients on their own streams")
     del X, shards, dY, Y, dX, slots, staging, main_grad, runner
     torch.cuda.empty_cache()
     return res

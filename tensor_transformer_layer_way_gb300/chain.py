@@ -24,6 +24,7 @@ class GtpChain:
         self.L = len(shards)
         self.side = torch.cuda.Stream()
         self.fin = torch.cuda.Stream()                         # deferred finalizes
+        self.wg = torch.cuda.Stream()                          # weight gradients beside the dgrads
         self.ready = [torch.cuda.Event() for _ in range(2)]
         self.free = [torch.cuda.Event() for _ in range(2)]
         self.wgrad_done = [torch.cuda.Event() for _ in range(self.L)]
@@ -58,7 +59,7 @@ class GtpChain:
             ttl.gtp_gather_gemm(X, self.shards[l], Y[l], slot=self.slots[l % 2])
             self.free[l % 2].record(main)
 
-    def backward(self, X, dY, dX, staging, main_grad, *, folded=False, finalize_stream=True):
+    def backward(self, X, dY, dX, staging, main_grad, *, folded=False, finalize_stream=True, wgrad_stream=True):
         """Reverse chain: dX = dY[l] W_l^T with the gather of layer l-1 beside it; the wgrad of
         layer l is reduce-scattered into staging[l] and finalized into main_grad[l] one backward
         layer later (layer 0 at once).  ``dX`` may be one buffer or a list per layer.
@@ -67,12 +68,20 @@ class GtpChain:
         backward step l on a stream of its own (after the event recorded behind layer l+1's
         weight gradient), so it runs beside step l's GEMMs instead of between them; the
         compute stream joins it before returning.  Otherwise it runs on the compute stream,
-        inside the weight-gradient call of step l."""
+        inside the weight-gradient call of step l.
+
+        With ``wgrad_stream`` (and ``finalize_stream``) the weight gradients run on a stream of
+        their own: they depend only on X and dY, so layer l's weight gradient can fill the SMs
+        that layer l-1's dgrad leaves idle in its last wave; the compute stream joins that
+        stream before returning."""
         ttl = self.ttl
         main = self.torch.cuda.current_stream()
         L = self.L
         if finalize_stream:
             self.fin.wait_stream(main)
+        wgs = wgrad_stream and finalize_stream
+        if wgs:
+            self.wg.wait_stream(main)                           # X and every dY[l] are ready
         if not folded:
             self.side.wait_stream(main)
             self._gather_async(L - 1, wait_free=False)          # head of the reverse chain
@@ -91,10 +100,14 @@ class GtpChain:
                 ttl.gtp_gather_gemm(dY[l], self.shards[l], out, slot=self.slots[l % 2], transpose_w=True)
                 self.free[l % 2].record(main)
             in_stream = prev is not None and not finalize_stream
+            ws = self.wg if wgs else main
             ttl.gtp_wgrad_rs_finalize(X, dY[l], staging[l],
                                       staging_prev=staging[prev] if in_stream else None,
                                       main_grad_prev=main_grad[prev] if in_stream else None,
-                                      sync=(l == 0), main_grad_cur=main_grad[0] if l == 0 else None)
-            self.wgrad_done[l].record(main)
+                                      sync=(l == 0), main_grad_cur=main_grad[0] if l == 0 else None,
+                                      stream=ws)
+            self.wgrad_done[l].record(ws)
+        if wgs:
+            main.wait_stream(self.wg)
         if finalize_stream:
             main.wait_stream(self.fin)

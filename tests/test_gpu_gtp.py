@@ -190,8 +190,9 @@ def test_trace_records_launches():
 
 def test_finalize_is_one_fp32_add_and_the_finalize_stream_changes_no_bit():
     """Each main_grad element after the chain is exactly initial + staging in fp32 (one IEEE
-    addition), and the chain with its deferred finalizes on a stream of their own gives the
-    same bits as with every finalize on the compute stream."""
+    addition), and the chain with its deferred finalizes on a stream of their own, or with its
+    weight gradients on a stream of their own too, gives the same bits as with everything on
+    the compute stream."""
     from tensor_transformer_layer_way_gb300 import chain
     L, g, M, K, N = 3, 4, 256, 512, 320
     inp = si.gtp_inputs(L, K, N, M, seed=23)
@@ -201,18 +202,20 @@ def test_finalize_is_one_fp32_add_and_the_finalize_stream_changes_no_bit():
     slots = [torch.empty((K, N), device="cuda", dtype=torch.bfloat16) for _ in range(2)]
     mg0 = [[torch.randn((K // g, N), generator=si.generator(200 + l * g + j)) for j in range(g)] for l in range(L)]
 
-    def run(fin):
+    def run(fin, wgs=False):
         runner = chain.GtpChain(ttl, torch, shards, slots)
         mg = [[m.cuda() for m in layer] for layer in mg0]
         staging = [[torch.empty((K // g, N), device="cuda") for _ in range(g)] for _ in range(L)]
         dX = torch.empty((M, K), device="cuda", dtype=torch.bfloat16)
-        runner.backward(X, dYs, dX, staging, mg, finalize_stream=fin)
+        runner.backward(X, dYs, dX, staging, mg, finalize_stream=fin, wgrad_stream=wgs)
         torch.cuda.synchronize()
         assert ttl.device_status() == 0
-        return mg, staging
+        return mg, staging, dX
 
-    mg_a, st_a = run(True)
-    mg_b, st_b = run(False)
+    mg_a, st_a, dx_a = run(True)
+    mg_b, st_b, dx_b = run(False)
+    mg_c, st_c, dx_c = run(True, True)
+    assert torch.equal(dx_a, dx_b) and torch.equal(dx_a, dx_c)
     for l in range(L):
         for j in range(g):
             expect = (mg0[l][j].numpy() + f32(st_a[l][j])).astype(np.float32)
@@ -220,5 +223,6 @@ def test_finalize_is_one_fp32_add_and_the_finalize_stream_changes_no_bit():
                                           err_msg=f"main_grad[{l}][{j}]")
             assert torch.equal(st_a[l][j], st_b[l][j])
             assert torch.equal(mg_a[l][j], mg_b[l][j]), f"finalize stream: main_grad[{l}][{j}]"
+            assert torch.equal(st_a[l][j], st_c[l][j]) and torch.equal(mg_a[l][j], mg_c[l][j]), f"wgrad stream [{l}][{j}]"
     with pytest.raises(ttl.TTLError):
         ttl.gtp_finalize(st_a[0], st_a[0])       # staging and main_grad alias
