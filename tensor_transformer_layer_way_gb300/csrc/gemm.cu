@@ -691,6 +691,14 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
       const bool ready = mbar_wait(&tfull_bar[0], acc_phase, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
+      // Boxes in a warp's own region (warps 6 and 7) are not lent by the producer: the plain
+      // path hands such a warp's share back before its stores have read them, so it waits for
+      // them here, before it writes the boxes again.
+      const bool lent = 4 * ew < 24;
+      if (!lent) {
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+      }
       uint8_t* const slot_a = smem + static_cast<int>((kb_end + 2) % C::STAGES) * C::STAGE;
       uint8_t* const slot_b = smem + static_cast<int>((kb_end + 3) % C::STAGES) * C::STAGE;
       // Staging box j of this warp: boxes 0..11 in slot_a, 12..23 in slot_b, 24..31 in the own region.
@@ -886,6 +894,12 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
         tmem_ld_32x32b_x32(tb + j * 64, r0);
         tmem_ld_32x32b_x32(tb + j * 64 + 32, r1);
         tmem_ld_wait();
+        if (j == 3) {
+          // Every TMEM read of this warp is complete (tcgen05.wait::ld): the MMA may start the next tile.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+        }
         float v[64];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -901,24 +915,14 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
                                      pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
           *reinterpret_cast<uint4*>(rowp + ((k ^ (lane & 7)) << 4)) = w;
         }
+        // Each box is stored as soon as it is written, so the stores run beside the next reads.
+        fence_proxy_async_smem();   // generic-proxy writes before the TMA engine's reads
+        __syncwarp();
+        if (lane == 0 && y < pr.M && col0 + j * 64 < pr.N) tma_store_2d(&P.maps[pr.omap], box(j), col0 + j * 64, y);
       }
-      // Every TMEM read of this warp is complete (tcgen05.wait::ld): the MMA may start the next tile.
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
-      // The generic-proxy staging writes must be visible to the TMA engine's reads.
-      fence_proxy_async_smem();
-      __syncwarp();
       if (lane == 0) {
-        if (y < pr.M) {
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            if (col0 + j * 64 >= pr.N) break;
-            tma_store_2d(&P.maps[pr.omap], box(j), col0 + j * 64, y);
-          }
-        }
         bulk_commit_group();
-        bulk_wait_group_read<0>();   // the boxes may be overwritten: hand the borrowed slots back
+        if (lent) bulk_wait_group_read<0>();   // the boxes may be overwritten: hand the borrowed slots back
         mbar_arrive(stg_bar);
       }
       __syncwarp();
