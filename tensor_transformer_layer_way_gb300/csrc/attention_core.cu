@@ -102,25 +102,29 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void row_stats64(const uint32_t (&r0)[32], const uint32_t (&r1)[32], int nv, float k,
                                             float& m, float& l) {
   if (nv >= 64) {   // below the diagonal: no mask
+    // Three-input max and packed fp32 pairs: the same values and sums as the scalar form
+    // (four running maxima, four partial sums over the same elements), fewer instructions.
     float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      x0 = fmaxf(x0, __uint_as_float(r0[e]));
-      x1 = fmaxf(x1, __uint_as_float(r0[e + 1]));
-      x2 = fmaxf(x2, __uint_as_float(r1[e]));
-      x3 = fmaxf(x3, __uint_as_float(r1[e + 1]));
+    for (int e = 0; e < 32; e += 4) {
+      x0 = fmax3(x0, __uint_as_float(r0[e]), __uint_as_float(r0[e + 2]));
+      x1 = fmax3(x1, __uint_as_float(r0[e + 1]), __uint_as_float(r0[e + 3]));
+      x2 = fmax3(x2, __uint_as_float(r1[e]), __uint_as_float(r1[e + 2]));
+      x3 = fmax3(x3, __uint_as_float(r1[e + 1]), __uint_as_float(r1[e + 3]));
     }
     const float mnew = fmaxf(m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * k);
     const float nm = -mnew;
-    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    const uint64_t k2 = f2_pack(k, k), nm2 = f2_pack(nm, nm);
+    uint64_t s01 = 0, s23 = 0;   // (s0, s1) and (s2, s3), all 0.0f
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      s0 += ex2_approx(fmaf(__uint_as_float(r0[e]), k, nm));
-      s1 += ex2_approx(fmaf(__uint_as_float(r0[e + 1]), k, nm));
-      s2 += ex2_approx(fmaf(__uint_as_float(r1[e]), k, nm));
-      s3 += ex2_approx(fmaf(__uint_as_float(r1[e + 1]), k, nm));
+      const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1])), k2, nm2));
+      const float2 b = f2_unpack(ffma2(f2_pack(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1])), k2, nm2));
+      s01 = fadd2(s01, f2_pack(ex2_approx(a.x), ex2_approx(a.y)));
+      s23 = fadd2(s23, f2_pack(ex2_approx(b.x), ex2_approx(b.y)));
     }
-    l = l * ex2_approx(m - mnew) + ((s0 + s1) + (s2 + s3));
+    const float2 p01 = f2_unpack(s01), p23 = f2_unpack(s23);
+    l = l * ex2_approx(m - mnew) + ((p01.x + p01.y) + (p23.x + p23.y));
     m = mnew;
   } else if (nv > 0) {
     float mx = -INFINITY;
@@ -506,12 +510,13 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_fwd_core_kernel(const __
       const int nv = q - (j * kBKV + half * 64) + 1;
       uint32_t w[32];   // keys 2i, 2i + 1 of this warp's 64 in word i
       if (nv >= 64) {   // below the diagonal: no mask
+        const uint64_t k2 = f2_pack(k, k), nm2 = f2_pack(nm, nm);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const uint32_t a0 = i < 16 ? r0[2 * i] : r1[2 * i - 32];
           const uint32_t a1 = i < 16 ? r0[2 * i + 1] : r1[2 * i - 31];
-          w[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(a0), k, nm)),
-                             ex2_approx(fmaf(__uint_as_float(a1), k, nm)));
+          const float2 x = f2_unpack(ffma2(f2_pack(__uint_as_float(a0), __uint_as_float(a1)), k2, nm2));
+          w[i] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
         }
       } else {
 #pragma unroll
@@ -842,6 +847,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
     const bool row_ok = q < P.T;
     const float Dq = row_ok ? P.D[(static_cast<int64_t>(shard) * P.nql + c) * P.T + q] : 0.0f;
     const float scale = P.scale;
+    const uint64_t nD2 = f2_pack(-Dq, -Dq), scale2 = f2_pack(scale, scale);
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = true;
@@ -871,16 +877,19 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
         uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
         const uint4 pw = *unit;
         const uint32_t pv[4] = {pw.x, pw.y, pw.z, pw.w};
-        float e8[8];
+        // dS = (dP - D) (P scale), two columns per packed fp32 instruction (the same roundings
+        // as the scalar form: dP + (-D) is dP - D exactly).  P is zero above the diagonal.
+        uint32_t o4[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int col = u * 8 + e;
-          const float dp = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
-          const float p = (e & 1) ? bf16_hi(pv[e >> 1]) : bf16_lo(pv[e >> 1]);
-          e8[e] = (dp - Dq) * (p * scale);   // P is zero above the diagonal
+        for (int e = 0; e < 4; ++e) {
+          const int col = u * 8 + 2 * e;
+          const uint64_t dp2 = f2_pack(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]),
+                                       __uint_as_float(col < 32 ? r0[col + 1] : r1[col - 31]));
+          const uint64_t p2 = f2_pack(bf16_lo(pv[e]), bf16_hi(pv[e]));
+          const float2 d2 = f2_unpack(fmul2(fadd2(dp2, nD2), fmul2(p2, scale2)));
+          o4[e] = pack_bf16x2(d2.x, d2.y);
         }
-        *unit = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
-                           pack_bf16x2(e8[6], e8[7]));
+        *unit = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1221,6 +1230,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
       const int q = pair_row(j) + r;
       const int c = pair_head(j);
       const float Dq = q < P.T ? P.D[(static_cast<int64_t>(shard) * P.nql + c) * P.T + q] : 0.0f;
+      const uint64_t nD2 = f2_pack(-Dq, -Dq), scale2 = f2_pack(scale, scale);
       ok = mbar_wait(&dp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -1247,16 +1257,19 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
         uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
         const uint4 pw = *unit;
         const uint32_t pv[4] = {pw.x, pw.y, pw.z, pw.w};
-        float e8[8];
+        // dS = (dP - D) (P scale), two columns per packed fp32 instruction (the same roundings
+        // as the scalar form: dP + (-D) is dP - D exactly).  P is zero above the diagonal.
+        uint32_t o4[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int col = u * 8 + e;
-          const float dp = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
-          const float p = (e & 1) ? bf16_hi(pv[e >> 1]) : bf16_lo(pv[e >> 1]);
-          e8[e] = (dp - Dq) * (p * scale);   // P is zero above the diagonal
+        for (int e = 0; e < 4; ++e) {
+          const int col = u * 8 + 2 * e;
+          const uint64_t dp2 = f2_pack(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]),
+                                       __uint_as_float(col < 32 ? r0[col + 1] : r1[col - 31]));
+          const uint64_t p2 = f2_pack(bf16_lo(pv[e]), bf16_hi(pv[e]));
+          const float2 d2 = f2_unpack(fmul2(fadd2(dp2, nD2), fmul2(p2, scale2)));
+          o4[e] = pack_bf16x2(d2.x, d2.y);
         }
-        *unit = make_uint4(pack_bf16x2(e8[0], e8[1]), pack_bf16x2(e8[2], e8[3]), pack_bf16x2(e8[4], e8[5]),
-                           pack_bf16x2(e8[6], e8[7]));
+        *unit = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
