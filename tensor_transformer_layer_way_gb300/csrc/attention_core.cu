@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
     const bool row_ok = q < P.T;
     const float Dq = row_ok ? P.D[(static_cast<int64_t>(shard) * P.nql + c) * P.T + q] : 0.0f;
     const float scale = P.scale;
-    const uint64_t nD2 = f2_pack(-Dq, -Dq), scale2 = f2_pack(scale, scale);
+    const uint64_t nDs2 = f2_pack(-Dq * scale, -Dq * scale), scale2 = f2_pack(scale, scale);
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = true;
@@ -877,8 +877,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
         uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
         const uint4 pw = *unit;
         const uint32_t pv[4] = {pw.x, pw.y, pw.z, pw.w};
-        // dS = (dP - D) (P scale), two columns per packed fp32 instruction (the same roundings
-        // as the scalar form: dP + (-D) is dP - D exactly).  P is zero above the diagonal.
+        // dS = (dP scale - D scale) P, two columns per packed fp32 instruction (one fma and one
+        // multiply per pair).  P is zero above the diagonal.
         uint32_t o4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -886,7 +886,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
           const uint64_t dp2 = f2_pack(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]),
                                        __uint_as_float(col < 32 ? r0[col + 1] : r1[col - 31]));
           const uint64_t p2 = f2_pack(bf16_lo(pv[e]), bf16_hi(pv[e]));
-          const float2 d2 = f2_unpack(fmul2(fadd2(dp2, nD2), fmul2(p2, scale2)));
+          const float2 d2 = f2_unpack(fmul2(ffma2(dp2, scale2, nDs2), p2));
           o4[e] = pack_bf16x2(d2.x, d2.y);
         }
         *unit = make_uint4(o4[0], o4[1], o4[2], o4[3]);
@@ -1230,7 +1230,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
       const int q = pair_row(j) + r;
       const int c = pair_head(j);
       const float Dq = q < P.T ? P.D[(static_cast<int64_t>(shard) * P.nql + c) * P.T + q] : 0.0f;
-      const uint64_t nD2 = f2_pack(-Dq, -Dq), scale2 = f2_pack(scale, scale);
+      const uint64_t nDs2 = f2_pack(-Dq * scale, -Dq * scale), scale2 = f2_pack(scale, scale);
       ok = mbar_wait(&dp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -1257,8 +1257,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
         uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
         const uint4 pw = *unit;
         const uint32_t pv[4] = {pw.x, pw.y, pw.z, pw.w};
-        // dS = (dP - D) (P scale), two columns per packed fp32 instruction (the same roundings
-        // as the scalar form: dP + (-D) is dP - D exactly).  P is zero above the diagonal.
+        // dS = (dP scale - D scale) P, two columns per packed fp32 instruction (one fma and one
+        // multiply per pair).  P is zero above the diagonal.
         uint32_t o4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -1266,7 +1266,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
           const uint64_t dp2 = f2_pack(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]),
                                        __uint_as_float(col < 32 ? r0[col + 1] : r1[col - 31]));
           const uint64_t p2 = f2_pack(bf16_lo(pv[e]), bf16_hi(pv[e]));
-          const float2 d2 = f2_unpack(fmul2(fadd2(dp2, nD2), fmul2(p2, scale2)));
+          const float2 d2 = f2_unpack(fmul2(ffma2(dp2, scale2, nDs2), p2));
           o4[e] = pack_bf16x2(d2.x, d2.y);
         }
         *unit = make_uint4(o4[0], o4[1], o4[2], o4[3]);
