@@ -163,21 +163,28 @@ extern "C" int ttl_tp_attn_fwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   GemmBatch batch;
 
-  // Column-parallel projections: Q_i = X Wq_i, and K_i, V_i = X Wk_i, X Wv_i as one paired
-  // problem (each 256-column accumulator tile holds 128 columns of K_i and the same 128 of V_i,
-  // so the narrow KV heads run as full-width MMAs), all in one tile group over X.
+  // Column-parallel projections: Q_i = X Wq_i in one launch (one tile group over X; wide tiles
+  // where Q is wider than 256 columns), then K_i, V_i = X Wk_i, X Wv_i as one paired problem
+  // per shard in a second launch (each 256-column accumulator tile holds 128 columns of K_i
+  // and the same 128 of V_i, so the narrow KV heads run as full-width MMAs).  Kept apart, the
+  // paired problems do not hold the Q problems back to the 256-column tiles.
   for (int i = 0; i < t; ++i) {
-    if (!batch.has_room(4, 2) && (rc = batch.flush(st))) return rc;
+    if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
     const int mx = batch.add_map(X, T, h, h, false);
     const int mq = batch.add_map(Wq[i], h, s.qc, s.qc, true);
-    const int mk = batch.add_map(Wk[i], h, s.kc, s.kc, true);
-    const int mv = batch.add_map(Wv[i], h, s.kc, s.kc, true);
     Problem* p = batch.add_problem(T, s.qc, false, true, EPI_BF16, false, true);
     if (batch.error()) return batch.error();
     p->out0 = Q_save[i];
     p->ld_out = s.qc;
     if ((rc = batch.add_seg(p, mx, 0, mq, -1, 0, h))) return rc;
-    p = batch.add_problem(T, s.kc, false, true, EPI_PAIR_BF16, true, true);
+  }
+  if ((rc = batch.flush(st))) return rc;
+  for (int i = 0; i < t; ++i) {
+    if (!batch.has_room(3, 1) && (rc = batch.flush(st))) return rc;
+    const int mx = batch.add_map(X, T, h, h, false);
+    const int mk = batch.add_map(Wk[i], h, s.kc, s.kc, true);
+    const int mv = batch.add_map(Wv[i], h, s.kc, s.kc, true);
+    Problem* p = batch.add_problem(T, s.kc, false, true, EPI_PAIR_BF16, true, true);
     if (batch.error()) return batch.error();
     p->out0 = K_save[i];
     p->out1 = V_save[i];
@@ -334,26 +341,32 @@ extern "C" int ttl_tp_attn_bwd(int t, int64_t T, int64_t h, int n_q, int n_kv, i
       return rc;
   }
 
-  // Column-parallel projections backward: dW{q,k,v}_i = X^T d{Q,K,V}_i (one tile group over
-  // X^T; dWk_i and dWv_i as one paired problem) and the dX partials
-  // dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T (three K segments).
+  // Column-parallel projections backward: dWk_i and dWv_i = X^T dK_i, X^T dV_i as one paired
+  // problem per shard (one launch, a tile group over X^T), then dWq_i = X^T dQ_i (a tile group
+  // over X^T) and the dX partials dQ_i Wq_i^T + dK_i Wk_i^T + dV_i Wv_i^T (three K segments) in
+  // one launch that the paired problems do not hold back to the 256-column tiles.
   for (int i = 0; i < t; ++i) {
-    if (!batch.has_room(4, 2) && (rc = batch.flush(st))) return rc;
+    if (!batch.has_room(3, 1) && (rc = batch.flush(st))) return rc;
     const int mx = batch.add_map(X, T, h, h, true);
-    const int mq = batch.add_map(dQ_of(i), T, s.qc, s.qc, true);
     const int mk = batch.add_map(dK_of(i), T, s.kc, s.kc, true);
     const int mv = batch.add_map(dV_of(i), T, s.kc, s.kc, true);
-    Problem* p = batch.add_problem(h, s.qc, true, true, EPI_BF16, false, true);
-    if (batch.error()) return batch.error();
-    p->out0 = dWq[i];
-    p->ld_out = s.qc;
-    if ((rc = batch.add_seg(p, mx, 0, mq, -1, 0, T))) return rc;
-    p = batch.add_problem(h, s.kc, true, true, EPI_PAIR_BF16, true, true);
+    Problem* p = batch.add_problem(h, s.kc, true, true, EPI_PAIR_BF16, true, true);
     if (batch.error()) return batch.error();
     p->out0 = dWk[i];
     p->out1 = dWv[i];
     p->ld_out = s.kc;
     if ((rc = batch.add_seg(p, mx, 0, mk, mv, 0, T))) return rc;
+  }
+  if ((rc = batch.flush(st))) return rc;
+  for (int i = 0; i < t; ++i) {
+    if (!batch.has_room(2, 1) && (rc = batch.flush(st))) return rc;
+    const int mx = batch.add_map(X, T, h, h, true);
+    const int mq = batch.add_map(dQ_of(i), T, s.qc, s.qc, true);
+    Problem* p = batch.add_problem(h, s.qc, true, true, EPI_BF16, false, true);
+    if (batch.error()) return batch.error();
+    p->out0 = dWq[i];
+    p->ld_out = s.qc;
+    if ((rc = batch.add_seg(p, mx, 0, mq, -1, 0, T))) return rc;
   }
   for (int i = 0; i < t; ++i) {
     const __nv_bfloat16* G[3] = {dQ_of(i), dK_of(i), dV_of(i)};
