@@ -142,3 +142,65 @@ def test_qwen3_8b_swiglu_t8_full_size_sampled():
     for i in range(1, cfg.t):
         assert torch.equal(fwd["Z"][0], fwd["Z"][i])
         assert torch.equal(bwd["dX"][0], bwd["dX"][i])
+
+
+_CHILD = r"""
+import os, sys
+root, out = sys.argv[1], sys.argv[2]
+sys.path[:0] = [root, os.path.join(root, "tests")]
+import torch
+import synth_inputs as si
+import test_gpu_mlp as m
+inp = si.mlp_inputs(520, 392, 640, "swiglu", seed=31)
+fwd, bwd = m._run(inp, "swiglu", 2)
+ce = m._ce_case()
+torch.save({"fwd": {k: [x.cpu() for x in v] for k, v in fwd.items() if isinstance(v, list)},
+            "bwd": {k: [x.cpu() for x in v] for k, v in bwd.items() if isinstance(v, list)},
+            "ce": {k: ([x.cpu() for x in v] if isinstance(v, list) else v.cpu()) for k, v in ce.items() if v is not None}},
+           out)
+"""
+
+
+def _ce_case():
+    """Vocab-parallel CE, t = 2, 600-column shards (fp32 logits and the fused partials take the
+    wide tiles when allowed), ragged T."""
+    import tensor_transformer_layer_way_gb300 as ttl_
+    g = torch.Generator().manual_seed(41)
+    T, h, V = 300, 256, 1200
+    H = torch.randn((T, h), generator=g).to(torch.bfloat16).cuda()
+    W = [(torch.randn((V // 2, h), generator=g) * 0.05).to(torch.bfloat16).cuda() for _ in range(2)]
+    target = torch.randint(0, V, (T,), generator=g).cuda()
+    out = ttl_.vocab_parallel_ce(H, W, target, fused_stats=True)
+    torch.cuda.synchronize()
+    assert ttl_.device_status() == 0
+    return {k: v for k, v in out.items() if k != "ws"}
+
+
+def test_wide_tiles_give_the_same_bits_as_256_column_tiles(tmp_path):
+    """Every GEMM output element is the same chain of K = 16 MMAs whichever tile width the
+    launch uses, rounded once, so the 256x512 tiles (this process) and the 256x256 tiles (a
+    child process with TTL_GEMM_WIDE=0) must agree bit for bit: on a SwiGLU block whose fc1,
+    fc2, weight-gradient and dX launches all qualify for the wide tiles (ragged T = 520), and
+    on a vocab-parallel CE (fp32 logits, the fused partials, the loss, dlogits and dH)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = str(tmp_path / "narrow.pt")
+    env = dict(os.environ, TTL_GEMM_WIDE="0")
+    subprocess.run([sys.executable, "-c", _CHILD, root, out], env=env, check=True, timeout=600)
+    narrow = torch.load(out)
+    inp = si.mlp_inputs(520, 392, 640, "swiglu", seed=31)
+    fwd, bwd = _run(inp, "swiglu", 2)
+    for part, res in (("fwd", fwd), ("bwd", bwd)):
+        for k, lst in narrow[part].items():
+            for i, x in enumerate(lst):
+                assert torch.equal(res[k][i].cpu(), x), f"{part} {k}[{i}] differs between tile widths"
+    ce = _ce_case()
+    for k, v in narrow["ce"].items():
+        got = ce[k]
+        if isinstance(v, list):
+            for i, x in enumerate(v):
+                assert torch.equal(got[i].cpu(), x), f"ce {k}[{i}] differs between tile widths"
+        else:
+            assert torch.equal(got.cpu(), v), f"ce {k} differs between tile widths"
