@@ -2,24 +2,27 @@
 //
 // One launch computes a list of problems (e.g. the t shards of a column-parallel layer,
 // or the t shards' dgrad and wgrad) so that the narrow per-shard GEMMs fill the GPU
-// together.  Work is cut into tiles of TILE_M rows x 256 accumulator columns, walked by
-// persistent workers with a static stride.  Roles (192 threads per CTA):
+// together.  Work is cut into tiles of TILE_M rows x 256 (wide: 512) accumulator columns,
+// walked by persistent workers with a static stride.  Roles (192 threads per CTA; wide: 320):
 //   warp 0      TMA producer: one thread issues cp.async.bulk.tensor loads of this CTA's
 //               A rows and B columns for each 64-wide K block into a shared-memory ring;
 //   warp 1      MMA issuer: allocates 512 TMEM columns (two 128 x 256 fp32 accumulators,
-//               double-buffered) and one thread issues tcgen05.mma per 16-wide K step;
-//   warps 2..5  epilogue: tcgen05.ld the accumulator rows, apply the fused op (bias,
-//               GeLU, SwiGLU, their derivatives) and store bf16/fp32 to global memory.
+//               double-buffered; wide: one 128 x 512) and one thread issues tcgen05.mma per
+//               16-wide K step;
+//   warps 2..   epilogue (4 warps; wide: 8): tcgen05.ld the accumulator rows, apply the fused
+//               op (bias, GeLU, SwiGLU, their derivatives, cross-entropy partials) and store
+//               bf16/fp32 to global memory.
 //
 // Three variants share the code:
 //   single CTA  (PAIR = false): TILE_M = 128, MMA M=128 N=256, 4 stages of 48 KiB.
 //   CTA pair    (PAIR = true) : a cluster of two CTAs on two SMs computes a 256 x 256 tile
 //               with tcgen05.mma.cta_group::2 (M=256 N=256).  Each CTA holds its own 128 A
 //               rows and 128 of the 256 B columns, so the B tile is read from HBM/L2 and
-//               shared memory once per pair; each stage is 32 KiB and 6 stages fit.  Both
+//               shared memory once per pair; each stage is 32 KiB and 7 stages fit.  Both
 //               CTAs' TMA loads complete on the leader CTA's full barrier, the leader alone
 //               issues MMAs, and its commits arrive on both CTAs' barriers (multicast).
-//   wide pair   (WIDE = true) : 256 x 512 tiles for plain bf16 outputs.  Each K step issues two
+//   wide pair   (WIDE = true) : 256 x 512 tiles (bf16, SwiGLU-forward and fp32 outputs, see
+//               launch() for which launches qualify).  Each K step issues two
 //               independent N=256 MMAs into the halves of one 512-column accumulator: MMAs
 //               into one accumulator wait for each other, two chains overlap, and the operand
 //               bytes per MMA drop by a quarter (each stage: 16 KiB of A, 32 KiB of B per CTA,
