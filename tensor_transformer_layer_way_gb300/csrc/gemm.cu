@@ -215,23 +215,6 @@ __device__ __forceinline__ void load_row32_bf16(const void* base, int64_t ld, in
   }
 }
 
-// Asks L2 to fetch this thread's row of the auxiliary inputs an epilogue will read (the
-// saved pre-activations of a backward epilogue), so those loads hit L2 when the tile's
-// accumulator is ready.  One 128-byte line per 64 bf16 columns, over the BN / 2 columns of
-// this warp's half of the tile.
-__device__ __forceinline__ void prefetch_aux_row(const Problem& pr, int row, int n_base) {
-  if (pr.epi != EPI_GELU_BWD && pr.epi != EPI_SWIGLU_BWD) return;
-  if (row >= pr.M) return;
-#pragma unroll
-  for (int c = 0; c < BN / 2; c += 64) {
-    if (n_base + c >= pr.N) break;
-    const int64_t off = static_cast<int64_t>(row) * pr.ld_aux + n_base + c;
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const __nv_bfloat16*>(pr.aux0) + off));
-    if (pr.epi == EPI_SWIGLU_BWD)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const __nv_bfloat16*>(pr.aux1) + off));
-  }
-}
-
 // Per-row state an epilogue carries across the chunks of one tile.
 struct EpiState {
   float m = -INFINITY, s = 0.0f;   // EPI_F32_CE: running max and sum
@@ -944,25 +927,16 @@ __global__ void __launch_bounds__(Cfg<PAIR, WIDE>::THREADS, 1) gemm_tcgen05_kern
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint32_t tempty_leader0 = PAIR ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
-    const int my_row0 = static_cast<int>(rank) * 128 + row_in_tile;
-    int gi = 0, gi_next = 0;
-    if (unit < P.total_tiles) {
-      const TileCoord c0 = decode_tile_s(*sched, unit, gi_next);
-      for (int half = 0; half < 2; ++half)
-        prefetch_aux_row(P.probs[c0.p], c0.tm * C::TILE_M + my_row0, c0.tn * BN + half * (BN / 2));
-    }
+    // (The saved pre-activations of a backward epilogue are not prefetched to L2 a tile
+    // ahead: measured on the fc2 dgrad, the prefetches added 0.5 GB of DRAM reads, lines
+    // evicted before use, and made the launch 2% slower.)
+    int gi = 0;
     for (int tile = unit; tile < P.total_tiles; tile += nunits) {
       const TileCoord c = decode_tile_s(*sched, tile, gi);
       const Problem& pr = P.probs[c.p];
       const bool ready = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
-      // The next tile's auxiliary rows travel to L2 while this tile's epilogue runs.
-      if (tile + nunits < P.total_tiles) {
-        const TileCoord cn = decode_tile_s(*sched, tile + nunits, gi_next);
-        for (int half = 0; half < 2; ++half)
-          prefetch_aux_row(P.probs[cn.p], cn.tm * C::TILE_M + my_row0, cn.tn * BN + half * (BN / 2));
-      }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const int row = c.tm * C::TILE_M + static_cast<int>(rank) * 128 + row_in_tile;
       for (int half = 0; half < 2; ++half) epilogue_tile(pr, tbase, row, c.tn * (BN / 2), c.tn * BN, half);
