@@ -595,15 +595,21 @@ struct BwdParams {
 template <int D>
 struct BwdCfg {
   static constexpr int KB = D / 64;
+  static constexpr int RING = 5;                          // V / K slots
   static constexpr int A_BYTES = KB * kBQ * 128;          // the dO tile
   static constexpr int SLOT = KB * kBKV * 128;            // a V tile or a K tile
-  static constexpr int P_BYTES = kBQ * kBKV * 2;          // a P tile, overwritten in place by dS
+  static constexpr int P_BYTES = kBQ * kBKV * 2;          // a P tile, read by the dS warps alone
   static constexpr int OFF_A = 0;
   static constexpr int OFF_RING = OFF_A + A_BYTES;
-  static constexpr int OFF_P = OFF_RING + kRing * SLOT;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_P = OFF_RING + RING * SLOT;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+  // tensor memory: two dP buffers, the dQ accumulator, two dS buffers (bf16, keys 2i and 2i + 1
+  // in column i: the A operand of dQ += dS K)
+  static constexpr int T_DQ = 2 * kBKV;
+  static constexpr int T_DS = 2 * kBKV + D;
+  static_assert(T_DS + 2 * (kBKV / 2) <= kTmemCols, "tensor memory layout");
 };
 
 // Asks L2 to fetch one box ahead of its load (HBM latency hidden without shared memory).
@@ -625,12 +631,14 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
 
 // dQ: for every (shard, query head, 128-query tile) over the key tiles 0..qt (128 keys each):
 //   dP_j = dO_c V_j^T (tcgen05, TMEM); the P_j tile arrives by TMA into a shared buffer; the
-//   softmax warps overwrite it in place (each thread its own row) with
-//   dS_j = P_j (dP_j - D) / sqrt(d) (P is zero above the diagonal, so is dS), and
-//   dQ += dS_j K_j accumulates in TMEM.  dQ is stored at the end.
-// Roles (352 threads): warp 0 loads dO, then V_j / K_j through the 4-slot ring; warp 10 loads
-// the P tiles into the two P buffers; warp 1 issues the MMAs (dP_j, then dQ_(j-1)); warps 2..9
-// compute dS, two per TMEM lane quadrant.
+//   dS warps read it (each thread its own row) and write dS_j = P_j (dP_j - D) / sqrt(d) (P is
+//   zero above the diagonal, so is dS) into tensor memory, where dQ += dS_j K_j reads it as the
+//   A operand.  dQ accumulates in TMEM and is stored at the end.  The P tile is free as soon as
+//   the dS warps hold it in registers, so one buffer suffices, and the shared memory it saves
+//   holds a fifth V / K slot: the ring's loads get more lead.
+// Roles (352 threads): warp 0 loads dO, then V_j / K_j through the 5-slot ring; warp 10 loads
+// the P tiles; warp 1 issues the MMAs (dP_j, then dQ_(j-1)); warps 2..9 compute dS, two per
+// TMEM lane quadrant.
 template <int D>
 __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __grid_constant__ BwdParams P) {
   using C = BwdCfg<D>;
@@ -641,13 +649,14 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
   uint8_t* sP = smem + C::OFF_P;
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* ring_full = a_full + 1;
-  uint64_t* ring_empty = ring_full + kRing;
-  uint64_t* dp_full = ring_empty + kRing;
+  uint64_t* ring_empty = ring_full + C::RING;
+  uint64_t* dp_full = ring_empty + C::RING;
   uint64_t* dp_empty = dp_full + 2;
-  uint64_t* pb_full = dp_empty + 2;
-  uint64_t* pb_empty = pb_full + 2;
-  uint64_t* ds_full = pb_empty + 2;
-  uint64_t* dq_full = ds_full + 2;
+  uint64_t* pb_full = dp_empty + 2;            // the P tile in shared memory
+  uint64_t* pb_empty = pb_full + 1;
+  uint64_t* ds_full = pb_empty + 1;            // [2] dS in tensor memory
+  uint64_t* ds_empty = ds_full + 2;            // [2]
+  uint64_t* dq_full = ds_empty + 2;
   uint64_t* done_bar = dq_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -667,17 +676,18 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
 
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
-    for (int s = 0; s < kRing; ++s) {
+    for (int s = 0; s < C::RING; ++s) {
       mbar_init(&ring_full[s], 1);
       mbar_init(&ring_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dp_full[b], 1);
       mbar_init(&dp_empty[b], 8);
-      mbar_init(&pb_full[b], 1);
-      mbar_init(&pb_empty[b], 1);   // the dQ MMAs have read dS
       mbar_init(&ds_full[b], 8);
+      mbar_init(&ds_empty[b], 1);   // the dQ MMAs have read dS
     }
+    mbar_init(pb_full, 1);
+    mbar_init(pb_empty, 8);         // the eight dS warps have read the P tile
     mbar_init(dq_full, 1);
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -706,8 +716,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
       for (int kb = 0; kb < C::KB; ++kb) tma_load_2d(sA + kb * 16384, &P.dO[shard], a_full, c * D + kb * 64, q0);
       int issued = 0;
       for (int pos = 0; ok && pos < 2 * ntiles; ++pos) {
-        const int slot = pos % kRing;
-        if (!mbar_wait(&ring_empty[slot], (static_cast<uint32_t>(pos / kRing) & 1u) ^ 1u, abort_flag, status, tmo)) {
+        const int slot = pos % C::RING;
+        if (!mbar_wait(&ring_empty[slot], (static_cast<uint32_t>(pos / C::RING) & 1u) ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
@@ -727,9 +737,9 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
       }
       int dummy_abort = 0;
       mbar_wait(a_full, 0, reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
-      const int pending = issued < kRing ? issued : kRing;
+      const int pending = issued < C::RING ? issued : C::RING;
       for (int i = issued - pending; i < issued; ++i)
-        mbar_wait(&ring_full[i % kRing], static_cast<uint32_t>(i / kRing) & 1u,
+        mbar_wait(&ring_full[i % C::RING], static_cast<uint32_t>(i / C::RING) & 1u,
                   reinterpret_cast<volatile int*>(&dummy_abort), status, tmo);
     }
     __syncwarp();
@@ -743,31 +753,25 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
         tma_prefetch_3d(&P.p[shard], j * kBKV + 64, q0, c);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        const int b = j & 1;
         if (j + 2 < ntiles) {   // two tiles ahead into L2
           tma_prefetch_3d(&P.p[shard], (j + 2) * kBKV, q0, c);
           tma_prefetch_3d(&P.p[shard], (j + 2) * kBKV + 64, q0, c);
         }
-        if (!mbar_wait(&pb_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo)) {
+        if (!mbar_wait(pb_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag, status, tmo)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&pb_full[b], C::P_BYTES);
-        tma_load_3d(sP + b * C::P_BYTES, &P.p[shard], &pb_full[b], j * kBKV, q0, c);
-        tma_load_3d(sP + b * C::P_BYTES + 16384, &P.p[shard], &pb_full[b], j * kBKV + 64, q0, c);
+        mbar_arrive_expect_tx(pb_full, C::P_BYTES);
+        tma_load_3d(sP, &P.p[shard], pb_full, j * kBKV, q0, c);
+        tma_load_3d(sP + 16384, &P.p[shard], pb_full, j * kBKV + 64, q0, c);
         ++started;
       }
-      // No copy may still be landing when the CTA leaves: wait (bounded) for the latest phase of
-      // each buffer.  Only the latest: a parity wait on a phase the barrier has since passed
-      // twice would never see it complete.  An earlier load on a buffer completed before the
-      // buffer could be reused.
+      // No copy may still be landing when the CTA leaves: wait (bounded) for the latest load (an
+      // earlier one completed before the buffer could be reused).
       int dummy_abort = 0;
-      for (int b = 0; b < 2; ++b) {
-        const int jl = started - 1 - ((started - 1 - b) & 1);   // last started tile on buffer b
-        if (jl >= 0)
-          mbar_wait(&pb_full[b], static_cast<uint32_t>(jl >> 1) & 1u, reinterpret_cast<volatile int*>(&dummy_abort),
-                    status, tmo);
-      }
+      if (started > 0)
+        mbar_wait(pb_full, static_cast<uint32_t>(started - 1) & 1u, reinterpret_cast<volatile int*>(&dummy_abort),
+                  status, tmo);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -777,12 +781,11 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
       tc_fence_after_sync();
       const uint64_t dod = smem_desc_sw128(smem_u32(sA), 16, 1024);   // the dO tile (A of dP)
       const uint32_t ring0 = smem_u32(sRing);
-      const uint32_t paddr = smem_u32(sP);
       const uint32_t idesc_dp = idesc_bf16_f32(kBQ, kBKV, false, false);
       const uint32_t idesc_dq = idesc_bf16_f32(kBQ, D, false, true);
       auto wait_pos = [&](int pos) {
-        const int slot = pos % kRing;
-        if (!mbar_wait(&ring_full[slot], static_cast<uint32_t>(pos / kRing) & 1u, abort_flag, status, tmo))
+        const int slot = pos % C::RING;
+        if (!mbar_wait(&ring_full[slot], static_cast<uint32_t>(pos / C::RING) & 1u, abort_flag, status, tmo))
           return -1;
         tc_fence_after_sync();
         return slot;
@@ -818,18 +821,17 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
             break;
           }
           tc_fence_after_sync();
-          const uint64_t pd = smem_desc_sw128(paddr + b * C::P_BYTES, 16, 1024);
           const uint64_t kd = smem_desc_sw128(ring0 + kslot * C::SLOT, 8192, 1024);
+          const uint32_t t_ds = tmem_base + C::T_DS + b * (kBKV / 2);
           for (int kk2 = 0; kk2 < 2; ++kk2) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = desc_advance(pd, kk2 * 16384 + kk * 32);
+            for (int kk = 0; kk < 4; ++kk) {   // keys 64 kk2 + 16 kk .. +15: dS columns 32 kk2 + 8 kk
               const uint64_t bd = desc_advance(kd, kk2 * C::KB * 8192 + kk * 2048);
-              umma_bf16(tmem_base + 2 * kBKV, ad, bd, idesc_dq, (jp | kk2 | kk) ? 1u : 0u);
+              umma_bf16_ts(tmem_base + C::T_DQ, t_ds + kk2 * 32 + kk * 8, bd, idesc_dq, (jp | kk2 | kk) ? 1u : 0u);
             }
           }
           umma_commit(&ring_empty[kslot]);
-          umma_commit(&pb_empty[b]);                 // the MMAs have read dS: the buffer is free
+          umma_commit(&ds_empty[b]);                 // the MMAs have read dS_(j-1)
         }
       }
       if (ok) umma_commit(dq_full);
@@ -849,7 +851,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
     const float scale = P.scale;
     const uint64_t nDs2 = f2_pack(-Dq * scale, -Dq * scale), scale2 = f2_pack(scale, scale);
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
+    const uint8_t* my_row = sP + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = true;
     for (int j = 0; ok && j < ntiles; ++j) {
       const int b = j & 1;
@@ -866,32 +868,45 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&dp_empty[b]);
-      ok = mbar_wait(&pb_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status, tmo);
+      ok = mbar_wait(pb_full, static_cast<uint32_t>(j) & 1u, abort_flag, status, tmo);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      uint8_t* row = my_row + b * C::P_BYTES;
+      uint32_t pv[32];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        uint4* unit = reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4));
-        const uint4 pw = *unit;
-        const uint32_t pv[4] = {pw.x, pw.y, pw.z, pw.w};
-        // dS = (dP scale - D scale) P, two columns per packed fp32 instruction (one fma and one
-        // multiply per pair).  P is zero above the diagonal.
-        uint32_t o4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = u * 8 + 2 * e;
-          const uint64_t dp2 = f2_pack(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]),
-                                       __uint_as_float(col < 32 ? r0[col + 1] : r1[col - 31]));
-          const uint64_t p2 = f2_pack(bf16_lo(pv[e]), bf16_hi(pv[e]));
-          const float2 d2 = f2_unpack(fmul2(ffma2(dp2, scale2, nDs2), p2));
-          o4[e] = pack_bf16x2(d2.x, d2.y);
-        }
-        *unit = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        const uint4 pw = *reinterpret_cast<const uint4*>(my_row + ((u ^ (r & 7)) << 4));
+        pv[4 * u] = pw.x;
+        pv[4 * u + 1] = pw.y;
+        pv[4 * u + 2] = pw.z;
+        pv[4 * u + 3] = pw.w;
       }
-      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pb_empty);   // P_j is in registers: the tile may be refilled
+      // dS = (dP scale - D scale) P, two columns per packed fp32 instruction (one fma and one
+      // multiply per pair).  P is zero above the diagonal.
+      uint32_t ds[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int col = 2 * e;
+        const uint64_t dp2 = f2_pack(__uint_as_float(col < 32 ? r0[col] : r1[col - 32]),
+                                     __uint_as_float(col < 32 ? r0[col + 1] : r1[col - 31]));
+        const uint64_t p2 = f2_pack(bf16_lo(pv[e]), bf16_hi(pv[e]));
+        const float2 d2 = f2_unpack(fmul2(ffma2(dp2, scale2, nDs2), p2));
+        ds[e] = pack_bf16x2(d2.x, d2.y);
+      }
+      if (j >= 2) {
+        ok = mbar_wait(&ds_empty[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status, tmo);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+      }
+      tmem_st_32x32b_x32(lane_base + C::T_DS + b * (kBKV / 2) + half * 32, ds);
+      tmem_st_wait();
+      tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[b]);
     }
@@ -902,7 +917,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_core_kernel(const __
 #pragma unroll
       for (int cc = 0; cc < D / 2; cc += 32) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(lane_base + 2 * kBKV + half * (D / 2) + cc, o);
+        tmem_ld_32x32b_x32(lane_base + C::T_DQ + half * (D / 2) + cc, o);
         tmem_ld_wait();
         if (row_ok) {
 #pragma unroll
