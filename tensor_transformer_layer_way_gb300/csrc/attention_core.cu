@@ -974,7 +974,7 @@ struct KvCfg {
 };
 
 // dK and dV: for every (shard, KV head g, 128-key tile kt), over the pairs (query head c of the
-// group, query tile qt >= kt), with the queries as rows of every score tile:
+// group, query tile qt >= kt, the last tile first), with the queries as rows of every score tile:
 //   dP = dO_c V^T (TMEM); the saved P tile arrives by TMA; dV += P^T dO_c reads it as an
 //   MN-major operand; the softmax warps then overwrite it in place with
 //   dS = P (dP - D) / sqrt(d) (zero above the diagonal, where P is zero); dK += dS^T Q_c.
@@ -1063,8 +1063,11 @@ __global__ void __launch_bounds__(kCoreThreads, 1) attn_bwd_kv_kernel(const __gr
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Query-tile row and query head of pair j.
-  auto pair_row = [&](int j) { return (kt + j / P.grp) * kBQ; };
+  // Query-tile row and query head of pair j.  The query tiles run from the last one down to kt:
+  // every CTA of a shard then reads the same dO and Q tiles at about the same time, whatever its
+  // key tile, and finds most of them in L2 (dK/dV core 0.736 -> 0.723 ms at the Qwen3 shape
+  // against the upward order).
+  auto pair_row = [&](int j) { return (P.ntq - 1 - j / P.grp) * kBQ; };
   auto pair_head = [&](int j) { return g * P.grp + j % P.grp; };
 
   if (warp == 0) {
