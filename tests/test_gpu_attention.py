@@ -177,6 +177,29 @@ def test_single_cta_tiles_in_a_child_process():
     assert "3 passed" in r.stdout, r.stdout[-2000:]
 
 
+def test_repeatable_bit_for_bit():
+    """Three runs on the same inputs give the same bits in every output: a shape with several
+    waves of CTAs in each core (the forward and dQ cores 512 CTAs, the dK/dV core 128), so a race
+    between a core's roles or its CTAs would show as a difference between runs."""
+    t, T, h, n_q, n_kv, d = 8, 2048, 1024, 32, 8, 128
+    inp = si.attn_inputs(T, h, n_q, n_kv, d, seed=11)
+    runs = [_run(inp, t, n_q, n_kv, d) for _ in range(3)]
+    f0, b0 = runs[0]
+    j = torch.arange(T, device=f0["P"][0].device)
+    written = j[None, :] < torch.clamp((j[:, None] // 128 + 1) * 128, max=T)   # P's stored band
+    for fwd, bwd in runs[1:]:
+        for k in ("Q", "K", "V", "O", "Y"):
+            for i in range(t):
+                assert torch.equal(fwd[k][i], f0[k][i]), f"{k}[{i}] differs between runs"
+        for i in range(t):
+            assert torch.equal(fwd["P"][i][:, written], f0["P"][i][:, written]), f"P[{i}] differs between runs"
+        for k in ("dWq", "dWk", "dWv", "dWo", "dX"):
+            for i in range(t):
+                assert torch.equal(bwd[k][i], b0[k][i]), f"{k}[{i}] differs between runs"
+    del runs, f0, b0
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ Qwen3-8B shape, t = 8
 
 @pytest.fixture(scope="module")
