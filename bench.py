@@ -536,18 +536,29 @@ def bench_gtp(ttl, torch, dev, pk, args):
         if ga:
             res[key]["gather_gbs"] = round(sum(r[3] for r in ga) / (sum(r[1] for r in ga) * 1e-3) / 1e9, 1)
     # The gather kernel alone (in the chain it shares HBM with the GEMM it hides behind): the
-    # L layers' shards gathered back to back into L distinct slots on this stream (512 MiB of
-    # traffic, beyond L2), L2 flushed before each repetition, median of 5.
+    # L layers' shards gathered back to back into L distinct slots (512 MiB of traffic, beyond
+    # L2), L2 flushed before each repetition, median of 5.  The L launches are replayed from a
+    # CUDA graph: issued one by one from Python they arrive about 13.7 us apart, slower than
+    # the kernel runs, and the measurement would time the host's launch rate.
     flush = [torch.zeros(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev) for _ in range(2)]
     dst = [torch.empty((K, N), device=dev, dtype=torch.bfloat16) for _ in range(L)]
     gather_bytes = L * 2.0 * K * N * 2
+    for l in range(L):   # first calls outside the capture (one-time host set-up)
+        ttl.gtp_gather(shards[l], dst[l])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    g_gather = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_gather, stream=side):
+        for l in range(L):
+            ttl.gtp_gather(shards[l], dst[l])
+    torch.cuda.synchronize()
     times = []
     for _ in range(5):
         _flush(torch, flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for l in range(L):
-            ttl.gtp_gather(shards[l], dst[l])
+        g_gather.replay()
         e1.record()
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
@@ -555,22 +566,29 @@ def bench_gtp(ttl, torch, dev, pk, args):
     # the same bytes moved by torch's own device copy (one contiguous [K, N] source per layer),
     # timed the same way: the ceiling for copies of this size
     src = [torch.empty((K, N), device=dev, dtype=torch.bfloat16) for _ in range(L)]
+    g_copy = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_copy, stream=side):
+        for l in range(L):
+            dst[l].copy_(src[l])
+    torch.cuda.synchronize()
     ctimes = []
     for _ in range(5):
         _flush(torch, flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for l in range(L):
-            dst[l].copy_(src[l])
+        g_copy.replay()
         e1.record()
         torch.cuda.synchronize()
         ctimes.append(e0.elapsed_time(e1))
     cms = sorted(ctimes)[len(ctimes) // 2]
+    del g_gather, g_copy
     res["gather_isolated"] = {"us_per_layer": round(ms * 1e3 / L, 1),
                               "gbs": round(gather_bytes / (ms * 1e-3) / 1e9, 1),
                               "frac": round(gather_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                               "torch_copy_same_bytes_gbs": round(gather_bytes / (cms * 1e-3) / 1e9, 1),
-                              "bytes": gather_bytes, "l2": "flushed before each repetition of the 8 launches"}
+                              "bytes": gather_bytes, "l2": "flushed before each repetition of the 8 launches",
+                              "timing": "the 8 launches replayed from a CUDA graph (device time; issued one by one "
+                                        "from Python they run at the host's launch rate, about 13.7 us per call)"}
     del flush, dst, src
     res["roofline"] = pending("tensor", "gemm_tcgen05_kernel", res["slot_prefetch_all_on_compute_stream"]["gemm_tflops"],
                               path="GEMM launches of the slot_prefetch chain with every launch on the compute "
