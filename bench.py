@@ -507,15 +507,20 @@ def bench_gtp(ttl, torch, dev, pk, args):
     for key, folded, fin, wgs in (("slot_prefetch", False, True, True), ("folded", True, True, True),
                                   ("slot_prefetch_wgrad_on_compute_stream", False, True, False),
                                   ("slot_prefetch_all_on_compute_stream", False, False, False)):
-        ttl.trace_enable(True, 1 << 14)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # the wall time untraced (an event pair around every launch costs about 1%), then the
+        # per-launch durations from a traced pass of the same passes
         reps = 3
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(reps):
             fwd_bwd(folded, fin, wgs)
         e1.record()
         torch.cuda.synchronize()
         wall = e0.elapsed_time(e1) / reps
+        ttl.trace_enable(True, 1 << 14)
+        for _ in range(reps):
+            fwd_bwd(folded, fin, wgs)
+        torch.cuda.synchronize()
         recs = ttl.trace_read(1 << 14)
         ttl.trace_enable(False)
         gm = [r for r in recs if r[0] == "gemm"]
@@ -614,16 +619,20 @@ def bench_ce(ttl, torch, dev, pk, args):
             ttl.vocab_parallel_ce(H, W, target, out=out, fused_stats=fused)
         torch.cuda.synchronize()
         reps = 3
-        ttl.trace_enable(True, 4096)
+        # the wall time untraced, then the per-launch durations from a traced pass
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(reps):
             ttl.vocab_parallel_ce(H, W, target, out=out, fused_stats=fused)
         e1.record()
         torch.cuda.synchronize()
+        wall = e0.elapsed_time(e1) / reps
+        ttl.trace_enable(True, 4096)
+        for _ in range(reps):
+            ttl.vocab_parallel_ce(H, W, target, out=out, fused_stats=fused)
+        torch.cuda.synchronize()
         recs = ttl.trace_read(4096)
         ttl.trace_enable(False)
-        wall = e0.elapsed_time(e1) / reps
 
         def agg(kind, flops=False):
             rr = [r for r in recs if r[0] == kind]
@@ -674,16 +683,20 @@ def bench_sp_mlp(ttl, torch, dev, pk, args):
         step()
     torch.cuda.synchronize()
     n = max(10, min(args.steps, 50))
-    ttl.trace_enable(True, 1 << 14)
+    # the wall time untraced, then the per-launch durations from a traced pass
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(n):
         step()
     e1.record()
     torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    ttl.trace_enable(True, 1 << 14)
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
     recs = ttl.trace_read(1 << 14)
     ttl.trace_enable(False)
-    ms = e0.elapsed_time(e1) / n
     gm = [r for r in recs if r[0] == "gemm"]
     res = {"workload": "qwen3_8b_swiglu_mlp_t8_T8192_sequence_parallel_fwd_bwd", "ms_per_step": round(ms, 4),
            "tflops": round(MLP_FLOPS / (ms * 1e-3) / 1e12, 1),
@@ -764,16 +777,20 @@ def bench_attention(ttl, torch, dev, pk, args):
         step()
     torch.cuda.synchronize()
     n = max(5, min(args.steps, 20))
-    ttl.trace_enable(True, 1 << 14)
+    # the wall time untraced, then the per-launch durations from a traced pass
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(n):
         step()
     e1.record()
     torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    ttl.trace_enable(True, 1 << 14)
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
     recs = ttl.trace_read(1 << 14)
     ttl.trace_enable(False)
-    ms = e0.elapsed_time(e1) / n
     flops = sum(r[2] for r in recs) / n        # algorithmic: causal contractions count their triangle
     gm = [r for r in recs if r[0] == "gemm"]
     co = [r for r in recs if r[0] == "attn_core"]
